@@ -1,0 +1,134 @@
+// Memory-bound helper kernels of libmxa2a: scale-factor packing, the unfused
+// pack of A, the split-K reduction and the benchmark's L2 flush.
+//
+// Scale-factor "atom" layout used by the MMA: for every 128-wide K block and
+// every group of 128 rows (of A) or columns (of B), 512 bytes in which the 4
+// E8M0 bytes of row/column x (one per 32-wide K sub-block, in K order) sit as
+// one 32-bit word at word index (x % 32) * 4 + (x % 128) / 32.  Copied to TMEM
+// with tcgen05.cp 32x128b.warpx4, word (x%32)*4 + c lands in column c of lane
+// x%32 (of every lane quarter), which is where the block-scaled MMA reads the
+// scale of row/column 32c + x%32.  The pages' scale operands are the E8M0
+// tensors scaleA / scaleB (all_to_all_matmul_impl.h, LayoutScaleA/B with byte
+// pairs SCALE_C0 = 2): the same bytes in the hardware's own order.
+#include <cuda_bf16.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace mxa2a {
+
+__device__ __forceinline__ size_t atom_word(int kbg, int groups, int x) {
+    return ((size_t)kbg * groups + (size_t)(x >> 7)) * (kSfAtomBytes / 4) + (size_t)((x & 31) * 4 + ((x & 127) >> 5));
+}
+
+// B_scale [N][K/32] -> atoms [K/128][Ng2][512]; columns N..Ng2*128 get 0.
+__global__ void pack_sfb_kernel(const uint8_t* __restrict__ B_scale, int N, int K, int Ng2, uint32_t* __restrict__ sfb) {
+    const int kbs = K / BK;
+    const long long total = (long long)kbs * Ng2 * 128;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int n = (int)(i % (Ng2 * 128));
+        const int kbg = (int)(i / (Ng2 * 128));
+        uint32_t v = 0;
+        if (n < N) v = ptx::ld_nc_u32(B_scale + (size_t)n * (K / 32) + (size_t)kbg * 4);
+        sfb[atom_word(kbg, Ng2, n)] = v;
+    }
+}
+
+// Unfused variant: A_packed[m][r*ka + k] = A_seg[r][m][k] (the segments
+// concatenated along K), and the A scales into atoms [K/128][Mg][512].
+__global__ void pack_a_kernel(const __grid_constant__ GemmParams p, uint8_t* __restrict__ a_packed) {
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    const int v_per_row = p.K / 16;
+    const long long nvec = (long long)p.M * v_per_row;
+    for (long long i = tid; i < nvec; i += stride) {
+        const int m = (int)(i / v_per_row);
+        const int k = (int)(i - (long long)m * v_per_row) * 16;
+        const int r = k / p.ka;
+        const int kin = k - r * p.ka;
+        const uint4 v = ptx::ld_nc_v4(p.A_seg[r] + (size_t)m * p.ka + kin);
+        *reinterpret_cast<uint4*>(a_packed + (size_t)m * p.K + k) = v;
+    }
+    const int kbs = p.K / BK;
+    const long long nsf = (long long)kbs * p.Mg * 128;
+    uint32_t* sfa = reinterpret_cast<uint32_t*>(p.sfa_stage);
+    for (long long i = tid; i < nsf; i += stride) {
+        const int m = (int)(i % (p.Mg * 128));
+        const int kbg = (int)(i / (p.Mg * 128));
+        uint32_t v = 0;
+        if (m < p.M) {
+            const int r = kbg / p.kb_per_seg;
+            const int kb = kbg - r * p.kb_per_seg;
+            v = ptx::ld_nc_u32(p.A_sf_seg[r] + (size_t)m * (p.ka / 32) + (size_t)kb * 4);
+        }
+        sfa[atom_word(kbg, p.Mg, m)] = v;
+    }
+}
+
+// C = bf16(sum_q partial[q]) in the fixed order q = 0..S-1.
+__global__ void splitk_reduce_kernel(const float* __restrict__ partial, int S, long long MN, uint16_t* __restrict__ C) {
+    const long long n4 = MN / 4;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
+         i += (long long)gridDim.x * blockDim.x) {
+        float4 acc = reinterpret_cast<const float4*>(partial)[i];
+        for (int q = 1; q < S; ++q) {
+            const float4 v = reinterpret_cast<const float4*>(partial + (size_t)q * MN)[i];
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 out;
+        out.x = *reinterpret_cast<const uint32_t*>(&lo);
+        out.y = *reinterpret_cast<const uint32_t*>(&hi);
+        reinterpret_cast<uint2*>(C)[i] = out;
+    }
+}
+
+__global__ void l2_flush_kernel(uint4* buf, long long n16) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n16;
+         i += (long long)gridDim.x * blockDim.x) {
+        uint4 v = buf[i];
+        v.x += 1u;
+        buf[i] = v;
+    }
+}
+
+static int grid_for(long long work, int threads) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    long long g = (work + threads - 1) / threads;
+    const long long cap = (long long)sms * 8;
+    if (g > cap) g = cap;
+    if (g < 1) g = 1;
+    return (int)g;
+}
+
+cudaError_t launch_pack_sfb(const uint8_t* B_scale, int N, int K, int Ng2, uint8_t* sfb, cudaStream_t stream) {
+    const long long total = (long long)(K / BK) * Ng2 * 128;
+    pack_sfb_kernel<<<grid_for(total, 256), 256, 0, stream>>>(B_scale, N, K, Ng2, reinterpret_cast<uint32_t*>(sfb));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_a(const GemmParams& p, uint8_t* a_packed, int grid, cudaStream_t stream) {
+    const long long work = (long long)p.M * p.K / 16;
+    pack_a_kernel<<<grid > 0 ? grid : grid_for(work, 256), 256, 0, stream>>>(p, a_packed);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_reduce(const float* partial, int S, long long MN, uint16_t* C, cudaStream_t stream) {
+    splitk_reduce_kernel<<<grid_for(MN / 4, 256), 256, 0, stream>>>(partial, S, MN, C);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t stream) {
+    const long long n16 = (long long)(bytes / 16);
+    l2_flush_kernel<<<grid_for(n16, 256), 256, 0, stream>>>(reinterpret_cast<uint4*>(buf), n16);
+    return cudaGetLastError();
+}
+
+}  // namespace mxa2a

@@ -1,0 +1,94 @@
+// Shared declarations between the CUDA kernels and the C-ABI host layer of
+// libmxa2a (fused AllToAll + MXFP8 block-scaled GEMM on sm_103a).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mxa2a {
+
+constexpr int kMaxSegments = 64;   // R limit (segment pointer tables live in kernel params)
+
+// GEMM tile: 128 rows (M) x 256 columns (N), 128-byte (= 128 FP8) K blocks.
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;
+constexpr int kStages = 4;
+constexpr int kThreads = 256;      // 8 warps, roles below
+constexpr int kWarpTma = 0;        // TMA producer (one elected lane)
+constexpr int kWarpMma = 1;        // TMEM allocator + MMA issuer (one elected lane)
+constexpr int kWarpEpi0 = 2;       // warps 2..5: epilogue, one TMEM lane quarter each
+constexpr int kWarpCopy0 = 6;      // warps 6..7: staging copy (fused kernel only)
+constexpr int kCopyThreads = 64;
+
+constexpr int kAStageBytes = BM * BK;        // 16 KiB
+constexpr int kBStageBytes = BN * BK;        // 32 KiB
+constexpr int kSfAtomBytes = 512;            // 128 rows x 4 E8M0 bytes (one 128-K block)
+constexpr int kSfaStageBytes = kSfAtomBytes;
+constexpr int kSfbStageBytes = 2 * kSfAtomBytes;
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemAccCol = 0;          // 256 fp32 accumulator columns
+constexpr uint32_t kTmemSfCol = 256;         // per stage: 4 SFA + 8 SFB columns
+constexpr uint32_t kTmemSfColsPerStage = 12;
+
+// Device error codes written to the status block (same numbers as the C ABI).
+constexpr int kErrTimeout = 6;
+constexpr int kErrDeviceCheck = 8;
+
+// Role ids recorded with a device error.
+constexpr int kRoleCopy = 1, kRoleTma = 2, kRoleMma = 3, kRoleEpi = 4, kRoleExit = 5;
+
+struct DevStatus {
+    unsigned long long key;   // (launch_id << 8) | code, first error of a launch wins
+    int role, block, step, segment, slot, pad;
+    long long observed, expected;
+};
+
+// Monotonic credit counters of the staging ring, each on its own 128-byte line.
+// filled[slot][r]: staging copy chunks published for (slot, segment)
+// drained[slot]:   GEMM work items that finished reading the slot
+// cta_done:        CTAs that reached the end (the last one zeroes everything)
+struct FlagLayout {
+    static constexpr int kLine = 16;  // 16 x u64 = 128 bytes
+    __host__ __device__ static size_t filled(int slot, int r, int R) { return (size_t)(slot * R + r) * kLine; }
+    __host__ __device__ static size_t drained(int slot, int bn, int R) { return (size_t)(bn * R + slot) * kLine; }
+    __host__ __device__ static size_t cta_done(int bn, int R) { return (size_t)(bn * R + bn) * kLine; }
+    __host__ __device__ static size_t words(int bn, int R) { return (size_t)(bn * R + bn + 1) * kLine; }
+};
+
+struct GemmParams {
+    int R, M, N, ka, K, cm, bn, steps;
+    int Mt, Nt, S, W;           // m-tiles, n-tiles, K splits, work items
+    int kb_per_seg;             // ka / 128
+    int Mg, Ng2;                // 128-row groups of A (scale atoms), 128-col groups of B (padded to 256)
+    int box_m;                  // rows per A TMA box: 128 or 64
+    int zigzag, rotate;
+    const uint8_t* sfa;         // A scales, MMA atom layout [K/128][Mg][512]
+    const uint8_t* sfb;         // B scales, MMA atom layout [K/128][Ng2][512]
+    uint16_t* C;                // bf16 [M][N] (S == 1)
+    float* partial;             // fp32 [S][M][N] (S > 1)
+    // fused staging
+    int fused, exchange_only;
+    int rows_per_chunk, chunks_per_seg, n_copy_tasks;
+    int fault_skip_step;        // test knob: never publish the fill of this step (-1 = off)
+    uint8_t* ring;              // [bn][R][cm][ka]
+    uint8_t* sfa_stage;         // writable alias of sfa (staged by the copy role)
+    unsigned long long* flags;
+    DevStatus* status;
+    unsigned long long launch_id;
+    long long timeout_ns;
+    const uint8_t* A_seg[kMaxSegments];
+    const uint8_t* A_sf_seg[kMaxSegments];
+};
+
+// Launchers (mxgemm.cu / aux_kernels.cu).  All return cudaError_t of the launch.
+cudaError_t launch_mxgemm(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, int grid,
+                          bool fused, cudaStream_t stream);
+size_t mxgemm_smem_bytes();
+cudaError_t launch_pack_a(const GemmParams& p, uint8_t* a_packed, int grid, cudaStream_t stream);
+cudaError_t launch_pack_sfb(const uint8_t* B_scale, int N, int K, int Ng2, uint8_t* sfb, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const float* partial, int S, long long MN, uint16_t* C, cudaStream_t stream);
+cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t stream);
+
+}  // namespace mxa2a

@@ -1,0 +1,580 @@
+// C ABI of libmxa2a: plan creation and validation, workspace, TMA
+// descriptors, launch sequencing and status.  Host code only; the kernels
+// are in mxgemm.cu and aux_kernels.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "../../include/mxa2a.h"
+#include "kernels.cuh"
+
+using namespace mxa2a;
+
+namespace {
+
+thread_local int g_last_error = MXA2A_OK;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2D uint8 tensor [outer][inner] (inner contiguous), box [box_outer][128], 128-byte swizzle.
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int tile_span(int64_t M, int64_t cm) {
+    // the most staging steps any 128-row output tile touches
+    int span = 1;
+    const int64_t Mt = (M + BM - 1) / BM;
+    for (int64_t mt = 0; mt < Mt; ++mt) {
+        const int64_t r0 = mt * BM, r1 = std::min<int64_t>(M, r0 + BM) - 1;
+        span = std::max<int>(span, (int)(r1 / cm - r0 / cm + 1));
+    }
+    return span;
+}
+
+}  // namespace
+
+struct mxa2a_plan {
+    int R;
+    int64_t M, ka, N, cm;
+    int bn;
+    int device = 0, sm_count = 0;
+    // derived
+    int64_t K = 0;
+    int steps = 0, Mt = 0, Nt = 0, S = 1, W = 0, Mg = 0, Ng2 = 0, box_m = 128, span = 1;
+    int rows_per_chunk = 1, chunks_per_seg = 1, n_copy_tasks = 0;
+    int grid_fused = 0, grid_unfused = 0;
+    // options
+    int64_t timeout_ns = 2000000000LL;
+    int force_split = 0, zigzag = 1, rotate = 1, record_events = 0, exchange_only = 0;
+    int fault_skip_step = -1, grid_cap = 0;
+    int64_t chunk_bytes = 32768;
+    // workspace
+    uint8_t* ws = nullptr;
+    size_t ws_bytes = 0;
+    uint8_t *ring = nullptr, *sfa = nullptr, *sfb = nullptr, *a_packed = nullptr;
+    float* partial = nullptr;          // split-K partials, own allocation sized for the current split
+    unsigned long long* flags = nullptr;
+    DevStatus* status = nullptr;
+    size_t ring_bytes = 0, sfa_bytes = 0, sfb_bytes = 0, apacked_bytes = 0, partial_bytes = 0, flags_bytes = 0;
+    CUtensorMap tmap_ring, tmap_apacked, tmap_b;
+    const void* tmap_b_ptr = nullptr;
+    unsigned long long launch_id = 0, checked_launch = 0;
+    cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+    bool ev_recorded = false;
+    int last_launches = 0;
+    // host-buffer path
+    uint8_t* io = nullptr;
+    size_t io_bytes = 0;
+};
+
+namespace {
+
+void derive(mxa2a_plan* p) {
+    p->K = (int64_t)p->R * p->ka;
+    p->steps = (int)(p->M / p->cm);
+    p->Mt = (int)((p->M + BM - 1) / BM);
+    p->Nt = (int)((p->N + BN - 1) / BN);
+    p->Mg = p->Mt;
+    p->Ng2 = 2 * p->Nt;
+    p->box_m = (p->cm % BM == 0) ? BM : 64;
+    p->span = tile_span(p->M, p->cm);
+    const int tiles = p->Mt * p->Nt;
+    int S = 1;
+    if (p->force_split > 0) {
+        S = std::min(p->force_split, p->R);
+    } else if (tiles * 2 <= p->sm_count && p->K >= 1024) {
+        S = std::min<int>(p->R, p->sm_count / tiles);
+        while (S > 1 && p->K / S < 512) --S;
+    }
+    p->S = std::max(1, S);
+    p->W = tiles * p->S;
+    // staging copy chunk: the largest divisor of commMSize rows within chunk_bytes
+    int64_t want = std::max<int64_t>(1, p->chunk_bytes / p->ka);
+    int rpc = 1;
+    for (int64_t d = 1; d <= p->cm; ++d)
+        if (p->cm % d == 0 && d <= want) rpc = (int)d;
+    p->rows_per_chunk = rpc;
+    p->chunks_per_seg = (int)(p->cm / rpc);
+    p->n_copy_tasks = p->steps * p->R * p->chunks_per_seg;
+    int cap = p->sm_count;
+    if (p->grid_cap > 0) cap = std::min(cap, p->grid_cap);
+    p->grid_fused = std::max(1, std::min(cap, std::max(p->W, p->n_copy_tasks)));
+    p->grid_unfused = std::max(1, std::min(cap, p->W));
+}
+
+bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+int check_device(mxa2a_plan* p) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MXA2A_ERR_CUDA;
+    if (dev != p->device) return MXA2A_ERR_WRONG_DEVICE;
+    return MXA2A_OK;
+}
+
+int check_args(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, const void* B, const void* B_sf,
+               const void* C) {
+    if (!p || !A_seg || !A_sf || !B || !B_sf || !C) return MXA2A_ERR_NULL_PTR;
+    for (int r = 0; r < p->R; ++r) {
+        if (!A_seg[r] || !A_sf[r]) return MXA2A_ERR_NULL_PTR;
+        if (!aligned(A_seg[r], 16) || !aligned(A_sf[r], 4)) return MXA2A_ERR_MISALIGNED;
+    }
+    if (!aligned(B, 16) || !aligned(C, 16) || !aligned(B_sf, 4)) return MXA2A_ERR_MISALIGNED;
+    return MXA2A_OK;
+}
+
+void fill_params(mxa2a_plan* p, GemmParams& g, const void* const* A_seg, const void* const* A_sf, void* C,
+                 bool fused) {
+    std::memset(&g, 0, sizeof g);
+    g.R = p->R;
+    g.M = (int)p->M;
+    g.N = (int)p->N;
+    g.ka = (int)p->ka;
+    g.K = (int)p->K;
+    g.cm = (int)p->cm;
+    g.bn = p->bn;
+    g.steps = p->steps;
+    g.Mt = p->Mt;
+    g.Nt = p->Nt;
+    g.S = p->S;
+    g.W = p->W;
+    g.kb_per_seg = (int)(p->ka / BK);
+    g.Mg = p->Mg;
+    g.Ng2 = p->Ng2;
+    g.box_m = p->box_m;
+    g.zigzag = p->zigzag;
+    g.rotate = p->rotate;
+    g.sfa = p->sfa;
+    g.sfb = p->sfb;
+    g.C = static_cast<uint16_t*>(C);
+    g.partial = p->partial;
+    g.fused = fused ? 1 : 0;
+    g.exchange_only = fused ? p->exchange_only : 0;
+    g.rows_per_chunk = p->rows_per_chunk;
+    g.chunks_per_seg = p->chunks_per_seg;
+    g.n_copy_tasks = p->n_copy_tasks;
+    g.fault_skip_step = p->fault_skip_step;
+    g.ring = p->ring;
+    g.sfa_stage = p->sfa;
+    g.flags = p->flags;
+    g.status = p->status;
+    g.launch_id = ++p->launch_id;
+    g.timeout_ns = p->timeout_ns;
+    for (int r = 0; r < p->R; ++r) {
+        g.A_seg[r] = static_cast<const uint8_t*>(A_seg[r]);
+        g.A_sf_seg[r] = static_cast<const uint8_t*>(A_sf[r]);
+    }
+}
+
+int refresh_b_map(mxa2a_plan* p, const void* B) {
+    if (p->tmap_b_ptr == B) return MXA2A_OK;
+    if (!encode_2d(&p->tmap_b, B, (uint64_t)p->K, (uint64_t)p->N, BN)) return MXA2A_ERR_CUDA;
+    p->tmap_b_ptr = B;
+    return MXA2A_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MXA2A_OK : MXA2A_ERR_CUDA; }
+
+// (Re)allocate the split-K partial buffer for the plan's current split.
+int ensure_partials(mxa2a_plan* p) {
+    const size_t need = p->S > 1 ? (size_t)p->S * p->M * p->N * sizeof(float) : 0;
+    if (need <= p->partial_bytes) return MXA2A_OK;
+    if (p->partial) cudaFree(p->partial);
+    p->partial = nullptr;
+    p->partial_bytes = 0;
+    if (cudaMalloc(reinterpret_cast<void**>(&p->partial), need) != cudaSuccess) {
+        cudaGetLastError();
+        return MXA2A_ERR_CUDA;
+    }
+    p->partial_bytes = need;
+    return MXA2A_OK;
+}
+
+int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, const void* B, const void* B_sf,
+             void* C, void* stream_v, bool fused) {
+    int rc = check_args(p, A_seg, A_sf, B, B_sf, C);
+    if (rc) return rc;
+    if ((rc = check_device(p))) return rc;
+    if ((rc = refresh_b_map(p, B))) return rc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    int launches = 0;
+    if ((rc = cuda_rc(launch_pack_sfb(static_cast<const uint8_t*>(B_sf), (int)p->N, (int)p->K, p->Ng2, p->sfb,
+                                      stream))))
+        return rc;
+    ++launches;
+    GemmParams g;
+    fill_params(p, g, A_seg, A_sf, C, fused);
+    if (!fused) {
+        if ((rc = cuda_rc(launch_pack_a(g, p->a_packed, 0, stream)))) return rc;
+        ++launches;
+    }
+    if (p->record_events && (rc = cuda_rc(cudaEventRecord(p->ev0, stream)))) return rc;
+    rc = cuda_rc(launch_mxgemm(g, fused ? p->tmap_ring : p->tmap_apacked, p->tmap_b,
+                               fused ? p->grid_fused : p->grid_unfused, fused, stream));
+    if (rc) return rc;
+    ++launches;
+    if (p->record_events) {
+        if ((rc = cuda_rc(cudaEventRecord(p->ev1, stream)))) return rc;
+        p->ev_recorded = true;
+    }
+    if (p->S > 1 && !(fused && p->exchange_only)) {
+        if ((rc = cuda_rc(launch_splitk_reduce(p->partial, p->S, p->M * p->N, static_cast<uint16_t*>(C), stream))))
+            return rc;
+        ++launches;
+    }
+    p->last_launches = launches;
+    return MXA2A_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mxa2a_validate(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t commMSize, int buffer_num) {
+    if (R < 1 || R > kMaxSegments) return MXA2A_ERR_INVALID_SHAPE;
+    if (M < 1 || kPerRank < BK || N < 16 || commMSize < 64) return MXA2A_ERR_INVALID_SHAPE;
+    if (kPerRank % BK || N % 16 || commMSize % 64 || M % commMSize) return MXA2A_ERR_INVALID_SHAPE;
+    if (buffer_num < 1 || buffer_num > 8) return MXA2A_ERR_INVALID_SHAPE;
+    const int64_t lim = int64_t(1) << 20;
+    if (M > lim || N > lim || (int64_t)R * kPerRank > lim) return MXA2A_ERR_INVALID_SHAPE;
+    if (buffer_num < tile_span(M, commMSize)) return MXA2A_ERR_INVALID_SHAPE;
+    return MXA2A_OK;
+}
+
+int mxa2a_last_error(void) { return g_last_error; }
+
+mxa2a_plan* mxa2a_create(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t commMSize, int buffer_num) {
+    int rc = mxa2a_validate(R, M, kPerRank, N, commMSize, buffer_num);
+    if (rc) {
+        g_last_error = rc;
+        return nullptr;
+    }
+    int dev = 0, major = 0, minor = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        g_last_error = MXA2A_ERR_CUDA;
+        return nullptr;
+    }
+    if (major != 10 || minor != 3) {
+        g_last_error = MXA2A_ERR_UNSUPPORTED_DEVICE;
+        return nullptr;
+    }
+    mxa2a_plan* p = new (std::nothrow) mxa2a_plan();
+    if (!p) {
+        g_last_error = MXA2A_ERR_CUDA;
+        return nullptr;
+    }
+    p->R = R;
+    p->M = M;
+    p->ka = kPerRank;
+    p->N = N;
+    p->cm = commMSize;
+    p->bn = buffer_num;
+    p->device = dev;
+    p->sm_count = sms;
+    derive(p);
+    // workspace: ring | sfa | sfb | packed A | flags | status (split-K partials separately)
+    p->ring_bytes = (size_t)buffer_num * R * commMSize * kPerRank;
+    p->sfa_bytes = (size_t)(p->K / BK) * p->Mg * kSfAtomBytes;
+    p->sfb_bytes = (size_t)(p->K / BK) * p->Ng2 * kSfAtomBytes;
+    p->apacked_bytes = (size_t)M * p->K;
+    p->flags_bytes = FlagLayout::words(buffer_num, R) * sizeof(unsigned long long);
+    size_t off = 0;
+    const size_t o_ring = off; off = align_up(off + p->ring_bytes, 1024);
+    const size_t o_sfa = off; off = align_up(off + p->sfa_bytes, 1024);
+    const size_t o_sfb = off; off = align_up(off + p->sfb_bytes, 1024);
+    const size_t o_ap = off; off = align_up(off + p->apacked_bytes, 1024);
+    const size_t o_flags = off; off = align_up(off + p->flags_bytes, 1024);
+    const size_t o_status = off; off = align_up(off + sizeof(DevStatus), 1024);
+    p->ws_bytes = off;
+    if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        delete p;
+        g_last_error = MXA2A_ERR_CUDA;
+        return nullptr;
+    }
+    p->ring = p->ws + o_ring;
+    p->sfa = p->ws + o_sfa;
+    p->sfb = p->ws + o_sfb;
+    p->a_packed = p->ws + o_ap;
+    p->flags = reinterpret_cast<unsigned long long*>(p->ws + o_flags);
+    p->status = reinterpret_cast<DevStatus*>(p->ws + o_status);
+    bool ok = cudaMemset(p->ws + o_sfa, 0, p->sfa_bytes) == cudaSuccess &&
+              cudaMemset(p->flags, 0, p->flags_bytes) == cudaSuccess &&
+              cudaMemset(p->status, 0, sizeof(DevStatus)) == cudaSuccess &&
+              cudaEventCreate(&p->ev0) == cudaSuccess && cudaEventCreate(&p->ev1) == cudaSuccess &&
+              ensure_partials(p) == MXA2A_OK;
+    ok = ok && encode_2d(&p->tmap_ring, p->ring, (uint64_t)kPerRank, (uint64_t)buffer_num * R * commMSize,
+                         (uint32_t)p->box_m);
+    ok = ok && encode_2d(&p->tmap_apacked, p->a_packed, (uint64_t)p->K, (uint64_t)M, BM);
+    if (!ok || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        mxa2a_destroy(p);
+        g_last_error = MXA2A_ERR_CUDA;
+        return nullptr;
+    }
+    g_last_error = MXA2A_OK;
+    return p;
+}
+
+int mxa2a_run(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, const void* B, const void* B_sf,
+              void* C, void* stream) {
+    return run_impl(p, A_seg, A_sf, B, B_sf, C, stream, true);
+}
+
+int mxa2a_run_unfused(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, const void* B,
+                      const void* B_sf, void* C, void* stream) {
+    return run_impl(p, A_seg, A_sf, B, B_sf, C, stream, false);
+}
+
+int mxa2a_run_host(mxa2a_plan* p, const void* const* A_seg_h, const void* const* A_sf_h, const void* B_h,
+                   const void* B_sf_h, void* C_h, void* stream_v) {
+    if (!p || !A_seg_h || !A_sf_h || !B_h || !B_sf_h || !C_h) return MXA2A_ERR_NULL_PTR;
+    for (int r = 0; r < p->R; ++r)
+        if (!A_seg_h[r] || !A_sf_h[r]) return MXA2A_ERR_NULL_PTR;
+    int rc = check_device(p);
+    if (rc) return rc;
+    const size_t a_b = (size_t)p->M * p->ka, asf_b = (size_t)p->M * (p->ka / 32);
+    const size_t b_b = (size_t)p->N * p->K, bsf_b = (size_t)p->N * (p->K / 32), c_b = (size_t)p->M * p->N * 2;
+    const size_t a_s = align_up(a_b, 256), asf_s = align_up(asf_b, 256);
+    const size_t need = p->R * (a_s + asf_s) + align_up(b_b, 256) + align_up(bsf_b, 256) + align_up(c_b, 256);
+    if (p->io_bytes < need) {
+        if (p->io) cudaFree(p->io);
+        p->io = nullptr;
+        p->io_bytes = 0;
+        if (cudaMalloc(&p->io, need) != cudaSuccess) {
+            cudaGetLastError();
+            return MXA2A_ERR_CUDA;
+        }
+        p->io_bytes = need;
+        p->tmap_b_ptr = nullptr;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream_v);
+    const void* dA[kMaxSegments];
+    const void* dS[kMaxSegments];
+    uint8_t* cur = p->io;
+    for (int r = 0; r < p->R; ++r) {
+        dA[r] = cur;
+        if (cudaMemcpyAsync(cur, A_seg_h[r], a_b, cudaMemcpyHostToDevice, s) != cudaSuccess) return MXA2A_ERR_CUDA;
+        cur += a_s;
+        dS[r] = cur;
+        if (cudaMemcpyAsync(cur, A_sf_h[r], asf_b, cudaMemcpyHostToDevice, s) != cudaSuccess) return MXA2A_ERR_CUDA;
+        cur += asf_s;
+    }
+    uint8_t* dB = cur;
+    cur += align_up(b_b, 256);
+    uint8_t* dBs = cur;
+    cur += align_up(bsf_b, 256);
+    uint8_t* dC = cur;
+    if (cudaMemcpyAsync(dB, B_h, b_b, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dBs, B_sf_h, bsf_b, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return MXA2A_ERR_CUDA;
+    rc = run_impl(p, dA, dS, dB, dBs, dC, stream_v, true);
+    if (rc) return rc;
+    if (cudaMemcpyAsync(C_h, dC, c_b, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MXA2A_ERR_CUDA;
+    return MXA2A_OK;
+}
+
+int mxa2a_get_status(mxa2a_plan* p, mxa2a_status* out) {
+    if (!p || !out) return MXA2A_ERR_NULL_PTR;
+    int rc = check_device(p);
+    if (rc) return rc;
+    DevStatus st;
+    if (cudaMemcpy(&st, p->status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) return MXA2A_ERR_CUDA;
+    std::memset(out, 0, sizeof *out);
+    const unsigned long long launch = st.key >> 8;
+    const int code = (int)(st.key & 0xFF);
+    if (code != 0 && launch > p->checked_launch) {
+        out->code = code;
+        out->role = st.role;
+        out->block = st.block;
+        out->step = st.step;
+        out->segment = st.segment;
+        out->slot = st.slot;
+        out->observed = st.observed;
+        out->expected = st.expected;
+        out->launch = (int64_t)launch;
+    } else {
+        out->step = out->segment = out->slot = -1;
+    }
+    p->checked_launch = p->launch_id;
+    return MXA2A_OK;
+}
+
+int mxa2a_set_option(mxa2a_plan* p, int key, int64_t v) {
+    if (!p) return MXA2A_ERR_NULL_PTR;
+    switch (key) {
+        case MXA2A_OPT_TIMEOUT_NS:
+            if (v < 1000) return MXA2A_ERR_INVALID_OPTION;
+            p->timeout_ns = v;
+            return MXA2A_OK;
+        case MXA2A_OPT_SPLIT_K:
+            if (v < 0 || v > p->R) return MXA2A_ERR_INVALID_OPTION;
+            p->force_split = (int)v;
+            break;
+        case MXA2A_OPT_ZIGZAG:
+            if (v != 0 && v != 1) return MXA2A_ERR_INVALID_OPTION;
+            p->zigzag = (int)v;
+            return MXA2A_OK;
+        case MXA2A_OPT_ROTATE:
+            if (v != 0 && v != 1) return MXA2A_ERR_INVALID_OPTION;
+            p->rotate = (int)v;
+            return MXA2A_OK;
+        case MXA2A_OPT_RECORD_EVENTS:
+            if (v != 0 && v != 1) return MXA2A_ERR_INVALID_OPTION;
+            p->record_events = (int)v;
+            p->ev_recorded = false;
+            return MXA2A_OK;
+        case MXA2A_OPT_EXCHANGE_ONLY:
+            if (v != 0 && v != 1) return MXA2A_ERR_INVALID_OPTION;
+            if (v == 1 && p->bn < p->steps) return MXA2A_ERR_INVALID_OPTION;
+            p->exchange_only = (int)v;
+            return MXA2A_OK;
+        case MXA2A_OPT_FAULT_SKIP_STEP:
+            if (v < -1 || v >= p->steps) return MXA2A_ERR_INVALID_OPTION;
+            p->fault_skip_step = (int)v;
+            return MXA2A_OK;
+        case MXA2A_OPT_GRID:
+            if (v < 0) return MXA2A_ERR_INVALID_OPTION;
+            p->grid_cap = (int)v;
+            break;
+        case MXA2A_OPT_CHUNK_BYTES:
+            if (v < 16) return MXA2A_ERR_INVALID_OPTION;
+            p->chunk_bytes = v;
+            break;
+        default:
+            return MXA2A_ERR_INVALID_OPTION;
+    }
+    derive(p);
+    return ensure_partials(p);
+}
+
+int mxa2a_get_option(mxa2a_plan* p, int key, int64_t* v) {
+    if (!p || !v) return MXA2A_ERR_NULL_PTR;
+    switch (key) {
+        case MXA2A_OPT_TIMEOUT_NS: *v = p->timeout_ns; break;
+        case MXA2A_OPT_SPLIT_K: *v = p->force_split; break;
+        case MXA2A_OPT_ZIGZAG: *v = p->zigzag; break;
+        case MXA2A_OPT_ROTATE: *v = p->rotate; break;
+        case MXA2A_OPT_RECORD_EVENTS: *v = p->record_events; break;
+        case MXA2A_OPT_EXCHANGE_ONLY: *v = p->exchange_only; break;
+        case MXA2A_OPT_FAULT_SKIP_STEP: *v = p->fault_skip_step; break;
+        case MXA2A_OPT_GRID: *v = p->grid_cap; break;
+        case MXA2A_OPT_CHUNK_BYTES: *v = p->chunk_bytes; break;
+        case MXA2A_INFO_STEPS: *v = p->steps; break;
+        case MXA2A_INFO_MTILES: *v = p->Mt; break;
+        case MXA2A_INFO_NTILES: *v = p->Nt; break;
+        case MXA2A_INFO_SPLITS: *v = p->S; break;
+        case MXA2A_INFO_ITEMS: *v = p->W; break;
+        case MXA2A_INFO_GRID_FUSED: *v = p->grid_fused; break;
+        case MXA2A_INFO_GRID_UNFUSED: *v = p->grid_unfused; break;
+        case MXA2A_INFO_COPY_TASKS: *v = p->n_copy_tasks; break;
+        case MXA2A_INFO_ROWS_PER_CHUNK: *v = p->rows_per_chunk; break;
+        case MXA2A_INFO_WORKSPACE_BYTES: *v = (int64_t)p->ws_bytes; break;
+        case MXA2A_INFO_SM_COUNT: *v = p->sm_count; break;
+        case MXA2A_INFO_LAUNCHES: *v = p->last_launches; break;
+        default: return MXA2A_ERR_INVALID_OPTION;
+    }
+    return MXA2A_OK;
+}
+
+int mxa2a_last_kernel_ms(mxa2a_plan* p, float* ms) {
+    if (!p || !ms) return MXA2A_ERR_NULL_PTR;
+    if (!p->record_events || !p->ev_recorded) return MXA2A_ERR_INVALID_OPTION;
+    if (cudaEventSynchronize(p->ev1) != cudaSuccess) return MXA2A_ERR_CUDA;
+    return cudaEventElapsedTime(ms, p->ev0, p->ev1) == cudaSuccess ? MXA2A_OK : MXA2A_ERR_CUDA;
+}
+
+int mxa2a_read_workspace(mxa2a_plan* p, int which, void* dst, size_t bytes, size_t* bytes_out) {
+    if (!p) return MXA2A_ERR_NULL_PTR;
+    const void* src = nullptr;
+    size_t size = 0;
+    switch (which) {
+        case MXA2A_WS_RING: src = p->ring; size = p->ring_bytes; break;
+        case MXA2A_WS_SFA: src = p->sfa; size = p->sfa_bytes; break;
+        case MXA2A_WS_SFB: src = p->sfb; size = p->sfb_bytes; break;
+        case MXA2A_WS_FLAGS: src = p->flags; size = p->flags_bytes; break;
+        case MXA2A_WS_APACKED: src = p->a_packed; size = p->apacked_bytes; break;
+        default: return MXA2A_ERR_INVALID_OPTION;
+    }
+    if (bytes_out) *bytes_out = size;
+    if (!dst || bytes == 0) return MXA2A_OK;
+    int rc = check_device(p);
+    if (rc) return rc;
+    return cudaMemcpy(dst, src, std::min(bytes, size), cudaMemcpyDeviceToHost) == cudaSuccess ? MXA2A_OK
+                                                                                             : MXA2A_ERR_CUDA;
+}
+
+int mxa2a_l2_flush(void* buf, size_t bytes, void* stream) {
+    if (!buf) return MXA2A_ERR_NULL_PTR;
+    if (bytes % 16 || !aligned(buf, 16)) return MXA2A_ERR_MISALIGNED;
+    return launch_l2_flush(buf, bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MXA2A_OK
+                                                                                        : MXA2A_ERR_CUDA;
+}
+
+void mxa2a_destroy(mxa2a_plan* p) {
+    if (!p) return;
+    int prev = -1;
+    cudaGetDevice(&prev);
+    if (prev != p->device) cudaSetDevice(p->device);
+    cudaDeviceSynchronize();
+    if (p->ws) cudaFree(p->ws);
+    if (p->partial) cudaFree(p->partial);
+    if (p->io) cudaFree(p->io);
+    if (p->ev0) cudaEventDestroy(p->ev0);
+    if (p->ev1) cudaEventDestroy(p->ev1);
+    if (prev >= 0 && prev != p->device) cudaSetDevice(prev);
+    delete p;
+}
+
+const char* mxa2a_strerror(int code) {
+    switch (code) {
+        case MXA2A_OK: return "ok";
+        case MXA2A_ERR_INVALID_SHAPE: return "invalid shape";
+        case MXA2A_ERR_NULL_PTR: return "null pointer";
+        case MXA2A_ERR_MISALIGNED: return "misaligned pointer";
+        case MXA2A_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+        case MXA2A_ERR_CUDA: return "CUDA call failed";
+        case MXA2A_ERR_TIMEOUT: return "device wait timed out";
+        case MXA2A_ERR_INVALID_OPTION: return "invalid option";
+        case MXA2A_ERR_DEVICE_CHECK: return "device consistency check failed";
+        case MXA2A_ERR_WRONG_DEVICE: return "current device differs from the plan's device";
+        default: return "unknown error";
+    }
+}
+
+}  // extern "C"

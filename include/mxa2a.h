@@ -1,0 +1,200 @@
+/*
+ * libmxa2a — fused AllToAll + MXFP8 block-scaled GEMM for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the MC2 "AllToAll + quantised matmul" kernel of the
+ * all_to_all_matmul example (all_to_all_matmul_impl.h, class
+ * AllToAllQuantMatmulImpl: AllToAllProcess stages the R K-segments of A
+ * through a ring of bufferSize slots of commMSize rows; MatmulProcess runs a
+ * block-scaled FP8 GEMM over every staged slot with split-K over the R
+ * segments and writes BF16).  On one GPU the R "ranks" are R separate device
+ * buffers A_seg[0..R-1]; the library stages them through its own ring and
+ * computes, for every m < M, n < N:
+ *
+ *   C[m][n] = bf16( sum_{r<R} sum_{k<kPerRank}
+ *                    e4m3(A_seg[r][m][k])      * 2^(A_scale_seg[r][m][k/32] - 127)
+ *                  * e4m3(B[n][r*kPerRank + k]) * 2^(B_scale[n][(r*kPerRank + k)/32] - 127) )
+ *
+ * accumulated in fp32 on the tensor cores and rounded once to BF16 (round to
+ * nearest even).  K = R * kPerRank.
+ *
+ * Data types and layouts (all row-major, all device memory unless noted):
+ *   A_seg[r]        uint8 E4M3 ("fn": no infinities, 0x7F/0xFF are NaN), [M][kPerRank]
+ *   A_scale_seg[r]  uint8 E8M0 (2^(x-127), 0xFF = NaN), [M][kPerRank/32]
+ *   B               uint8 E4M3, [N][K]  (B is logically K x N, stored transposed:
+ *                   the kernel entry's TransB = true)
+ *   B_scale         uint8 E8M0, [N][K/32]
+ *   C_bf16          uint16 BF16 bit patterns, [M][N]
+ * Alignment: A_seg[r], B and C_bf16 16-byte aligned; scale pointers 4-byte aligned.
+ *
+ * Ownership: the caller owns every input and output buffer and the stream;
+ * the plan owns its device workspace (staging ring, scale-factor tiles, credit
+ * counters, split-K partials, status block), allocated by mxa2a_create on the
+ * current device and freed by mxa2a_destroy.  Runs are asynchronous on the
+ * given stream; one plan must not run on two streams at once.
+ *
+ * Errors: every int-returning call returns MXA2A_OK (0) or an MXA2A_ERR_* code
+ * and never aborts the process.  Device-side failures (a bounded wait that ran
+ * out) are reported by mxa2a_get_status after the stream has been synchronised.
+ */
+#ifndef MXA2A_H
+#define MXA2A_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum mxa2a_error {
+    MXA2A_OK = 0,
+    MXA2A_ERR_INVALID_SHAPE = 1,      /* shape rule broken (see mxa2a_validate) */
+    MXA2A_ERR_NULL_PTR = 2,           /* a required pointer is NULL */
+    MXA2A_ERR_MISALIGNED = 3,         /* pointer alignment rule broken */
+    MXA2A_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
+    MXA2A_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
+    MXA2A_ERR_TIMEOUT = 6,            /* device: a bounded wait ran out (get_status) */
+    MXA2A_ERR_INVALID_OPTION = 7,     /* unknown option key or value out of range */
+    MXA2A_ERR_DEVICE_CHECK = 8,       /* device: an internal consistency check failed */
+    MXA2A_ERR_WRONG_DEVICE = 9        /* current device differs from the plan's */
+};
+
+typedef struct mxa2a_plan mxa2a_plan;   /* opaque */
+
+/* Device-side status of the runs since the previous mxa2a_get_status call. */
+typedef struct mxa2a_status {
+    int32_t code;       /* MXA2A_OK, or the first device error of the reported launch */
+    int32_t role;       /* 1 staging copy, 2 TMA producer, 3 MMA issuer, 4 epilogue, 5 exit */
+    int32_t block;      /* CTA that reported */
+    int32_t step;       /* staging step waited on, -1 if none */
+    int32_t segment;    /* segment waited on, -1 if none */
+    int32_t slot;       /* ring slot waited on, -1 if none */
+    int64_t observed;   /* counter value seen when the wait gave up */
+    int64_t expected;   /* value it waited for */
+    int64_t launch;     /* index (1-based, per plan) of the launch that failed */
+} mxa2a_status;
+
+/*
+ * Shape rules, checked by mxa2a_validate and mxa2a_create (the pages take
+ * m, k, n and rankNum, require k % rankNum == 0 and CeilDiv(k/rankNum, 64)
+ * even, and silently drop rows when commMSize does not divide m; here every
+ * rule is an error instead):
+ *   1 <= R <= 64; M >= 1; kPerRank % 128 == 0; N % 16 == 0, N >= 16;
+ *   commMSize % 64 == 0; M % commMSize == 0; 1 <= buffer_num <= 8;
+ *   buffer_num >= the number of staging steps one 128-row output tile spans
+ *   (2 when commMSize is 64 or not a multiple of 128, else 1);
+ *   M, N, K <= 2^20.
+ * Returns MXA2A_OK or MXA2A_ERR_INVALID_SHAPE.  Pure host code.
+ */
+int mxa2a_validate(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t commMSize, int buffer_num);
+
+/*
+ * Create a plan for one problem shape on the current CUDA device: validates
+ * the shape, derives the tiling (128x256 output tiles, 128-wide K blocks,
+ * split-K over segments when there are too few tiles to fill the GPU),
+ * allocates the workspace and encodes the TMA descriptors of the ring.
+ * Returns NULL on error; mxa2a_last_error() then gives the code.
+ */
+mxa2a_plan *mxa2a_create(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t commMSize, int buffer_num);
+
+/* Error code of the last failed mxa2a_create on this thread. */
+int mxa2a_last_error(void);
+
+/*
+ * The fused path: one persistent cooperative kernel stages A_seg[r] rows
+ * (commMSize per step, buffer_num-slot ring, per-slot credits) and runs the
+ * block-scaled GEMM on the staged slots as they fill; plus a small kernel that
+ * reorders B_scale for the MMA, and a split-K reduction when the plan splits.
+ * A_seg / A_scale_seg are host arrays of R device pointers.  stream is a
+ * cudaStream_t (NULL = legacy default stream).  Asynchronous.
+ */
+int mxa2a_run(mxa2a_plan *plan, const void *const *A_seg, const void *const *A_scale_seg, const void *B,
+              const void *B_scale, void *C_bf16, void *stream);
+
+/*
+ * The unfused comparison path: first pack the R segments into one [M][K]
+ * operand (and its scales), then run the same GEMM on it.  Same arguments,
+ * same result bits as mxa2a_run for the same plan and options.
+ */
+int mxa2a_run_unfused(mxa2a_plan *plan, const void *const *A_seg, const void *const *A_scale_seg, const void *B,
+                      const void *B_scale, void *C_bf16, void *stream);
+
+/*
+ * End-to-end variant with HOST buffers (same layouts): copies the inputs to
+ * plan-owned device buffers (allocated on the first call), runs the fused
+ * path and copies C back, all asynchronously on stream.  Host buffers should
+ * be pinned for the copies to overlap; the caller synchronises the stream
+ * before reading C_bf16.
+ */
+int mxa2a_run_host(mxa2a_plan *plan, const void *const *A_seg_host, const void *const *A_scale_seg_host,
+                   const void *B_host, const void *B_scale_host, void *C_bf16_host, void *stream);
+
+/*
+ * Copy the device status block to *out (synchronous; call after the runs'
+ * stream is synchronised) and mark it read.  out->code is MXA2A_OK unless a
+ * launch since the previous call reported a device error.
+ */
+int mxa2a_get_status(mxa2a_plan *plan, mxa2a_status *out);
+
+/* Option keys for mxa2a_set_option / mxa2a_get_option. */
+enum mxa2a_option {
+    MXA2A_OPT_TIMEOUT_NS = 1,      /* limit of every device wait, ns (default 2e9) */
+    MXA2A_OPT_SPLIT_K = 2,         /* 0 = automatic, s >= 1: split K into s segment groups */
+    MXA2A_OPT_ZIGZAG = 3,          /* 1 (default): alternate n-tile direction per m-tile */
+    MXA2A_OPT_ROTATE = 4,          /* 1 (default): start each tile's K loop at a rotated segment */
+    MXA2A_OPT_RECORD_EVENTS = 5,   /* 1: time the main GEMM kernel of each run (mxa2a_last_kernel_ms) */
+    MXA2A_OPT_EXCHANGE_ONLY = 6,   /* 1: fused runs only stage A into the ring (needs buffer_num >= steps) */
+    MXA2A_OPT_FAULT_SKIP_STEP = 7, /* test knob: never publish staging step k (-1 = off); waits then time out */
+    MXA2A_OPT_GRID = 8,            /* cap on persistent CTAs (0 = one per SM) */
+    MXA2A_OPT_CHUNK_BYTES = 9,     /* target staging copy chunk (default 32768) */
+    /* read-only plan facts (mxa2a_get_option only) */
+    MXA2A_INFO_STEPS = 100,        /* M / commMSize */
+    MXA2A_INFO_MTILES = 101,
+    MXA2A_INFO_NTILES = 102,
+    MXA2A_INFO_SPLITS = 103,       /* effective K split */
+    MXA2A_INFO_ITEMS = 104,        /* work items of the persistent GEMM */
+    MXA2A_INFO_GRID_FUSED = 105,
+    MXA2A_INFO_GRID_UNFUSED = 106,
+    MXA2A_INFO_COPY_TASKS = 107,
+    MXA2A_INFO_ROWS_PER_CHUNK = 108,
+    MXA2A_INFO_WORKSPACE_BYTES = 109,
+    MXA2A_INFO_SM_COUNT = 110,
+    MXA2A_INFO_LAUNCHES = 111      /* kernels launched by the last run call */
+};
+
+int mxa2a_set_option(mxa2a_plan *plan, int key, int64_t value);
+int mxa2a_get_option(mxa2a_plan *plan, int key, int64_t *value);
+
+/* Duration of the main GEMM kernel of the last run, in ms (needs
+ * MXA2A_OPT_RECORD_EVENTS = 1; synchronises on that run's end event). */
+int mxa2a_last_kernel_ms(mxa2a_plan *plan, float *ms);
+
+/* Workspace regions readable with mxa2a_read_workspace (debug and tests). */
+enum mxa2a_workspace {
+    MXA2A_WS_RING = 1,      /* staging ring  [buffer_num][R][commMSize][kPerRank] */
+    MXA2A_WS_SFA = 2,       /* A scales in MMA atom layout [K/128][ceil(M/128)][512] */
+    MXA2A_WS_SFB = 3,       /* B scales in MMA atom layout [K/128][2*ceil(N/256)][512] */
+    MXA2A_WS_FLAGS = 4,     /* credit counters, u64, one per 128-byte line */
+    MXA2A_WS_APACKED = 5    /* unfused packed A [M][K] */
+};
+
+/* Synchronous copy of a workspace region to host memory (at most bytes);
+ * *bytes_out receives the region's full size.  Synchronise the plan's
+ * stream first. */
+int mxa2a_read_workspace(mxa2a_plan *plan, int which, void *host_dst, size_t bytes, size_t *bytes_out);
+
+/* Benchmark helper: add 1 to every 32-bit word of a device buffer (bytes %
+ * 16 == 0), evicting other data from L2 when bytes exceeds its size. */
+int mxa2a_l2_flush(void *device_buf, size_t bytes, void *stream);
+
+/* Free the plan's workspace (synchronises the device first). NULL is a no-op. */
+void mxa2a_destroy(mxa2a_plan *plan);
+
+/* Static string for an error code. */
+const char *mxa2a_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXA2A_H */

@@ -1,0 +1,308 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Gate per element: |gpu - ref| <= 1e-2 + 1e-2*|ref| (the pages' verify
+tolerance, atol = rtol = 1e-2, measured against the exact oracle).  Small
+shapes are compared in full; the full-size workloads on sampled rows (every
+column), in the launch configuration the benchmark times.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from all_mxfp8_block_gb300 import inputs, mxa2a
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from all_mxfp8_block_gb300 import build
+    build.build()
+    mxa2a.load()
+    torch.cuda.init()
+
+
+def _plan(w, **opts):
+    p = mxa2a.Plan(w.R, w.M, w.kPerRank, w.N, w.commMSize, w.buffer_num)
+    p.set_option(mxa2a.MXA2A_OPT_TIMEOUT_NS, opts.pop("timeout_ns", 500_000_000))
+    for k, v in opts.items():
+        p.set_option(getattr(mxa2a, "MXA2A_OPT_" + k.upper()), v)
+    return p
+
+
+def _status_ok(p):
+    st = p.status()
+    assert st["code"] == 0, st
+
+
+def _check_full(w, fused=True, **opts):
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w, **opts) as p:
+        C = gu.run_gpu(p, d, w.M, w.N, fused=fused)
+        torch.cuda.synchronize()
+        _status_ok(p)
+        got = gu.host_bits(C)
+    ref = gu.oracle_full(x)
+    gu.assert_parity(got, ref, f"{w.name} fused={fused} {opts}")
+    return got, ref
+
+
+# --- targeted layout checks: exact results ------------------------------------------------
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_identity_B_reproduces_A(fused):
+    """B = I (K = N): C must equal A times its scales exactly; any mix-up of
+    rows, K order, swizzle or scale-factor placement shows up here."""
+    R, M, ka = 2, 128, 128
+    K = N = R * ka
+    w = inputs.Workload("identity", R, M, ka, N, 64, 2, 0)
+    A = inputs.random_codes((M, K), 101)
+    sA = inputs.random_scales((M, K // 32), 102, 117, 137)
+    B = torch.zeros((N, K), dtype=torch.uint8)
+    B[torch.arange(N), torch.arange(K)] = 0x38
+    sB = torch.full((N, K // 32), 127, dtype=torch.uint8)
+    x = {"A_seg": [A[:, r * ka:(r + 1) * ka].contiguous() for r in range(R)],
+         "A_scale_seg": [sA[:, r * ka // 32:(r + 1) * ka // 32].contiguous() for r in range(R)],
+         "B": B, "B_scale": sB}
+    d = gu.to_device(x)
+    with _plan(w) as p:
+        C = gu.run_gpu(p, d, M, N, fused=fused)
+        torch.cuda.synchronize()
+        _status_ok(p)
+        got = gu.host_bits(C)
+    ref = gu.oracle_full(x)
+    gv, rv = gu.bits_to_f64(got), gu.bits_to_f64(ref)
+    assert np.array_equal(gv, rv), f"{np.sum(gv != rv)} of {gv.size} differ"
+
+
+def test_scale_factors_per_block_and_column():
+    """One-hot B with varied B scales per 32-block and column: exercises every
+    scale-factor lane/column/byte position of both operands."""
+    R, M, ka, N = 2, 128, 256, 256
+    K = R * ka
+    w = inputs.Workload("onehot", R, M, ka, N, 128, 2, 0)
+    rng = np.random.default_rng(7)
+    perm = rng.integers(0, K, size=N)
+    A = inputs.random_codes((M, K), 201)
+    sA = inputs.random_scales((M, K // 32), 202, 112, 142)
+    B = torch.zeros((N, K), dtype=torch.uint8)
+    B[torch.arange(N), torch.from_numpy(perm)] = 0x38
+    sB = inputs.random_scales((N, K // 32), 203, 120, 134)
+    x = {"A_seg": [A[:, r * ka:(r + 1) * ka].contiguous() for r in range(R)],
+         "A_scale_seg": [sA[:, r * ka // 32:(r + 1) * ka // 32].contiguous() for r in range(R)],
+         "B": B, "B_scale": sB}
+    d = gu.to_device(x)
+    with _plan(w) as p:
+        C = gu.run_gpu(p, d, M, N)
+        torch.cuda.synchronize()
+        _status_ok(p)
+        got = gu.host_bits(C)
+    ref = gu.oracle_full(x)
+    assert np.array_equal(gu.bits_to_f64(got), gu.bits_to_f64(ref))
+
+
+# --- the smallest workload, and small shapes spanning tiles with ragged tails -------------
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_workload_tiny(fused):
+    _check_full(inputs.workload(0), fused=fused)
+
+
+SMALL = [
+    # name, R, M, ka, N, cm, bn
+    ("tiles_ragged_n", 3, 384, 256, 528, 128, 2),
+    ("cm64_tail_tile", 2, 192, 128, 256, 64, 2),
+    ("cm192_straddle", 2, 384, 128, 272, 192, 2),
+    ("many_steps_bn2", 2, 1024, 128, 256, 64, 2),
+    ("single_slot", 2, 512, 128, 256, 128, 1),
+    ("bn3", 2, 768, 128, 256, 128, 3),
+    ("one_segment", 1, 256, 512, 256, 128, 2),
+    ("n16", 2, 128, 128, 16, 64, 2),
+    ("one_step", 4, 256, 128, 512, 256, 2),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_small_shapes(case):
+    name, R, M, ka, N, cm, bn = case
+    w = inputs.Workload(name, R, M, ka, N, cm, bn, 11)
+    got_f, ref = _check_full(w, fused=True)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w) as p:
+        got_u = gu.host_bits(gu.run_gpu(p, d, M, N, fused=False))
+    assert np.array_equal(got_f, got_u), "fused and unfused differ"
+
+
+@pytest.mark.parametrize("split", [2, 3])
+def test_forced_split_k(split):
+    w = inputs.Workload("split", 6, 256, 256, 512, 128, 2, 13)
+    _check_full(w, fused=True, split_k=split)
+    _check_full(w, fused=False, split_k=split)
+
+
+def test_automatic_split_small_m():
+    w = inputs.Workload("autosplit", 8, 64, 256, 1024, 64, 2, 17, outliers=True)
+    with _plan(w) as p:
+        assert p.get_option(mxa2a.MXA2A_INFO_SPLITS) > 1
+    _check_full(w, fused=True)
+
+
+def test_zigzag_rotation_off_same_tolerance():
+    w = inputs.Workload("noswizzle", 4, 512, 256, 768, 128, 2, 19)
+    _check_full(w, fused=True, zigzag=0, rotate=0)
+
+
+def test_small_grid_many_items_per_cta():
+    w = inputs.Workload("grid3", 3, 512, 128, 768, 64, 2, 23)
+    _check_full(w, fused=True, grid=3)
+
+
+def test_repeat_runs_identical_and_counters_reset():
+    w = inputs.Workload("repeat", 2, 512, 128, 512, 64, 2, 29)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w) as p:
+        outs = [gu.host_bits(gu.run_gpu(p, d, w.M, w.N)) for _ in range(3)]
+        torch.cuda.synchronize()
+        _status_ok(p)
+        flags = p.read_workspace(mxa2a.MXA2A_WS_FLAGS).view(np.uint64)
+        assert np.all(flags == 0)
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+
+
+def test_non_default_stream_and_host_entry():
+    w = inputs.workload(0)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    s = torch.cuda.Stream()
+    with _plan(w) as p:
+        C = gu.run_gpu(p, d, w.M, w.N, stream=s)
+        s.synchronize()
+        got = gu.host_bits(C)
+        hA = [a.pin_memory() for a in x["A_seg"]]
+        hS = [a.pin_memory() for a in x["A_scale_seg"]]
+        hB, hBs = x["B"].pin_memory(), x["B_scale"].pin_memory()
+        hC = torch.empty((w.M, w.N), dtype=torch.int16).pin_memory()
+        p.run_host(hA, hS, hB, hBs, hC, s)
+        s.synchronize()
+        _status_ok(p)
+    assert np.array_equal(got, hC.numpy().view(np.uint16))
+    gu.assert_parity(got, gu.oracle_full(x), "stream")
+
+
+def test_zero_A_gives_zero():
+    w = inputs.Workload("zero", 2, 128, 128, 256, 64, 2, 0)
+    x = inputs.make_inputs(w)
+    x["A_seg"] = [torch.zeros_like(a) for a in x["A_seg"]]
+    d = gu.to_device(x)
+    with _plan(w) as p:
+        got = gu.host_bits(gu.run_gpu(p, d, w.M, w.N))
+    assert np.all(gu.bits_to_f64(got) == 0)
+
+
+# --- building blocks: the staging exchange and the scale-factor layouts --------------------
+
+def _atom_restate(sf: np.ndarray, rows_pad: int) -> np.ndarray:
+    """CPU restatement of the MMA scale atom layout: [K/128][rows_pad/128][512]."""
+    rows, kb32 = sf.shape
+    kbs = kb32 // 4
+    out = np.zeros((kbs, rows_pad // 128, 128, 4), dtype=np.uint8)
+    for x in range(rows):
+        g, xi = divmod(x, 128)
+        word = (xi % 32) * 4 + xi // 32
+        for kb in range(kbs):
+            out[kb, g, word] = sf[x, kb * 4:(kb + 1) * 4]
+    return out.reshape(-1)
+
+
+def test_exchange_only_ring_and_scales():
+    """Only the staging copy runs (buffer_num >= steps): the ring must hold the
+    segments byte for byte at [slot][r][row], the scales in the MMA layout."""
+    w = inputs.Workload("xchg", 3, 256, 256, 256, 64, 4, 31)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w, exchange_only=1) as p:
+        gu.run_gpu(p, d, w.M, w.N)
+        torch.cuda.synchronize()
+        _status_ok(p)
+        ring = p.read_workspace(mxa2a.MXA2A_WS_RING).reshape(w.buffer_num, w.R, w.commMSize, w.kPerRank)
+        sfa = p.read_workspace(mxa2a.MXA2A_WS_SFA)
+    for s in range(w.M // w.commMSize):
+        for r in range(w.R):
+            src = x["A_seg"][r].numpy()[s * w.commMSize:(s + 1) * w.commMSize]
+            assert np.array_equal(ring[s % w.buffer_num, r], src), (s, r)
+    sf_full = np.concatenate([s.numpy() for s in x["A_scale_seg"]], axis=1)
+    assert np.array_equal(sfa, _atom_restate(sf_full, 128 * ((w.M + 127) // 128)))
+
+
+def test_b_scale_pack_layout():
+    w = inputs.Workload("sfb", 2, 128, 256, 400, 64, 2, 37)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w) as p:
+        gu.run_gpu(p, d, w.M, w.N)
+        torch.cuda.synchronize()
+        sfb = p.read_workspace(mxa2a.MXA2A_WS_SFB)
+    npad = 256 * ((w.N + 255) // 256)
+    assert np.array_equal(sfb, _atom_restate(x["B_scale"].numpy(), npad))
+
+
+def test_unfused_pack_matches_concatenation():
+    w = inputs.Workload("pack", 3, 192, 128, 256, 64, 2, 41)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w) as p:
+        gu.run_gpu(p, d, w.M, w.N, fused=False)
+        torch.cuda.synchronize()
+        ap = p.read_workspace(mxa2a.MXA2A_WS_APACKED).reshape(w.M, w.K)
+    assert np.array_equal(ap, np.concatenate([a.numpy() for a in x["A_seg"]], axis=1))
+
+
+# --- error handling ---------------------------------------------------------------------------
+
+def test_create_rejects_bad_shapes():
+    with pytest.raises(mxa2a.Mxa2aError) as e:
+        mxa2a.Plan(2, 0, 128, 256, 64, 2)
+    assert e.value.code == mxa2a.MXA2A_ERR_INVALID_SHAPE
+    with pytest.raises(mxa2a.Mxa2aError) as e:
+        mxa2a.Plan(2, 100, 128, 256, 64, 2)
+    assert e.value.code == mxa2a.MXA2A_ERR_INVALID_SHAPE
+
+
+def test_run_rejects_misaligned_pointers():
+    w = inputs.workload(0)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w) as p:
+        C = torch.empty((w.M * w.N + 8,), dtype=torch.int16, device="cuda")
+        with pytest.raises(mxa2a.Mxa2aError) as e:
+            p.run(d["A_seg"], d["A_scale_seg"], d["B"], d["B_scale"], C.data_ptr() + 2)
+        assert e.value.code == mxa2a.MXA2A_ERR_MISALIGNED
+
+
+# --- full-size workloads: sampled rows, all columns ---------------------------------------
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4])
+def test_full_size_workloads_sampled(idx):
+    w = inputs.workload(idx)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    rows = gu.sample_rows(w.M, 40 if w.M > 64 else w.M, seed=idx)
+    with _plan(w, timeout_ns=2_000_000_000) as p:
+        Cf = gu.run_gpu(p, d, w.M, w.N, fused=True)
+        Cu = gu.run_gpu(p, d, w.M, w.N, fused=False)
+        torch.cuda.synchronize()
+        _status_ok(p)
+        got_f = gu.host_bits(Cf)
+        got_u = gu.host_bits(Cu)
+    ref = oracle.gemm(x["A_seg"], x["A_scale_seg"], x["B"], x["B_scale"], rows=rows)
+    gu.assert_parity(got_f[rows], ref, f"{w.name} fused sampled {len(rows)} rows")
+    assert np.array_equal(got_f, got_u), "fused and unfused differ"
+    # every output written (no NaN left from the 0xFFFF fill), magnitudes sane
+    assert not np.isnan(gu.bits_to_f64(got_f)).any()
