@@ -92,8 +92,12 @@ struct mxa2a_plan {
     CUtensorMap tmap_ring, tmap_apacked, tmap_b;
     const void* tmap_b_ptr = nullptr;
     unsigned long long launch_id = 0, checked_launch = 0;
-    cudaEvent_t ev0 = nullptr, ev1 = nullptr;
-    bool ev_recorded = false;
+    // ring of (start, end) events around the main GEMM kernel of the last runs
+    static constexpr int kEvRing = 4096;
+    cudaEvent_t* ev0 = nullptr;
+    cudaEvent_t* ev1 = nullptr;
+    int ev_count = 0;       // events created
+    long long ev_recorded = 0;   // runs recorded since the option was set
     int last_launches = 0;
     // host-buffer path
     uint8_t* io = nullptr;
@@ -240,14 +244,15 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
         if ((rc = cuda_rc(launch_pack_a(g, p->a_packed, 0, stream)))) return rc;
         ++launches;
     }
-    if (p->record_events && (rc = cuda_rc(cudaEventRecord(p->ev0, stream)))) return rc;
+    const int ev_slot = p->record_events ? (int)(p->ev_recorded % p->record_events) : 0;
+    if (p->record_events && (rc = cuda_rc(cudaEventRecord(p->ev0[ev_slot], stream)))) return rc;
     rc = cuda_rc(launch_mxgemm(g, fused ? p->tmap_ring : p->tmap_apacked, p->tmap_b,
                                fused ? p->grid_fused : p->grid_unfused, fused, stream));
     if (rc) return rc;
     ++launches;
     if (p->record_events) {
-        if ((rc = cuda_rc(cudaEventRecord(p->ev1, stream)))) return rc;
-        p->ev_recorded = true;
+        if ((rc = cuda_rc(cudaEventRecord(p->ev1[ev_slot], stream)))) return rc;
+        ++p->ev_recorded;
     }
     if (p->S > 1 && !(fused && p->exchange_only)) {
         if ((rc = cuda_rc(launch_splitk_reduce(p->partial, p->S, p->M * p->N, static_cast<uint16_t*>(C), stream))))
@@ -336,7 +341,6 @@ mxa2a_plan* mxa2a_create(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t 
     bool ok = cudaMemset(p->ws + o_sfa, 0, p->sfa_bytes) == cudaSuccess &&
               cudaMemset(p->flags, 0, p->flags_bytes) == cudaSuccess &&
               cudaMemset(p->status, 0, sizeof(DevStatus)) == cudaSuccess &&
-              cudaEventCreate(&p->ev0) == cudaSuccess && cudaEventCreate(&p->ev1) == cudaSuccess &&
               ensure_partials(p) == MXA2A_OK;
     ok = ok && encode_2d(&p->tmap_ring, p->ring, (uint64_t)kPerRank, (uint64_t)buffer_num * R * commMSize,
                          (uint32_t)p->box_m);
@@ -455,9 +459,24 @@ int mxa2a_set_option(mxa2a_plan* p, int key, int64_t v) {
             p->rotate = (int)v;
             return MXA2A_OK;
         case MXA2A_OPT_RECORD_EVENTS:
-            if (v != 0 && v != 1) return MXA2A_ERR_INVALID_OPTION;
+            if (v < 0 || v > mxa2a_plan::kEvRing) return MXA2A_ERR_INVALID_OPTION;
+            if (v > p->ev_count) {
+                if (!p->ev0) {
+                    p->ev0 = new (std::nothrow) cudaEvent_t[mxa2a_plan::kEvRing]();
+                    p->ev1 = new (std::nothrow) cudaEvent_t[mxa2a_plan::kEvRing]();
+                    if (!p->ev0 || !p->ev1) return MXA2A_ERR_CUDA;
+                }
+                for (int i = p->ev_count; i < v; ++i) {
+                    if (cudaEventCreate(&p->ev0[i]) != cudaSuccess) return MXA2A_ERR_CUDA;
+                    if (cudaEventCreate(&p->ev1[i]) != cudaSuccess) {
+                        cudaEventDestroy(p->ev0[i]);
+                        return MXA2A_ERR_CUDA;
+                    }
+                    p->ev_count = i + 1;
+                }
+            }
             p->record_events = (int)v;
-            p->ev_recorded = false;
+            p->ev_recorded = 0;
             return MXA2A_OK;
         case MXA2A_OPT_EXCHANGE_ONLY:
             if (v != 0 && v != 1) return MXA2A_ERR_INVALID_OPTION;
@@ -513,10 +532,25 @@ int mxa2a_get_option(mxa2a_plan* p, int key, int64_t* v) {
 }
 
 int mxa2a_last_kernel_ms(mxa2a_plan* p, float* ms) {
-    if (!p || !ms) return MXA2A_ERR_NULL_PTR;
-    if (!p->record_events || !p->ev_recorded) return MXA2A_ERR_INVALID_OPTION;
-    if (cudaEventSynchronize(p->ev1) != cudaSuccess) return MXA2A_ERR_CUDA;
-    return cudaEventElapsedTime(ms, p->ev0, p->ev1) == cudaSuccess ? MXA2A_OK : MXA2A_ERR_CUDA;
+    int n = 0;
+    return mxa2a_kernel_times(p, ms, 1, &n);
+}
+
+int mxa2a_kernel_times(mxa2a_plan* p, float* ms, int max_count, int* count) {
+    if (!p || !ms || !count) return MXA2A_ERR_NULL_PTR;
+    *count = 0;
+    if (!p->record_events || p->ev_recorded == 0 || max_count < 1) return MXA2A_ERR_INVALID_OPTION;
+    const long long avail = std::min<long long>(p->ev_recorded, p->record_events);
+    const int n = (int)std::min<long long>(avail, max_count);
+    for (int i = 0; i < n; ++i) {
+        // oldest first among the last n runs
+        const long long run = p->ev_recorded - n + i;
+        const int slot = (int)(run % p->record_events);
+        if (cudaEventSynchronize(p->ev1[slot]) != cudaSuccess) return MXA2A_ERR_CUDA;
+        if (cudaEventElapsedTime(&ms[i], p->ev0[slot], p->ev1[slot]) != cudaSuccess) return MXA2A_ERR_CUDA;
+    }
+    *count = n;
+    return MXA2A_OK;
 }
 
 int mxa2a_read_workspace(mxa2a_plan* p, int which, void* dst, size_t bytes, size_t* bytes_out) {
@@ -555,8 +589,12 @@ void mxa2a_destroy(mxa2a_plan* p) {
     if (p->ws) cudaFree(p->ws);
     if (p->partial) cudaFree(p->partial);
     if (p->io) cudaFree(p->io);
-    if (p->ev0) cudaEventDestroy(p->ev0);
-    if (p->ev1) cudaEventDestroy(p->ev1);
+    for (int i = 0; i < p->ev_count; ++i) {
+        cudaEventDestroy(p->ev0[i]);
+        cudaEventDestroy(p->ev1[i]);
+    }
+    delete[] p->ev0;
+    delete[] p->ev1;
     if (prev >= 0 && prev != p->device) cudaSetDevice(prev);
     delete p;
 }

@@ -84,6 +84,8 @@ _SIGS = [
     ("mxa2a_set_option", ctypes.c_int, [_VP, ctypes.c_int, _I64]),
     ("mxa2a_get_option", ctypes.c_int, [_VP, ctypes.c_int, ctypes.POINTER(_I64)]),
     ("mxa2a_last_kernel_ms", ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_float)]),
+    ("mxa2a_kernel_times", ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_float), ctypes.c_int,
+                                          ctypes.POINTER(ctypes.c_int)]),
     ("mxa2a_read_workspace", ctypes.c_int, [_VP, ctypes.c_int, _VP, ctypes.c_size_t,
                                             ctypes.POINTER(ctypes.c_size_t)]),
     ("mxa2a_l2_flush", ctypes.c_int, [_VP, ctypes.c_size_t, _VP]),
@@ -198,6 +200,13 @@ def mxa2a_last_kernel_ms(plan) -> float:
     return v.value
 
 
+def mxa2a_kernel_times(plan, max_count: int) -> list:
+    buf = (ctypes.c_float * max_count)()
+    n = ctypes.c_int()
+    _check(load().mxa2a_kernel_times(plan, buf, max_count, ctypes.byref(n)), "mxa2a_kernel_times")
+    return list(buf[:n.value])
+
+
 def mxa2a_read_workspace(plan, which: int):
     import numpy as np
     n = ctypes.c_size_t()
@@ -248,6 +257,9 @@ class Plan:
 
     def last_kernel_ms(self) -> float:
         return mxa2a_last_kernel_ms(self.handle)
+
+    def kernel_times(self, max_count: int) -> list:
+        return mxa2a_kernel_times(self.handle, max_count)
 
     def read_workspace(self, which):
         return mxa2a_read_workspace(self.handle, which)

@@ -1,0 +1,405 @@
+"""Benchmark of the fused AllToAll + MXFP8 block-scaled GEMM (libmxa2a) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME_OR_INDEX] [--path fused|unfused]
+
+A step is one pass of the whole hot path (B-scale pack + the fused staging /
+block-scaled GEMM kernel [+ split-K reduce]) over one batch of synthetic
+inputs already resident in HBM.  Before every step the L2 is flushed (a write
+of twice its size); the flush sits outside the per-step CUDA events, which are
+recorded on the launch stream around the library call.  Rank 0 prints one
+JSON line.
+
+With N > 1 (torchrun), every rank runs its own replica on its own GPU (the
+path has no cross-GPU exchange on a one-GPU-per-box pool: the R segments are
+local buffers); ranks are barrier-aligned, the slowest rank's time counts and
+``value`` is the job's total TFLOP/s ("scaling": "weak").
+
+``--impl reference`` times the CPU oracle (exact integer accumulation, the
+correctness reference) on the host cores instead, on a bounded sample of the
+same workload, and prints the same line with ``"impl": "reference"``.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused MXFP8 a2a-GEMM TFLOP/s and % of roofline (1 GB300)"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = 1          # the 4-segment 2048 x 4096 x 4096 problem
+FP8_OVER_BF16 = 2.0           # nominal dense fp8 : bf16 tensor rate (4.5 : 2.25 PFLOP/s)
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["mxgemm.cu", "kernels.cuh", "ptx.cuh"]
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max_sum(t_local: float, work_local: float, device=None):
+    """(max over ranks of t, sum over ranks of work) with torch.distributed;
+    identity when no process group is initialised."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return t_local, work_local
+    t = torch.tensor([t_local], dtype=torch.float64, device=device)
+    w = torch.tensor([work_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(w, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(w.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "all_mxfp8_block_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
+    or None when there is none or the kernel sources changed since."""
+    path = os.path.join(ROOT, "profiles", f"mxgemm_fused_{workload_name}.md")
+    try:
+        txt = open(path).read()
+    except OSError:
+        return None
+    m_t = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)
+    m_h = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", txt)
+    if not m_t or not m_h or m_h.group(1) != kernel_source_hash():
+        return None
+    return int(m_t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = open(f"/tmp/mxa2a_clocks_{os.getpid()}.csv", "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.period), "-i", str(self.gpu)],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.out:
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == len(self.FIELDS):
+                    rows.append(parts)
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+def roofline_terms(w, p_tflops: float, bw_gbs: float):
+    t_flop = w.flops / (p_tflops * 1e12)
+    t_bytes = w.bytes_alg / (bw_gbs * 1e9)
+    return max(t_flop, t_bytes), ("tensor" if t_flop >= t_bytes else "hbm")
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) arm
+def time_oracle(w, x, seconds: float = 12.0, max_rows: int | None = None):
+    """Time the CPU oracle on rows 0..r-1 of C (all columns, full K), r grown
+    until one call takes about `seconds`.  Returns (TFLOP/s, rows, secs, cores)."""
+    import oracle
+    rows = 8
+    cores = os.cpu_count() or 1
+    while True:
+        t0 = time.perf_counter()
+        oracle.gemm(x["A_seg"], x["A_scale_seg"], x["B"], x["B_scale"], rows=list(range(rows)))
+        dt = time.perf_counter() - t0
+        cap = w.M if max_rows is None else min(w.M, max_rows)
+        if dt >= seconds * 0.5 or rows >= cap:
+            return 2.0 * rows * w.N * w.K / dt / 1e12, rows, dt, cores
+        rows = min(cap, max(rows + 1, int(rows * min(8.0, seconds / max(dt, 1e-3)))))
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from all_mxfp8_block_gb300 import inputs
+    import oracle
+    oracle.build()
+    x = inputs.make_inputs(w)
+    # size one step to roughly 1.5 s of oracle work
+    _, rows, dt, cores = time_oracle(w, x, seconds=1.5)
+    for _ in range(args.warmup):
+        oracle.gemm(x["A_seg"], x["A_scale_seg"], x["B"], x["B_scale"], rows=list(range(rows)))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm(x["A_seg"], x["A_scale_seg"], x["B"], x["B_scale"], rows=list(range(rows)))
+    total = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K
+    value = flops * args.steps / total / 1e12
+    sample = f"rows 0..{rows - 1} of C ({rows} x {w.N} outputs, full K={w.K}) per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64-exact",
+        "data": "synthetic",
+        "config": {"workload": w.name, "R": w.R, "M": w.M, "kPerRank": w.kPerRank, "K": w.K, "N": w.N,
+                   "commMSize": w.commMSize, "buffer_num": w.buffer_num, "seed": w.seed,
+                   "path": "cpu oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+    from all_mxfp8_block_gb300 import build as mxbuild
+    from all_mxfp8_block_gb300 import inputs, mxa2a
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0:
+        mxbuild.build()
+    if ws > 1:
+        dist.barrier()
+    mxa2a.load()
+
+    x = inputs.make_inputs(w)
+    dA = [a.to(dev) for a in x["A_seg"]]
+    dS = [s.to(dev) for s in x["A_scale_seg"]]
+    dB, dBs = x["B"].to(dev), x["B_scale"].to(dev)
+    C = torch.empty((w.M, w.N), dtype=torch.int16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_bytes = max(2 * l2, 64 << 20) // 16 * 16
+    flush = torch.zeros(flush_bytes // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    plan = mxa2a.Plan(w.R, w.M, w.kPerRank, w.N, w.commMSize, w.buffer_num)
+    plan.set_option(mxa2a.MXA2A_OPT_RECORD_EVENTS, min(4096, max(1, args.steps)))
+    run = plan.run if args.path == "fused" else plan.run_unfused
+
+    def timed_loop(fn, steps, warmup, sampler=None):
+        for _ in range(warmup):
+            mxa2a.mxa2a_l2_flush(flush, flush_bytes, stream)
+            fn(dA, dS, dB, dBs, C, stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        ctx = sampler if sampler is not None else _Null()
+        with ctx:
+            for i in range(steps):
+                mxa2a.mxa2a_l2_flush(flush, flush_bytes, stream)
+                ev[i][0].record(stream)
+                fn(dA, dS, dB, dBs, C, stream)
+                ev[i][1].record(stream)
+            torch.cuda.synchronize(dev)
+        if ws > 1:
+            dist.barrier()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    sampler = ClockSampler(local)
+    step_ms = timed_loop(run, args.steps, args.warmup, sampler)
+    launches_per_run = plan.get_option(mxa2a.MXA2A_INFO_LAUNCHES)
+    kern_ms = plan.kernel_times(min(4096, args.steps))
+    st = plan.status()
+    if st["code"] != 0:
+        raise RuntimeError(f"device status after the timed region: {st}")
+    clocks = sampler.summary()
+
+    # the other variant, same caliber, for the fused-vs-unfused comparison
+    other = plan.run_unfused if args.path == "fused" else plan.run
+    other_steps = min(args.steps, 500)
+    other_ms = timed_loop(other, other_steps, args.warmup)
+
+    t_local = sum(step_ms) / 1e3
+    t_max, flops_total = reduce_max_sum(t_local, float(w.flops) * args.steps, dev if ws > 1 else None)
+    value = flops_total / t_max / 1e12
+    ms_per_step = t_max / args.steps * 1e3
+
+    # end to end through the C ABI with pinned host buffers (copies in the timed region)
+    e2e = None
+    if not args.no_e2e:
+        hA = [a.pin_memory() for a in x["A_seg"]]
+        hS = [s.pin_memory() for s in x["A_scale_seg"]]
+        hB, hBs = x["B"].pin_memory(), x["B_scale"].pin_memory()
+        hC = torch.empty((w.M, w.N), dtype=torch.int16).pin_memory()
+        e2e_steps = min(args.steps, 50)
+        for _ in range(max(3, args.warmup)):
+            plan.run_host(hA, hS, hB, hBs, hC, stream)
+        torch.cuda.synchronize(dev)
+        if ws > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            plan.run_host(hA, hS, hB, hBs, hC, stream)
+            stream.synchronize()
+        t_e2e = time.perf_counter() - t0
+        if ws > 1:
+            dist.barrier()
+        t_e2e_max, fl = reduce_max_sum(t_e2e, float(w.flops) * e2e_steps, dev if ws > 1 else None)
+        h2d = (sum(a.numel() for a in hA) + sum(s.numel() for s in hS) + hB.numel() + hBs.numel())
+        e2e = {"value": fl / t_e2e_max / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(hC.numel() * 2),
+               "timer": "host wall clock per step (h2d copies + run + d2h copy + stream sync)",
+               "steps": e2e_steps}
+
+    bf16_tf, hbm, peak_src = measured_peaks()
+    p_fp8 = bf16_tf * FP8_OVER_BF16
+    t_roof, bound = roofline_terms(w, p_fp8, hbm)
+    kern_avg_s = (sum(kern_ms) / len(kern_ms) / 1e3) if kern_ms else None
+    achieved = w.flops / kern_avg_s / 1e12 if kern_avg_s else None
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
+
+    cpu = None
+    if not args.no_cpu_baseline and ws >= 1:
+        tf, rows, dt, cores = time_oracle(w, x, seconds=args.cpu_seconds)
+        cpu = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"rows 0..{rows - 1} of C ({rows} x {w.N} outputs, full K={w.K}), one call, "
+                         f"{dt:.1f} s wall"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "mxfp8", "data": "synthetic",
+        "config": {"workload": w.name, "R": w.R, "M": w.M, "kPerRank": w.kPerRank, "K": w.K, "N": w.N,
+                   "commMSize": w.commMSize, "buffer_num": w.buffer_num, "seed": w.seed,
+                   "path": args.path, "parallelism": "replicas" if ws > 1 else "single",
+                   "splits": plan.get_option(mxa2a.MXA2A_INFO_SPLITS),
+                   "grid": plan.get_option(mxa2a.MXA2A_INFO_GRID_FUSED if args.path == "fused"
+                                           else mxa2a.MXA2A_INFO_GRID_UNFUSED),
+                   "l2": f"flushed before every step ({flush_bytes >> 20} MiB write, 2x L2), outside the events",
+                   "timer": "CUDA events on the launch stream around each library call"},
+        "roofline_pct": 100.0 * t_roof / (ms_per_step / 1e3),
+        "roofline": {"bound": bound, "achieved": achieved, "peak": p_fp8, "unit": "TFLOP/s",
+                     "frac": (achieved / p_fp8) if achieved else None,
+                     "traffic": profiled_traffic(w.name),
+                     "kernel": "mxgemm_kernel<fused>" if args.path == "fused" else "mxgemm_kernel<unfused>",
+                     "kernel_ms_avg": kern_avg_s * 1e3 if kern_avg_s else None,
+                     "peak_note": f"{peak_src} bf16 {bf16_tf:.0f} TFLOP/s (burst) x nominal fp8:bf16 ratio 2",
+                     "t_roof_us": t_roof * 1e6, "hbm_gbs": hbm},
+        "unfused" if args.path == "fused" else "fused": {
+            "ms_per_step": sum(other_ms) / len(other_ms), "steps": other_steps,
+            "value": w.flops / (sum(other_ms) / len(other_ms) / 1e3) / 1e12},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(args.steps * (1 + launches_per_run)),
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    plan.destroy()
+    return 0
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=str(DEFAULT_WORKLOAD))
+    ap.add_argument("--path", choices=["fused", "unfused"], default="fused")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from all_mxfp8_block_gb300 import inputs
+    w = inputs.workload(int(args.workload)) if args.workload.isdigit() else inputs.workload(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -142,7 +142,8 @@ enum mxa2a_option {
     MXA2A_OPT_SPLIT_K = 2,         /* 0 = automatic, s >= 1: split K into s segment groups */
     MXA2A_OPT_ZIGZAG = 3,          /* 1 (default): alternate n-tile direction per m-tile */
     MXA2A_OPT_ROTATE = 4,          /* 1 (default): start each tile's K loop at a rotated segment */
-    MXA2A_OPT_RECORD_EVENTS = 5,   /* 1: time the main GEMM kernel of each run (mxa2a_last_kernel_ms) */
+    MXA2A_OPT_RECORD_EVENTS = 5,   /* n >= 1: time the main GEMM kernel of each run, keeping the last n
+                                      (n <= 4096) for mxa2a_kernel_times; 0 = off (default) */
     MXA2A_OPT_EXCHANGE_ONLY = 6,   /* 1: fused runs only stage A into the ring (needs buffer_num >= steps) */
     MXA2A_OPT_FAULT_SKIP_STEP = 7, /* test knob: never publish staging step k (-1 = off); waits then time out */
     MXA2A_OPT_GRID = 8,            /* cap on persistent CTAs (0 = one per SM) */
@@ -166,8 +167,13 @@ int mxa2a_set_option(mxa2a_plan *plan, int key, int64_t value);
 int mxa2a_get_option(mxa2a_plan *plan, int key, int64_t *value);
 
 /* Duration of the main GEMM kernel of the last run, in ms (needs
- * MXA2A_OPT_RECORD_EVENTS = 1; synchronises on that run's end event). */
+ * MXA2A_OPT_RECORD_EVENTS >= 1; synchronises on that run's end event). */
 int mxa2a_last_kernel_ms(mxa2a_plan *plan, float *ms);
+
+/* Durations (ms) of the main GEMM kernel of the last min(max_count, recorded)
+ * runs, oldest first, timed with CUDA events on each run's stream; *count
+ * receives how many were written.  Synchronises on those runs' end events. */
+int mxa2a_kernel_times(mxa2a_plan *plan, float *ms, int max_count, int *count);
 
 /* Workspace regions readable with mxa2a_read_workspace (debug and tests). */
 enum mxa2a_workspace {
