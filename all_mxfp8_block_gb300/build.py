@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmxa2a.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["mxgemm.cu", "aux_kernels.cu", "mxa2a_api.cu"]
+SOURCES = ["mxgemm.cu", "aux_kernels.cu", "mxa2a_api.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-Xptxas", "-v",
          f"-I{os.path.join(ROOT, 'include')}"]

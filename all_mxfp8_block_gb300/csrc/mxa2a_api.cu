@@ -611,6 +611,7 @@ const char* mxa2a_strerror(int code) {
         case MXA2A_ERR_INVALID_OPTION: return "invalid option";
         case MXA2A_ERR_DEVICE_CHECK: return "device consistency check failed";
         case MXA2A_ERR_WRONG_DEVICE: return "current device differs from the plan's device";
+        case MXA2A_ERR_SCRATCH_TOO_SMALL: return "problem needs more scratch than the allocation-free entry point holds";
         default: return "unknown error";
     }
 }

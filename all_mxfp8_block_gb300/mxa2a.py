@@ -25,6 +25,7 @@ MXA2A_ERR_TIMEOUT = 6
 MXA2A_ERR_INVALID_OPTION = 7
 MXA2A_ERR_DEVICE_CHECK = 8
 MXA2A_ERR_WRONG_DEVICE = 9
+MXA2A_ERR_SCRATCH_TOO_SMALL = 10
 
 MXA2A_OPT_TIMEOUT_NS = 1
 MXA2A_OPT_SPLIT_K = 2
@@ -89,6 +90,8 @@ _SIGS = [
     ("mxa2a_read_workspace", ctypes.c_int, [_VP, ctypes.c_int, _VP, ctypes.c_size_t,
                                             ctypes.POINTER(ctypes.c_size_t)]),
     ("mxa2a_l2_flush", ctypes.c_int, [_VP, ctypes.c_size_t, _VP]),
+    ("mxa2a_run_noalloc", ctypes.c_int, [ctypes.c_int, _I64, _I64, _I64, _I64, ctypes.c_int, _PP, _PP, _VP,
+                                         _VP, _VP, _VP]),
     ("mxa2a_destroy", None, [_VP]),
     ("mxa2a_strerror", ctypes.c_char_p, [ctypes.c_int]),
 ]
@@ -218,6 +221,15 @@ def mxa2a_read_workspace(plan, which: int):
 
 def mxa2a_l2_flush(buf, nbytes: int, stream=None) -> None:
     _check(load().mxa2a_l2_flush(_ptr(buf), nbytes, _stream(stream)), "mxa2a_l2_flush")
+
+
+def mxa2a_run_noalloc(R, M, kPerRank, N, commMSize, buffer_num, A_seg, A_scale_seg, B, B_scale, C_bf16,
+                      stream=None) -> None:
+    """The fused path without any device allocation (static scratch inside the
+    library; see include/mxa2a.h for its size limit and sharing rules)."""
+    _check(load().mxa2a_run_noalloc(R, M, kPerRank, N, commMSize, buffer_num, _ptr_array(A_seg),
+                                    _ptr_array(A_scale_seg), _ptr(B), _ptr(B_scale), _ptr(C_bf16),
+                                    _stream(stream)), "mxa2a_run_noalloc")
 
 
 def mxa2a_destroy(plan) -> None:

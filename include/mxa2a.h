@@ -56,7 +56,8 @@ enum mxa2a_error {
     MXA2A_ERR_TIMEOUT = 6,            /* device: a bounded wait ran out (get_status) */
     MXA2A_ERR_INVALID_OPTION = 7,     /* unknown option key or value out of range */
     MXA2A_ERR_DEVICE_CHECK = 8,       /* device: an internal consistency check failed */
-    MXA2A_ERR_WRONG_DEVICE = 9        /* current device differs from the plan's */
+    MXA2A_ERR_WRONG_DEVICE = 9,       /* current device differs from the plan's */
+    MXA2A_ERR_SCRATCH_TOO_SMALL = 10  /* mxa2a_run_noalloc: the problem needs more than its static scratch */
 };
 
 typedef struct mxa2a_plan mxa2a_plan;   /* opaque */
@@ -192,6 +193,32 @@ int mxa2a_read_workspace(mxa2a_plan *plan, int which, void *host_dst, size_t byt
 /* Benchmark helper: add 1 to every 32-bit word of a device buffer (bytes %
  * 16 == 0), evicting other data from L2 when bytes exceeds its size. */
 int mxa2a_l2_flush(void *device_buf, size_t bytes, void *stream);
+
+/*
+ * The fused path for callers that cannot allocate device memory — a runtime
+ * whose device memory is entirely budgeted by its own pool allocator (a
+ * library's cudaMalloc can fail or fragment it there), or a latency-critical
+ * loop where cudaMalloc / cudaFree would implicitly synchronise the device.
+ * The pages have no counterpart of this entry point; it is a deployment
+ * variant of mxa2a_run.
+ *
+ * Same shape rules, data layouts and result as mxa2a_run (no plan, no K
+ * split).  It allocates nothing: the staging ring, scale tiles, credit
+ * counters and status block live in one static device array of 16 MiB that
+ * every GPU which loads this library holds until the process exits.  A shape
+ * whose ring + scale tiles + counters exceed it returns
+ * MXA2A_ERR_SCRATCH_TOO_SMALL before any device work (the ring alone is
+ * buffer_num * R * commMSize * kPerRank bytes).  The first call on a device
+ * looks up the array's device address once; make that first call before any
+ * stream capture begins.  Every call reuses the same array (the counters are
+ * cleared on the stream at the start of each call), so calls that overlap on
+ * the GPU — on two streams, or from two host threads — race.  Device-side
+ * wait time-outs are not reported by this entry point.  Asynchronous on
+ * stream (a cudaStream_t, NULL = legacy default stream).
+ */
+int mxa2a_run_noalloc(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t commMSize, int buffer_num,
+                      const void *const *A_seg, const void *const *A_scale_seg, const void *B, const void *B_scale,
+                      void *C_bf16, void *stream);
 
 /* Free the plan's workspace (synchronises the device first). NULL is a no-op. */
 void mxa2a_destroy(mxa2a_plan *plan);
