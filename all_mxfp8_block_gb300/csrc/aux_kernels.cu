@@ -1,5 +1,5 @@
 // Memory-bound helper kernels of libmxa2a: scale-factor packing, the unfused
-// pack of A, the split-K reduction and the benchmark's L2 flush.
+// pack of A and the benchmark's L2 flush.
 //
 // Scale-factor "atom" layout used by the MMA: for every 128-wide K block and
 // every group of 128 rows (of A) or columns (of B), 512 bytes in which the 4
@@ -10,8 +10,6 @@
 // scale of row/column 32c + x%32.  The pages' scale operands are the E8M0
 // tensors scaleA / scaleB (all_to_all_matmul_impl.h, LayoutScaleA/B with byte
 // pairs SCALE_C0 = 2): the same bytes in the hardware's own order.
-#include <cuda_bf16.h>
-
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -66,28 +64,6 @@ __global__ void pack_a_kernel(const __grid_constant__ GemmParams p, uint8_t* __r
     }
 }
 
-// C = bf16(sum_q partial[q]) in the fixed order q = 0..S-1.
-__global__ void splitk_reduce_kernel(const float* __restrict__ partial, int S, long long MN, uint16_t* __restrict__ C) {
-    const long long n4 = MN / 4;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
-         i += (long long)gridDim.x * blockDim.x) {
-        float4 acc = reinterpret_cast<const float4*>(partial)[i];
-        for (int q = 1; q < S; ++q) {
-            const float4 v = reinterpret_cast<const float4*>(partial + (size_t)q * MN)[i];
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
-        }
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-        uint2 out;
-        out.x = *reinterpret_cast<const uint32_t*>(&lo);
-        out.y = *reinterpret_cast<const uint32_t*>(&hi);
-        reinterpret_cast<uint2*>(C)[i] = out;
-    }
-}
-
 __global__ void l2_flush_kernel(uint4* buf, long long n16) {
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n16;
          i += (long long)gridDim.x * blockDim.x) {
@@ -117,11 +93,6 @@ cudaError_t launch_pack_sfb(const uint8_t* B_scale, int N, int K, int Ng2, uint8
 cudaError_t launch_pack_a(const GemmParams& p, uint8_t* a_packed, int grid, cudaStream_t stream) {
     const long long work = (long long)p.M * p.K / 16;
     pack_a_kernel<<<grid > 0 ? grid : grid_for(work, 256), 256, 0, stream>>>(p, a_packed);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_splitk_reduce(const float* partial, int S, long long MN, uint16_t* C, cudaStream_t stream) {
-    splitk_reduce_kernel<<<grid_for(MN / 4, 256), 256, 0, stream>>>(partial, S, MN, C);
     return cudaGetLastError();
 }
 

@@ -14,11 +14,13 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 128;
 constexpr int kStages = 4;
-constexpr int kThreads = 256;      // 8 warps, roles below
+constexpr int kThreads = 384;      // 12 warps, roles below
 constexpr int kWarpTma = 0;        // TMA producer (one elected lane)
 constexpr int kWarpMma = 1;        // TMEM allocator + MMA issuer (one elected lane)
-constexpr int kWarpEpi0 = 2;       // warps 2..5: epilogue, one TMEM lane quarter each
-constexpr int kWarpCopy0 = 6;      // warps 6..7: staging copy (fused kernel only)
+constexpr int kWarpEpi0 = 2;       // warps 2..9: epilogue, warp w drains TMEM lane quarter w%4,
+constexpr int kEpiWarps = 8;       //   column half (w-2)/4 of the accumulator
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kWarpCopy0 = 10;     // warps 10..11: staging copy (fused kernel only)
 constexpr int kCopyThreads = 64;
 
 constexpr int kAStageBytes = BM * BK;        // 16 KiB
@@ -46,15 +48,19 @@ struct DevStatus {
 };
 
 // Monotonic credit counters of the staging ring, each on its own 128-byte line.
-// filled[slot][r]: staging copy chunks published for (slot, segment)
-// drained[slot]:   GEMM work items that finished reading the slot
-// cta_done:        CTAs that reached the end (the last one zeroes everything)
+// filled[slot][r]:  staging copy chunks published for (slot, segment r)
+// drained[slot][r]: work items that finished reading segment r of the slot
+// cta_done:         CTAs that reached the end (the last one zeroes everything)
+// copy_next:        next staging copy task to claim (tasks are claimed in order)
 struct FlagLayout {
     static constexpr int kLine = 16;  // 16 x u64 = 128 bytes
     __host__ __device__ static size_t filled(int slot, int r, int R) { return (size_t)(slot * R + r) * kLine; }
-    __host__ __device__ static size_t drained(int slot, int bn, int R) { return (size_t)(bn * R + slot) * kLine; }
-    __host__ __device__ static size_t cta_done(int bn, int R) { return (size_t)(bn * R + bn) * kLine; }
-    __host__ __device__ static size_t words(int bn, int R) { return (size_t)(bn * R + bn + 1) * kLine; }
+    __host__ __device__ static size_t drained(int slot, int r, int bn, int R) {
+        return (size_t)(bn * R + slot * R + r) * kLine;
+    }
+    __host__ __device__ static size_t cta_done(int bn, int R) { return (size_t)(2 * bn * R) * kLine; }
+    __host__ __device__ static size_t copy_next(int bn, int R) { return (size_t)(2 * bn * R + 1) * kLine; }
+    __host__ __device__ static size_t words(int bn, int R) { return (size_t)(2 * bn * R + 2) * kLine; }
 };
 
 struct GemmParams {
@@ -66,8 +72,14 @@ struct GemmParams {
     int zigzag, rotate;
     const uint8_t* sfa;         // A scales, MMA atom layout [K/128][Mg][512]
     const uint8_t* sfb;         // B scales, MMA atom layout [K/128][Ng2][512]
-    uint16_t* C;                // bf16 [M][N] (S == 1)
-    float* partial;             // fp32 [S][M][N] (S > 1)
+    uint16_t* C;                // bf16 [M][N]
+    // split-K (S > 1): items of one output tile finish in any order; all but the
+    // last write their fp32 tile to partial[tile][q] ([BM][BN]) and publish
+    // ready[tile][q] = launch_id; the last (ticket S-1 of tile_cnt[tile]) sums
+    // q = 0..S-1 in order, writes C and zeroes tile_cnt[tile]
+    float* partial;             // fp32 [Mt*Nt][S][BN/4][BM][4] (4-column chunks, row-contiguous)
+    unsigned* tile_cnt;         // [Mt*Nt]
+    unsigned long long* ready;  // [Mt*Nt][S]
     // fused staging
     int fused, exchange_only;
     int rows_per_chunk, chunks_per_seg, n_copy_tasks;
@@ -88,7 +100,6 @@ cudaError_t launch_mxgemm(const GemmParams& p, const CUtensorMap& tmap_a, const 
 size_t mxgemm_smem_bytes();
 cudaError_t launch_pack_a(const GemmParams& p, uint8_t* a_packed, int grid, cudaStream_t stream);
 cudaError_t launch_pack_sfb(const uint8_t* B_scale, int N, int K, int Ng2, uint8_t* sfb, cudaStream_t stream);
-cudaError_t launch_splitk_reduce(const float* partial, int S, long long MN, uint16_t* C, cudaStream_t stream);
 cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t stream);
 
 }  // namespace mxa2a

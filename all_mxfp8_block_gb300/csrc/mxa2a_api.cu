@@ -73,19 +73,25 @@ struct mxa2a_plan {
     int device = 0, sm_count = 0;
     // derived
     int64_t K = 0;
-    int steps = 0, Mt = 0, Nt = 0, S = 1, W = 0, Mg = 0, Ng2 = 0, box_m = 128, span = 1;
+    int steps = 0, Mt = 0, Nt = 0, Mg = 0, Ng2 = 0, box_m = 128, span = 1;
+    int S_fused = 1, S_unfused = 1, W_fused = 0, W_unfused = 0;   // K splits and work items per path
     int rows_per_chunk = 1, chunks_per_seg = 1, n_copy_tasks = 0;
     int grid_fused = 0, grid_unfused = 0;
     // options
     int64_t timeout_ns = 2000000000LL;
-    int force_split = 0, zigzag = 1, rotate = 1, record_events = 0, exchange_only = 0;
+    int force_split = 0, zigzag = 1, rotate = 0, record_events = 0, exchange_only = 0;
     int fault_skip_step = -1, grid_cap = 0;
-    int64_t chunk_bytes = 32768;
+    int64_t chunk_bytes = 8192;
     // workspace
     uint8_t* ws = nullptr;
     size_t ws_bytes = 0;
     uint8_t *ring = nullptr, *sfa = nullptr, *sfb = nullptr, *a_packed = nullptr;
-    float* partial = nullptr;          // split-K partials, own allocation sized for the current split
+    // split-K scratch, own allocation sized for the current splits:
+    // fp32 partial tiles [Mt*Nt][S][128][256] | tile counters u32 [Mt*Nt] | ready u64 [Mt*Nt][S]
+    uint8_t* split_ws = nullptr;
+    float* partial = nullptr;
+    unsigned* tile_cnt = nullptr;
+    unsigned long long* ready = nullptr;
     unsigned long long* flags = nullptr;
     DevStatus* status = nullptr;
     size_t ring_bytes = 0, sfa_bytes = 0, sfb_bytes = 0, apacked_bytes = 0, partial_bytes = 0, flags_bytes = 0;
@@ -115,16 +121,25 @@ void derive(mxa2a_plan* p) {
     p->Ng2 = 2 * p->Nt;
     p->box_m = (p->cm % BM == 0) ? BM : 64;
     p->span = tile_span(p->M, p->cm);
-    const int tiles = p->Mt * p->Nt;
-    int S = 1;
-    if (p->force_split > 0) {
-        S = std::min(p->force_split, p->R);
-    } else if (tiles * 2 <= p->sm_count && p->K >= 1024) {
-        S = std::min<int>(p->R, p->sm_count / tiles);
-        while (S > 1 && p->K / S < 512) --S;
-    }
-    p->S = std::max(1, S);
-    p->W = tiles * p->S;
+    // K split: enough work items to fill the GPU.  The fused path can only
+    // work on the output tiles whose rows sit in the staging ring at once
+    // (buffer_num * commMSize rows), the unfused path on all tiles.
+    // Split only when the tiles fill at most a quarter of the GPU: the in-kernel
+    // reduction of the partials costs more than a partly idle GPU otherwise.
+    auto split_for = [&](int tiles) {
+        if (p->force_split > 0) return std::min(p->force_split, p->R);
+        int S = 1;
+        if (tiles * 4 <= p->sm_count && p->K >= 1024) {
+            S = std::min<int>(p->R, p->sm_count / tiles);
+            while (S > 1 && p->K / S < 512) --S;
+        }
+        return std::max(1, S);
+    };
+    const int window_mtiles = (int)std::min<int64_t>(p->Mt, (p->bn * p->cm + BM - 1) / BM);
+    p->S_fused = split_for(window_mtiles * p->Nt);
+    p->S_unfused = split_for(p->Mt * p->Nt);
+    p->W_fused = p->Mt * p->Nt * p->S_fused;
+    p->W_unfused = p->Mt * p->Nt * p->S_unfused;
     // staging copy chunk: the largest divisor of commMSize rows within chunk_bytes
     int64_t want = std::max<int64_t>(1, p->chunk_bytes / p->ka);
     int rpc = 1;
@@ -135,8 +150,8 @@ void derive(mxa2a_plan* p) {
     p->n_copy_tasks = p->steps * p->R * p->chunks_per_seg;
     int cap = p->sm_count;
     if (p->grid_cap > 0) cap = std::min(cap, p->grid_cap);
-    p->grid_fused = std::max(1, std::min(cap, std::max(p->W, p->n_copy_tasks)));
-    p->grid_unfused = std::max(1, std::min(cap, p->W));
+    p->grid_fused = std::max(1, std::min(cap, std::max(p->W_fused, p->n_copy_tasks)));
+    p->grid_unfused = std::max(1, std::min(cap, p->W_unfused));
 }
 
 bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
@@ -172,8 +187,8 @@ void fill_params(mxa2a_plan* p, GemmParams& g, const void* const* A_seg, const v
     g.steps = p->steps;
     g.Mt = p->Mt;
     g.Nt = p->Nt;
-    g.S = p->S;
-    g.W = p->W;
+    g.S = fused ? p->S_fused : p->S_unfused;
+    g.W = fused ? p->W_fused : p->W_unfused;
     g.kb_per_seg = (int)(p->ka / BK);
     g.Mg = p->Mg;
     g.Ng2 = p->Ng2;
@@ -184,6 +199,8 @@ void fill_params(mxa2a_plan* p, GemmParams& g, const void* const* A_seg, const v
     g.sfb = p->sfb;
     g.C = static_cast<uint16_t*>(C);
     g.partial = p->partial;
+    g.tile_cnt = p->tile_cnt;
+    g.ready = p->ready;
     g.fused = fused ? 1 : 0;
     g.exchange_only = fused ? p->exchange_only : 0;
     g.rows_per_chunk = p->rows_per_chunk;
@@ -211,17 +228,30 @@ int refresh_b_map(mxa2a_plan* p, const void* B) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MXA2A_OK : MXA2A_ERR_CUDA; }
 
-// (Re)allocate the split-K partial buffer for the plan's current split.
+// (Re)allocate the split-K scratch for the plan's current splits (zeroed).
 int ensure_partials(mxa2a_plan* p) {
-    const size_t need = p->S > 1 ? (size_t)p->S * p->M * p->N * sizeof(float) : 0;
+    const int S = std::max(p->S_fused, p->S_unfused);
+    if (S <= 1) return MXA2A_OK;
+    const size_t tiles = (size_t)p->Mt * p->Nt;
+    const size_t part = tiles * S * BM * BN * sizeof(float);
+    const size_t cnt = align_up(tiles * sizeof(unsigned), 256);
+    const size_t rdy = tiles * S * sizeof(unsigned long long);
+    const size_t need = part + cnt + rdy;
     if (need <= p->partial_bytes) return MXA2A_OK;
-    if (p->partial) cudaFree(p->partial);
+    if (p->split_ws) cudaFree(p->split_ws);
+    p->split_ws = nullptr;
     p->partial = nullptr;
     p->partial_bytes = 0;
-    if (cudaMalloc(reinterpret_cast<void**>(&p->partial), need) != cudaSuccess) {
+    if (cudaMalloc(reinterpret_cast<void**>(&p->split_ws), need) != cudaSuccess ||
+        cudaMemset(p->split_ws + part, 0, cnt + rdy) != cudaSuccess) {
         cudaGetLastError();
+        if (p->split_ws) cudaFree(p->split_ws);
+        p->split_ws = nullptr;
         return MXA2A_ERR_CUDA;
     }
+    p->partial = reinterpret_cast<float*>(p->split_ws);
+    p->tile_cnt = reinterpret_cast<unsigned*>(p->split_ws + part);
+    p->ready = reinterpret_cast<unsigned long long*>(p->split_ws + part + cnt);
     p->partial_bytes = need;
     return MXA2A_OK;
 }
@@ -253,11 +283,6 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
     if (p->record_events) {
         if ((rc = cuda_rc(cudaEventRecord(p->ev1[ev_slot], stream)))) return rc;
         ++p->ev_recorded;
-    }
-    if (p->S > 1 && !(fused && p->exchange_only)) {
-        if ((rc = cuda_rc(launch_splitk_reduce(p->partial, p->S, p->M * p->N, static_cast<uint16_t*>(C), stream))))
-            return rc;
-        ++launches;
     }
     p->last_launches = launches;
     return MXA2A_OK;
@@ -517,8 +542,9 @@ int mxa2a_get_option(mxa2a_plan* p, int key, int64_t* v) {
         case MXA2A_INFO_STEPS: *v = p->steps; break;
         case MXA2A_INFO_MTILES: *v = p->Mt; break;
         case MXA2A_INFO_NTILES: *v = p->Nt; break;
-        case MXA2A_INFO_SPLITS: *v = p->S; break;
-        case MXA2A_INFO_ITEMS: *v = p->W; break;
+        case MXA2A_INFO_SPLITS: *v = p->S_fused; break;
+        case MXA2A_INFO_ITEMS: *v = p->W_fused; break;
+        case MXA2A_INFO_SPLITS_UNFUSED: *v = p->S_unfused; break;
         case MXA2A_INFO_GRID_FUSED: *v = p->grid_fused; break;
         case MXA2A_INFO_GRID_UNFUSED: *v = p->grid_unfused; break;
         case MXA2A_INFO_COPY_TASKS: *v = p->n_copy_tasks; break;
@@ -587,7 +613,7 @@ void mxa2a_destroy(mxa2a_plan* p) {
     if (prev != p->device) cudaSetDevice(p->device);
     cudaDeviceSynchronize();
     if (p->ws) cudaFree(p->ws);
-    if (p->partial) cudaFree(p->partial);
+    if (p->split_ws) cudaFree(p->split_ws);
     if (p->io) cudaFree(p->io);
     for (int i = 0; i < p->ev_count; ++i) {
         cudaEventDestroy(p->ev0[i]);

@@ -17,19 +17,24 @@
 //   warp 1   TMEM owner and MMA issuer: copies the stage's scale factors to
 //            TMEM (tcgen05.cp) and issues 4 tcgen05.mma kind::mxf8f6f4
 //            block-scaled MMAs (128x256x32 each) per 128-wide K block.
-//   warps 2-5 epilogue: TMEM -> registers -> BF16 (or fp32 split-K partials)
-//            -> global.  Each warp owns one 32-lane quarter of TMEM.
-//   warps 6-7 staging copy (fused only): copy-tasks (step, segment, chunk)
+//   warps 2-9 epilogue: TMEM -> registers -> BF16 -> global, or, for split
+//            K, the in-kernel fixed-order reduction of the split partials.
+//            Warp w drains TMEM lane quarter w%4, column half (w-2)/4.
+//   warps 10-11 staging copy (fused only): copy-tasks (step, segment, chunk)
 //            in step order; wait for the slot's credit, copy the rows of
 //            A_seg[r] and their scales, publish.
 //
 // Credits (the pages' per-slot signals with credit return, performance guide
-// 1.1/1.3) are monotonic u64 counters: a slot holds step s once
+// 1.1/1.3, kept per segment as its fine-grained signals suggest) are
+// monotonic u64 counters: segment r of a slot holds step s once
 // filled[slot][r] >= (s/bn + 1) * chunks_per_seg, and may be overwritten by
-// step s once drained[slot] counts every reader of the earlier steps that
-// used it.  Nothing is reset inside a launch; the last CTA to finish zeroes
-// the counters for the next launch.  Every wait is bounded by a time limit
-// and reports through the status block instead of hanging.
+// step s once drained[slot][r] counts every reader of segment r of the
+// earlier steps that used the slot.  A reader returns a segment's credit as
+// soon as its TMA loads of that segment have landed, so the next step's copy
+// of segment r overlaps the readers' work on the later segments.  Nothing is
+// reset inside a launch; the last CTA to finish zeroes the counters for the
+// next launch.  Every wait is bounded by a time limit and reports through the
+// status block instead of hanging.
 #include <cuda_bf16.h>
 
 #include "kernels.cuh"
@@ -49,6 +54,10 @@ struct __align__(8) SmemCtl {
     volatile int issued;     // stages issued by the TMA producer
     volatile int consumed;   // stages whose full barrier the MMA thread has passed
     volatile int copy_go;    // copy-role broadcast
+    volatile int copy_task;
+    volatile int ticket;     // split-K arrival order of the current tile (epilogue broadcast)
+    volatile int epi_ok;     // epilogue broadcast: the other partials of the tile are ready
+    volatile int epi_warp_ok[kEpiWarps];
 };
 
 constexpr size_t kSmemA = 0;
@@ -90,11 +99,12 @@ __device__ __forceinline__ int num_boxes(const GemmParams& p, int mt) {
     return (rows + p.box_m - 1) / p.box_m;
 }
 
-// Work items that read staging step s: m-tiles overlapping its rows x Nt x S.
-__device__ __forceinline__ unsigned long long readers_of_step(const GemmParams& p, int s) {
+// Work items that read one segment of staging step s: the m-tiles overlapping
+// its rows x Nt (of a tile's S split items exactly one covers the segment).
+__device__ __forceinline__ unsigned long long readers_of_segment(const GemmParams& p, int s) {
     const int first = (s * p.cm) / BM;
     const int last = ((s + 1) * p.cm - 1) / BM;
-    return (unsigned long long)(last - first + 1) * (unsigned long long)p.Nt * (unsigned long long)p.S;
+    return (unsigned long long)(last - first + 1) * (unsigned long long)p.Nt;
 }
 
 // ------------------------------------------------------------------ errors and bounded waits
@@ -168,8 +178,10 @@ __device__ bool wait_counter(const GemmParams& p, SmemCtl* ctl, const unsigned l
     unsigned long long v = ld_acquire_u64(ctr);
     if (v >= target) return true;
     const uint64_t t0 = globaltimer();
+    uint32_t nap = 64;   // exponential back-off keeps many pollers off the counter's L2 line
     for (uint32_t n = 1;; ++n) {
-        __nanosleep(32);
+        __nanosleep(nap);
+        if (nap < 1024) nap <<= 1;
         v = ld_acquire_u64(ctr);
         if (v >= target) return true;
         if (ctl->abort) return false;
@@ -262,6 +274,7 @@ __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_
         if (!wait_mbar(p, ctl, &ctl->acc_empty, acc_ph ^ 1u, kRoleMma)) return;
         tc_fence_after();
         const int total = item.nseg * p.kb_per_seg;
+        const int nbox = fused ? num_boxes(p, item.mt) : 0;
         for (int j = 0; j < total; ++j) {
             const int stage = it % kStages;
             const uint32_t ph = (uint32_t)(it / kStages) & 1u;
@@ -285,16 +298,21 @@ __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_
             }
             tc_commit(&ctl->empty[stage]);
             ++it;
-        }
-        if (fused) {
-            // every TMA read of the ring for this item has landed: return the credits
-            const int nbox = num_boxes(p, item.mt);
-            int last_s = -1;
-            for (int b = 0; b < nbox; ++b) {
-                const int s = (item.mt * BM + b * p.box_m) / p.cm;
-                if (s != last_s) {
-                    red_release_add_u64(p.flags + FlagLayout::drained(s % p.bn, p.bn, p.R), 1ull);
-                    last_s = s;
+            if (fused && (j % p.kb_per_seg) == p.kb_per_seg - 1) {
+                // Every TMA read of this segment of the ring has landed in shared
+                // memory (this thread observed the stages' full barriers), so no
+                // later global write can change what the MMAs read: the credit is
+                // returned with a relaxed add.  A release here would make this
+                // thread wait for its in-flight tensor-core work first.
+                const int i = j / p.kb_per_seg;
+                const int r = item.seg_lo + (i + item.rot) % item.nseg;
+                int last_s = -1;
+                for (int b = 0; b < nbox; ++b) {
+                    const int s = (item.mt * BM + b * p.box_m) / p.cm;
+                    if (s != last_s) {
+                        red_relaxed_add_u64(p.flags + FlagLayout::drained(s % p.bn, r, p.bn, p.R), 1ull);
+                        last_s = s;
+                    }
                 }
             }
         }
@@ -308,20 +326,44 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bi
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+__device__ __forceinline__ void wait_value_u64(const GemmParams& p, SmemCtl* ctl, const unsigned long long* ptr,
+                                               unsigned long long want, bool* ok) {
+    // like wait_counter, for an exact epoch value
+    if (!wait_counter(p, ctl, ptr, want, kRoleEpi, -1, -1, -1)) *ok = false;
+}
+
 __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, int warp, int lane) {
-    const int quarter = warp & 3;   // TMEM lanes this warp may access: 32*quarter .. +31
+    const int ep = warp - kWarpEpi0;         // 0..7
+    const int quarter = warp & 3;            // TMEM lanes this warp may access: 32*quarter .. +31
+    const int half = ep >> 2;                // accumulator columns 128*half .. +127
+    const bool leader = (ep == 0 && lane == 0);
     uint32_t acc_ph = 0;
     for (int w = blockIdx.x; w < p.W; w += gridDim.x) {
         const Item item = decode_item(p, w);
-        if (!wait_mbar_warp(p, ctl, &ctl->acc_full, acc_ph, kRoleEpi)) return;
-        tc_fence_after();
-        const int row = item.mt * BM + quarter * 32 + lane;
-        const uint32_t tbase = tmem + kTmemAccCol + ((uint32_t)(quarter * 32) << 16);
-        const int col0 = item.nt * BN;
-        if (p.S == 1) {
-            uint32_t packed[BN / 2];
+        const bool got = wait_mbar_warp(p, ctl, &ctl->acc_full, acc_ph, kRoleEpi);
+        if (p.S > 1) {
+            // the split path synchronises the 8 epilogue warps on a named barrier:
+            // leave only all together
+            if (lane == 0) ctl->epi_warp_ok[ep] = got ? 1 : 0;
+            named_barrier_sync(2, kEpiThreads);
+            bool all = true;
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int e = 0; e < kEpiWarps; ++e) all = all && ctl->epi_warp_ok[e] != 0;
+            if (!all) return;
+        } else if (!got) {
+            return;
+        }
+        tc_fence_after();
+        const int lrow = quarter * 32 + lane;            // row inside the tile
+        const int row = item.mt * BM + lrow;
+        const int tcol = half * (BN / 2);                // first accumulator column of this warp
+        const int col0 = item.nt * BN + tcol;
+        const uint32_t tbase = tmem + kTmemAccCol + ((uint32_t)(quarter * 32) << 16) + (uint32_t)tcol;
+        constexpr int kChunks = BN / 2 / 32;             // 4 chunks of 32 columns
+        if (p.S == 1) {
+            uint32_t packed[BN / 4];
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), v);
                 tc_wait_ld();
@@ -333,31 +375,97 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
             if (row < p.M) {
                 uint16_t* dst = p.C + (size_t)row * p.N + col0;
 #pragma unroll
-                for (int j = 0; j < BN / 8; ++j) {
+                for (int j = 0; j < BN / 16; ++j) {
                     if (col0 + j * 8 < p.N)
                         *reinterpret_cast<uint4*>(dst + j * 8) =
                             make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
                 }
             }
         } else {
-            float* dst = p.partial + ((size_t)item.q * p.M + row) * p.N + col0;
+            const size_t tile = (size_t)item.mt * p.Nt + item.nt;
+            if (leader) ctl->ticket = (int)atomicAdd(&p.tile_cnt[tile], 1u);
+            named_barrier_sync(2, kEpiThreads);
+            const bool last = ctl->ticket == p.S - 1;
+            // partial tile layout [BN/4][BM][4]: thread `lrow` of a warp stores the
+            // float4 of columns 4g..4g+3 at (g*BM + lrow)*4, so each warp store
+            // covers 512 contiguous bytes
+            float* part_tile = p.partial + tile * (size_t)p.S * (BM * BN);
+            if (!last) {
+                float* dst = part_tile + (size_t)item.q * (BM * BN) + ((size_t)(tcol / 4) * BM + lrow) * 4;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), v);
-                tc_wait_ld();
-                if (row < p.M) {
+                for (int c = 0; c < kChunks; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), v);
+                    tc_wait_ld();
+                    if (row < p.M) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int col = col0 + c * 32 + j * 4;
-                        if (col < p.N)
-                            *reinterpret_cast<uint4*>(dst + c * 32 + j * 4) =
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<uint4*>(dst + (size_t)(c * 8 + j) * BM * 4) =
                                 make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                     }
                 }
+                tc_fence_before();
+                mbar_arrive(&ctl->acc_empty);
+                __threadfence();
+                named_barrier_sync(2, kEpiThreads);
+                if (leader)
+                    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p.ready + tile * p.S + item.q),
+                                 "l"(p.launch_id)
+                                 : "memory");
+            } else {
+                // wait until every other split of this tile has published its partial
+                if (leader) {
+                    bool ok = true;
+                    for (int q = 0; q < p.S && ok; ++q)
+                        if (q != item.q) wait_value_u64(p, ctl, p.ready + tile * p.S + q, p.launch_id, &ok);
+                    ctl->epi_ok = ok ? 1 : 0;
+                }
+                named_barrier_sync(2, kEpiThreads);
+                const bool ok = ctl->epi_ok != 0;
+                uint16_t* dst = p.C + (size_t)row * p.N + col0;
+#pragma unroll 1
+                for (int c = 0; c < kChunks; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), v);
+                    tc_wait_ld();
+                    if (ok && row < p.M) {
+                        // fixed order q = 0..S-1, whichever split finished last
+                        float acc[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
+                        for (int q = 0; q < p.S; ++q) {
+                            if (q == item.q) {
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) acc[e] += __uint_as_float(v[e]);
+                            } else {
+                                const float* src = part_tile + (size_t)q * (BM * BN) +
+                                                   ((size_t)(tcol / 4 + c * 8) * BM + lrow) * 4;
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    const float4 t = *reinterpret_cast<const float4*>(src + (size_t)j * BM * 4);
+                                    acc[4 * j] += t.x;
+                                    acc[4 * j + 1] += t.y;
+                                    acc[4 * j + 2] += t.z;
+                                    acc[4 * j + 3] += t.w;
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            if (col0 + c * 32 + j * 8 < p.N)
+                                *reinterpret_cast<uint4*>(dst + c * 32 + j * 8) = make_uint4(
+                                    pack_bf16x2(__float_as_uint(acc[8 * j]), __float_as_uint(acc[8 * j + 1])),
+                                    pack_bf16x2(__float_as_uint(acc[8 * j + 2]), __float_as_uint(acc[8 * j + 3])),
+                                    pack_bf16x2(__float_as_uint(acc[8 * j + 4]), __float_as_uint(acc[8 * j + 5])),
+                                    pack_bf16x2(__float_as_uint(acc[8 * j + 6]), __float_as_uint(acc[8 * j + 7])));
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&ctl->acc_empty);
+                if (leader) p.tile_cnt[tile] = 0u;   // ready for the next launch
+                if (!ok) return;
             }
-            tc_fence_before();
-            mbar_arrive(&ctl->acc_empty);
         }
         acc_ph ^= 1u;
     }
@@ -391,24 +499,36 @@ __device__ void copy_role(const GemmParams& p, SmemCtl* ctl, int ctid) {
     const int per_step = p.R * p.chunks_per_seg;
     const long long chunk_bytes = (long long)p.rows_per_chunk * p.ka;
     const int sf_cols = p.ka / 32;
-    for (int t = blockIdx.x; t < p.n_copy_tasks; t += gridDim.x) {
+    unsigned long long* next = p.flags + FlagLayout::copy_next(p.bn, p.R);
+    for (;;) {
+        // Tasks are claimed from one global counter in (step, segment, chunk)
+        // order, so a copy role waiting for one slot's credit never holds back
+        // tasks that another CTA could already copy.
+        if (ctid == 0) {
+            int t = ctl->abort ? p.n_copy_tasks : (int)atomicAdd(next, 1ull);
+            bool ok = t < p.n_copy_tasks;
+            if (ok) {
+                const int s = t / per_step;
+                const int r = (t - s * per_step) / p.chunks_per_seg;
+                const int slot = s % p.bn;
+                if (s >= p.bn && !p.exchange_only) {
+                    unsigned long long target = 0;
+                    for (int s2 = slot; s2 < s; s2 += p.bn) target += readers_of_segment(p, s2);
+                    ok = wait_counter(p, ctl, p.flags + FlagLayout::drained(slot, r, p.bn, p.R), target,
+                                      kRoleCopy, s, r, slot);
+                }
+            }
+            ctl->copy_task = t;
+            ctl->copy_go = ok ? 1 : 0;
+        }
+        named_barrier_sync(1, kCopyThreads);
+        if (!ctl->copy_go) return;   // uniform over the 64 copy threads
+        const int t = ctl->copy_task;
         const int s = t / per_step;
         const int rem = t - s * per_step;
         const int r = rem / p.chunks_per_seg;
         const int c = rem - r * p.chunks_per_seg;
         const int slot = s % p.bn;
-        if (ctid == 0) {
-            bool ok = !ctl->abort;
-            if (ok && s >= p.bn && !p.exchange_only) {
-                unsigned long long target = 0;
-                for (int s2 = slot; s2 < s; s2 += p.bn) target += readers_of_step(p, s2);
-                ok = wait_counter(p, ctl, p.flags + FlagLayout::drained(slot, p.bn, p.R), target, kRoleCopy, s, r,
-                                  slot);
-            }
-            ctl->copy_go = ok ? 1 : 0;
-        }
-        named_barrier_sync(1, kCopyThreads);
-        if (!ctl->copy_go) return;   // uniform over the 64 copy threads
         const int row0 = s * p.cm + c * p.rows_per_chunk;
         copy_bytes(p.A_seg[r] + (size_t)row0 * p.ka,
                    p.ring + ((size_t)(slot * p.R + r) * p.cm + (size_t)c * p.rows_per_chunk) * p.ka, chunk_bytes,
@@ -453,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ctl->empty[s], 1);
         }
         mbar_init(&ctl->acc_full, 1);
-        mbar_init(&ctl->acc_empty, 4 * 32);
+        mbar_init(&ctl->acc_empty, kEpiThreads);
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
         ctl->issued = 0;
@@ -503,17 +623,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    if (kFused && threadIdx.x == 0) {
-        // The last CTA to finish zeroes the credit counters for the next launch.
+    if ((kFused || p.S > 1) && threadIdx.x == 0) {
+        // The last CTA to finish zeroes the staging credits for the next launch,
+        // and, if this launch gave up somewhere, the split-K tile counters.
         __threadfence();
         unsigned long long* done = p.flags + FlagLayout::cta_done(p.bn, p.R);
         const unsigned long long prev = atomicAdd(done, 1ull);
         if (prev == (unsigned long long)gridDim.x - 1) {
             __threadfence();
-            for (int slot = 0; slot < p.bn; ++slot) {
-                for (int r = 0; r < p.R; ++r) atomicExch(p.flags + FlagLayout::filled(slot, r, p.R), 0ull);
-                atomicExch(p.flags + FlagLayout::drained(slot, p.bn, p.R), 0ull);
+            if (kFused) {
+                atomicExch(p.flags + FlagLayout::copy_next(p.bn, p.R), 0ull);
+                for (int slot = 0; slot < p.bn; ++slot) {
+                    for (int r = 0; r < p.R; ++r) {
+                        atomicExch(p.flags + FlagLayout::filled(slot, r, p.R), 0ull);
+                        atomicExch(p.flags + FlagLayout::drained(slot, r, p.bn, p.R), 0ull);
+                    }
+                }
             }
+            if (p.S > 1 && launch_failed(p))
+                for (int t = 0; t < p.Mt * p.Nt; ++t) atomicExch(&p.tile_cnt[t], 0u);
             atomicExch(done, 0ull);
             __threadfence();
         }

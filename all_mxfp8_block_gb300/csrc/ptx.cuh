@@ -94,6 +94,9 @@ __device__ __forceinline__ uint64_t ld_relaxed_u64(const unsigned long long* p) 
 __device__ __forceinline__ void red_release_add_u64(unsigned long long* p, uint64_t v) {
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+__device__ __forceinline__ void red_relaxed_add_u64(unsigned long long* p, uint64_t v) {
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 
 // 16-byte streaming load of read-only input (not kept in L1)
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {

@@ -48,6 +48,7 @@ MXA2A_INFO_ROWS_PER_CHUNK = 108
 MXA2A_INFO_WORKSPACE_BYTES = 109
 MXA2A_INFO_SM_COUNT = 110
 MXA2A_INFO_LAUNCHES = 111
+MXA2A_INFO_SPLITS_UNFUSED = 112
 
 MXA2A_WS_RING = 1
 MXA2A_WS_SFA = 2

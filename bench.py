@@ -251,6 +251,8 @@ def run_ours(args, w):
 
     plan = mxa2a.Plan(w.R, w.M, w.kPerRank, w.N, w.commMSize, w.buffer_num)
     plan.set_option(mxa2a.MXA2A_OPT_RECORD_EVENTS, min(4096, max(1, args.steps)))
+    if args.split:
+        plan.set_option(mxa2a.MXA2A_OPT_SPLIT_K, args.split)
     run = plan.run if args.path == "fused" else plan.run_unfused
 
     def timed_loop(fn, steps, warmup, sampler=None):
@@ -391,6 +393,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--split", type=int, default=0, help="force the K split of both paths (0 = automatic)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -103,9 +103,11 @@ int mxa2a_last_error(void);
 
 /*
  * The fused path: one persistent cooperative kernel stages A_seg[r] rows
- * (commMSize per step, buffer_num-slot ring, per-slot credits) and runs the
- * block-scaled GEMM on the staged slots as they fill; plus a small kernel that
- * reorders B_scale for the MMA, and a split-K reduction when the plan splits.
+ * (commMSize per step, buffer_num-slot ring, per-segment credits) and runs
+ * the block-scaled GEMM on the staged slots as they fill, plus a small kernel
+ * that reorders B_scale for the MMA.  When the ring holds too few output
+ * tiles to fill the GPU, K is split over segment groups and the split
+ * partials are summed inside the kernel in a fixed order (deterministic).
  * A_seg / A_scale_seg are host arrays of R device pointers.  stream is a
  * cudaStream_t (NULL = legacy default stream).  Asynchronous.
  */
@@ -114,8 +116,9 @@ int mxa2a_run(mxa2a_plan *plan, const void *const *A_seg, const void *const *A_s
 
 /*
  * The unfused comparison path: first pack the R segments into one [M][K]
- * operand (and its scales), then run the same GEMM on it.  Same arguments,
- * same result bits as mxa2a_run for the same plan and options.
+ * operand (and its scales), then run the same GEMM on it.  Same arguments;
+ * the same result bits as mxa2a_run when both paths use the same K split
+ * (MXA2A_OPT_SPLIT_K forces one; by default each path picks its own).
  */
 int mxa2a_run_unfused(mxa2a_plan *plan, const void *const *A_seg, const void *const *A_scale_seg, const void *B,
                       const void *B_scale, void *C_bf16, void *stream);
@@ -142,26 +145,27 @@ enum mxa2a_option {
     MXA2A_OPT_TIMEOUT_NS = 1,      /* limit of every device wait, ns (default 2e9) */
     MXA2A_OPT_SPLIT_K = 2,         /* 0 = automatic, s >= 1: split K into s segment groups */
     MXA2A_OPT_ZIGZAG = 3,          /* 1 (default): alternate n-tile direction per m-tile */
-    MXA2A_OPT_ROTATE = 4,          /* 1 (default): start each tile's K loop at a rotated segment */
+    MXA2A_OPT_ROTATE = 4,          /* 1: start each tile's K loop at a rotated segment (default 0) */
     MXA2A_OPT_RECORD_EVENTS = 5,   /* n >= 1: time the main GEMM kernel of each run, keeping the last n
                                       (n <= 4096) for mxa2a_kernel_times; 0 = off (default) */
     MXA2A_OPT_EXCHANGE_ONLY = 6,   /* 1: fused runs only stage A into the ring (needs buffer_num >= steps) */
     MXA2A_OPT_FAULT_SKIP_STEP = 7, /* test knob: never publish staging step k (-1 = off); waits then time out */
     MXA2A_OPT_GRID = 8,            /* cap on persistent CTAs (0 = one per SM) */
-    MXA2A_OPT_CHUNK_BYTES = 9,     /* target staging copy chunk (default 32768) */
+    MXA2A_OPT_CHUNK_BYTES = 9,     /* target staging copy chunk (default 8192) */
     /* read-only plan facts (mxa2a_get_option only) */
     MXA2A_INFO_STEPS = 100,        /* M / commMSize */
     MXA2A_INFO_MTILES = 101,
     MXA2A_INFO_NTILES = 102,
-    MXA2A_INFO_SPLITS = 103,       /* effective K split */
-    MXA2A_INFO_ITEMS = 104,        /* work items of the persistent GEMM */
+    MXA2A_INFO_SPLITS = 103,       /* effective K split of the fused path */
+    MXA2A_INFO_ITEMS = 104,        /* work items of the fused persistent GEMM */
     MXA2A_INFO_GRID_FUSED = 105,
     MXA2A_INFO_GRID_UNFUSED = 106,
     MXA2A_INFO_COPY_TASKS = 107,
     MXA2A_INFO_ROWS_PER_CHUNK = 108,
     MXA2A_INFO_WORKSPACE_BYTES = 109,
     MXA2A_INFO_SM_COUNT = 110,
-    MXA2A_INFO_LAUNCHES = 111      /* kernels launched by the last run call */
+    MXA2A_INFO_LAUNCHES = 111,     /* kernels launched by the last run call */
+    MXA2A_INFO_SPLITS_UNFUSED = 112  /* effective K split of the unfused path */
 };
 
 int mxa2a_set_option(mxa2a_plan *plan, int key, int64_t value);
