@@ -9,22 +9,32 @@ namespace mxa2a {
 
 constexpr int kMaxSegments = 64;   // R limit (segment pointer tables live in kernel params)
 
-// GEMM tile: 128 rows (M) x 256 columns (N), 128-byte (= 128 FP8) K blocks.
+// GEMM tile per CTA: 128 rows (M) x 256 columns (N), 128-byte (= 128 FP8) K
+// blocks.  In the CTA-pair variant two CTAs compute a 256 x 256 tile with one
+// tcgen05 cta_group::2 MMA stream, each holding half of B, so a stage is
+// smaller and the ring deeper.
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 128;
-constexpr int kStages = 4;
-constexpr int kThreads = 384;      // 12 warps, roles below
-constexpr int kWarpTma = 0;        // TMA producer (one elected lane)
+constexpr int kStagesSingle = 4;
+constexpr int kStagesPair = 6;
+constexpr int kMaxStages = 6;
+constexpr int kThreads = 416;      // 13 warps, roles below
+constexpr int kWarpTma = 0;        // TMA producer 0 (one elected lane): even stages
 constexpr int kWarpMma = 1;        // TMEM allocator + MMA issuer (one elected lane)
 constexpr int kWarpEpi0 = 2;       // warps 2..9: epilogue, warp w drains TMEM lane quarter w%4,
 constexpr int kEpiWarps = 8;       //   column half (w-2)/4 of the accumulator
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kWarpCopy0 = 10;     // warps 10..11: staging copy (fused kernel only)
 constexpr int kCopyThreads = 64;
+constexpr int kWarpTma1 = 12;      // TMA producer 1 (one elected lane): odd stages
+// One thread's TMA loads overlap poorly (about one stage per 0.4 us per
+// thread on this GPU); two issuing warps double the per-SM load rate.
+constexpr int kProducers = 2;
 
 constexpr int kAStageBytes = BM * BK;        // 16 KiB
-constexpr int kBStageBytes = BN * BK;        // 32 KiB
+constexpr int kBStageBytesSingle = BN * BK;        // 32 KiB
+constexpr int kBStageBytesPair = BN / 2 * BK;      // 16 KiB
 constexpr int kSfAtomBytes = 512;            // 128 rows x 4 E8M0 bytes (one 128-K block)
 constexpr int kSfaStageBytes = kSfAtomBytes;
 constexpr int kSfbStageBytes = 2 * kSfAtomBytes;
@@ -50,6 +60,8 @@ struct DevStatus {
 // Monotonic credit counters of the staging ring, each on its own 128-byte line.
 // filled[slot][r]:  staging copy chunks published for (slot, segment r)
 // drained[slot][r]: work items that finished reading segment r of the slot
+// staged[slot]:     segments of the slot completely published (all chunks);
+//                   lets a reader check a whole step with one load
 // cta_done:         CTAs that reached the end (the last one zeroes everything)
 // copy_next:        next staging copy task to claim (tasks are claimed in order)
 struct FlagLayout {
@@ -58,18 +70,21 @@ struct FlagLayout {
     __host__ __device__ static size_t drained(int slot, int r, int bn, int R) {
         return (size_t)(bn * R + slot * R + r) * kLine;
     }
-    __host__ __device__ static size_t cta_done(int bn, int R) { return (size_t)(2 * bn * R) * kLine; }
-    __host__ __device__ static size_t copy_next(int bn, int R) { return (size_t)(2 * bn * R + 1) * kLine; }
-    __host__ __device__ static size_t words(int bn, int R) { return (size_t)(2 * bn * R + 2) * kLine; }
+    __host__ __device__ static size_t staged(int slot, int bn, int R) { return (size_t)(2 * bn * R + slot) * kLine; }
+    __host__ __device__ static size_t cta_done(int bn, int R) { return (size_t)(2 * bn * R + bn) * kLine; }
+    __host__ __device__ static size_t copy_next(int bn, int R) { return (size_t)(2 * bn * R + bn + 1) * kLine; }
+    __host__ __device__ static size_t words(int bn, int R) { return (size_t)(2 * bn * R + bn + 2) * kLine; }
 };
 
 struct GemmParams {
     int R, M, N, ka, K, cm, bn, steps;
     int Mt, Nt, S, W;           // m-tiles, n-tiles, K splits, work items
+    int pair;                   // 1: CTA-pair kernel, work items are pairs of m-tiles (Mt even)
     int kb_per_seg;             // ka / 128
     int Mg, Ng2;                // 128-row groups of A (scale atoms), 128-col groups of B (padded to 256)
     int box_m;                  // rows per A TMA box: 128 or 64
     int zigzag, rotate;
+    int group_m;                // m rows (tiles, or tile pairs) per raster group
     const uint8_t* sfa;         // A scales, MMA atom layout [K/128][Mg][512]
     const uint8_t* sfb;         // B scales, MMA atom layout [K/128][Ng2][512]
     uint16_t* C;                // bf16 [M][N]
@@ -97,7 +112,8 @@ struct GemmParams {
 // Launchers (mxgemm.cu / aux_kernels.cu).  All return cudaError_t of the launch.
 cudaError_t launch_mxgemm(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, int grid,
                           bool fused, cudaStream_t stream);
-size_t mxgemm_smem_bytes();
+// CTA pairs of the pair kernel that can be resident at once (0 if it cannot run)
+int mxgemm_max_pairs(bool fused);
 cudaError_t launch_pack_a(const GemmParams& p, uint8_t* a_packed, int grid, cudaStream_t stream);
 cudaError_t launch_pack_sfb(const uint8_t* B_scale, int N, int K, int Ng2, uint8_t* sfb, cudaStream_t stream);
 cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t stream);

@@ -53,12 +53,12 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-int tile_span(int64_t M, int64_t cm) {
-    // the most staging steps any 128-row output tile touches
+int tile_span(int64_t M, int64_t cm, int64_t rows = BM) {
+    // the most staging steps any output tile of `rows` rows touches
     int span = 1;
-    const int64_t Mt = (M + BM - 1) / BM;
+    const int64_t Mt = (M + rows - 1) / rows;
     for (int64_t mt = 0; mt < Mt; ++mt) {
-        const int64_t r0 = mt * BM, r1 = std::min<int64_t>(M, r0 + BM) - 1;
+        const int64_t r0 = mt * rows, r1 = std::min<int64_t>(M, r0 + rows) - 1;
         span = std::max<int>(span, (int)(r1 / cm - r0 / cm + 1));
     }
     return span;
@@ -75,6 +75,11 @@ struct mxa2a_plan {
     int64_t K = 0;
     int steps = 0, Mt = 0, Nt = 0, Mg = 0, Ng2 = 0, box_m = 128, span = 1;
     int S_fused = 1, S_unfused = 1, W_fused = 0, W_unfused = 0;   // K splits and work items per path
+    int pair_fused = 0, pair_unfused = 0;   // CTA-pair kernel in use, per path
+    int group_fused = 1, group_unfused = 1; // raster group, in m rows (tiles or tile pairs)
+    int group_cap = 16;                     // option: largest unfused raster group
+    int allow_pair = 0;           // option: 1 allows the CTA-pair kernel
+    int max_pairs_fused = 0, max_pairs_unfused = 0;
     int rows_per_chunk = 1, chunks_per_seg = 1, n_copy_tasks = 0;
     int grid_fused = 0, grid_unfused = 0;
     // options
@@ -95,7 +100,7 @@ struct mxa2a_plan {
     unsigned long long* flags = nullptr;
     DevStatus* status = nullptr;
     size_t ring_bytes = 0, sfa_bytes = 0, sfb_bytes = 0, apacked_bytes = 0, partial_bytes = 0, flags_bytes = 0;
-    CUtensorMap tmap_ring, tmap_apacked, tmap_b;
+    CUtensorMap tmap_ring, tmap_apacked, tmap_b, tmap_b_half;
     const void* tmap_b_ptr = nullptr;
     unsigned long long launch_id = 0, checked_launch = 0;
     // ring of (start, end) events around the main GEMM kernel of the last runs
@@ -138,8 +143,27 @@ void derive(mxa2a_plan* p) {
     const int window_mtiles = (int)std::min<int64_t>(p->Mt, (p->bn * p->cm + BM - 1) / BM);
     p->S_fused = split_for(window_mtiles * p->Nt);
     p->S_unfused = split_for(p->Mt * p->Nt);
-    p->W_fused = p->Mt * p->Nt * p->S_fused;
-    p->W_unfused = p->Mt * p->Nt * p->S_unfused;
+    // The CTA-pair kernel computes 256-row tiles with one 2-CTA MMA stream; it
+    // needs an even number of 128-row tiles and clusters of two resident CTAs.
+    // Both halves of a pair tile are consumed in lock step, so the fused path
+    // also needs every staging step of a 256-row tile resident in the ring.
+    const bool pair_ok = p->allow_pair && p->Mt % 2 == 0;
+    p->pair_unfused = (pair_ok && p->max_pairs_unfused > 0) ? 1 : 0;
+    p->pair_fused = (pair_ok && p->max_pairs_fused > 0 && p->bn >= tile_span(p->M, p->cm, 2 * BM)) ? 1 : 0;
+    p->W_fused = (p->pair_fused ? p->Mt / 2 : p->Mt) * p->Nt * p->S_fused;
+    p->W_unfused = (p->pair_unfused ? p->Mt / 2 : p->Mt) * p->Nt * p->S_unfused;
+    // Raster groups (m rows processed n-tile outer inside a group).  Unfused:
+    // up to group_cap m rows, so the CTAs in flight share a few B tiles and A
+    // rows in L2.  Fused: one m row.  A fused group must be whole staging
+    // steps that fit in the ring, and its slots then drain together only when
+    // its last items finish; measured on GB300 that stall costs more than the
+    // L2 reuse gains, so the fused path consumes the steps one m-tile at a time.
+    {
+        const int row_u = p->pair_unfused ? 2 * BM : BM;
+        const int rows_u = (int)((p->M + row_u - 1) / row_u);
+        p->group_unfused = std::max(1, std::min(rows_u, p->group_cap));
+        p->group_fused = 1;
+    }
     // staging copy chunk: the largest divisor of commMSize rows within chunk_bytes
     int64_t want = std::max<int64_t>(1, p->chunk_bytes / p->ka);
     int rpc = 1;
@@ -150,8 +174,18 @@ void derive(mxa2a_plan* p) {
     p->n_copy_tasks = p->steps * p->R * p->chunks_per_seg;
     int cap = p->sm_count;
     if (p->grid_cap > 0) cap = std::min(cap, p->grid_cap);
-    p->grid_fused = std::max(1, std::min(cap, std::max(p->W_fused, p->n_copy_tasks)));
-    p->grid_unfused = std::max(1, std::min(cap, p->W_unfused));
+    if (p->pair_fused) {
+        const int pf = std::min(cap / 2, p->max_pairs_fused);
+        p->grid_fused = 2 * std::max(1, std::min(pf, std::max(p->W_fused, (p->n_copy_tasks + 1) / 2)));
+    } else {
+        p->grid_fused = std::max(1, std::min(cap, std::max(p->W_fused, p->n_copy_tasks)));
+    }
+    if (p->pair_unfused) {
+        const int pu = std::min(cap / 2, p->max_pairs_unfused);
+        p->grid_unfused = 2 * std::max(1, std::min(pu, p->W_unfused));
+    } else {
+        p->grid_unfused = std::max(1, std::min(cap, p->W_unfused));
+    }
 }
 
 bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
@@ -189,6 +223,8 @@ void fill_params(mxa2a_plan* p, GemmParams& g, const void* const* A_seg, const v
     g.Nt = p->Nt;
     g.S = fused ? p->S_fused : p->S_unfused;
     g.W = fused ? p->W_fused : p->W_unfused;
+    g.pair = fused ? p->pair_fused : p->pair_unfused;
+    g.group_m = fused ? p->group_fused : p->group_unfused;
     g.kb_per_seg = (int)(p->ka / BK);
     g.Mg = p->Mg;
     g.Ng2 = p->Ng2;
@@ -221,7 +257,9 @@ void fill_params(mxa2a_plan* p, GemmParams& g, const void* const* A_seg, const v
 
 int refresh_b_map(mxa2a_plan* p, const void* B) {
     if (p->tmap_b_ptr == B) return MXA2A_OK;
-    if (!encode_2d(&p->tmap_b, B, (uint64_t)p->K, (uint64_t)p->N, BN)) return MXA2A_ERR_CUDA;
+    if (!encode_2d(&p->tmap_b, B, (uint64_t)p->K, (uint64_t)p->N, BN) ||
+        !encode_2d(&p->tmap_b_half, B, (uint64_t)p->K, (uint64_t)p->N, BN / 2))
+        return MXA2A_ERR_CUDA;
     p->tmap_b_ptr = B;
     return MXA2A_OK;
 }
@@ -276,7 +314,7 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
     }
     const int ev_slot = p->record_events ? (int)(p->ev_recorded % p->record_events) : 0;
     if (p->record_events && (rc = cuda_rc(cudaEventRecord(p->ev0[ev_slot], stream)))) return rc;
-    rc = cuda_rc(launch_mxgemm(g, fused ? p->tmap_ring : p->tmap_apacked, p->tmap_b,
+    rc = cuda_rc(launch_mxgemm(g, fused ? p->tmap_ring : p->tmap_apacked, g.pair ? p->tmap_b_half : p->tmap_b,
                                fused ? p->grid_fused : p->grid_unfused, fused, stream));
     if (rc) return rc;
     ++launches;
@@ -336,6 +374,8 @@ mxa2a_plan* mxa2a_create(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t 
     p->bn = buffer_num;
     p->device = dev;
     p->sm_count = sms;
+    p->max_pairs_fused = mxgemm_max_pairs(true);
+    p->max_pairs_unfused = mxgemm_max_pairs(false);
     derive(p);
     // workspace: ring | sfa | sfb | packed A | flags | status (split-K partials separately)
     p->ring_bytes = (size_t)buffer_num * R * commMSize * kPerRank;
@@ -520,6 +560,14 @@ int mxa2a_set_option(mxa2a_plan* p, int key, int64_t v) {
             if (v < 16) return MXA2A_ERR_INVALID_OPTION;
             p->chunk_bytes = v;
             break;
+        case MXA2A_OPT_CTA_PAIR:
+            if (v != 0 && v != 1) return MXA2A_ERR_INVALID_OPTION;
+            p->allow_pair = (int)v;
+            break;
+        case MXA2A_OPT_GROUP_M:
+            if (v < 1 || v > 4096) return MXA2A_ERR_INVALID_OPTION;
+            p->group_cap = (int)v;
+            break;
         default:
             return MXA2A_ERR_INVALID_OPTION;
     }
@@ -539,6 +587,12 @@ int mxa2a_get_option(mxa2a_plan* p, int key, int64_t* v) {
         case MXA2A_OPT_FAULT_SKIP_STEP: *v = p->fault_skip_step; break;
         case MXA2A_OPT_GRID: *v = p->grid_cap; break;
         case MXA2A_OPT_CHUNK_BYTES: *v = p->chunk_bytes; break;
+        case MXA2A_OPT_CTA_PAIR: *v = p->allow_pair; break;
+        case MXA2A_OPT_GROUP_M: *v = p->group_cap; break;
+        case MXA2A_INFO_GROUP_FUSED: *v = p->group_fused; break;
+        case MXA2A_INFO_GROUP_UNFUSED: *v = p->group_unfused; break;
+        case MXA2A_INFO_CTA_PAIR: *v = p->pair_fused; break;
+        case MXA2A_INFO_CTA_PAIR_UNFUSED: *v = p->pair_unfused; break;
         case MXA2A_INFO_STEPS: *v = p->steps; break;
         case MXA2A_INFO_MTILES: *v = p->Mt; break;
         case MXA2A_INFO_NTILES: *v = p->Nt; break;

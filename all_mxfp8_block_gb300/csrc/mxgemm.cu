@@ -10,13 +10,18 @@
 // segments and returns the slot's credit.  On one GPU the segments are R
 // separate HBM buffers and the "exchange" is this kernel's own copy role.
 //
-// CTA roles (256 threads, one CTA per SM, persistent over work items):
-//   warp 0   TMA producer: waits for a slot's segment to be published, then
-//            streams A (from the ring, or from the packed A when unfused), B
-//            and both scale tiles into a 4-stage shared-memory ring.
+// CTA roles (384 threads, one CTA per SM, persistent over work items):
+//   warps 0, 12  TMA producers (even / odd stages): wait for a slot's segment
+//            to be published, then stream A (from the ring, or from the packed
+//            A when unfused), B and both scale tiles into a shared-memory ring
+//            of stages.  Two issuing warps: one thread's TMA loads overlap
+//            poorly, two reach about twice the per-SM load rate.
 //   warp 1   TMEM owner and MMA issuer: copies the stage's scale factors to
 //            TMEM (tcgen05.cp) and issues 4 tcgen05.mma kind::mxf8f6f4
 //            block-scaled MMAs (128x256x32 each) per 128-wide K block.
+//            In the CTA-pair kernel the even CTA issues 256x256x32 MMAs for
+//            both CTAs (.cta_group::2) and the odd CTA's warp 1 forwards its
+//            stage-full and accumulator-empty signals to the even CTA.
 //   warps 2-9 epilogue: TMEM -> registers -> BF16 -> global, or, for split
 //            K, the in-kernel fixed-order reduction of the split partials.
 //            Warp w drains TMEM lane quarter w%4, column half (w-2)/4.
@@ -43,15 +48,38 @@
 namespace mxa2a {
 using namespace ptx;
 
+// Optional event trace (built only with -DMXA2A_TRACE): per CTA, up to
+// kTraceCap (event, %globaltimer) pairs; event = kind << 56 | a << 28 | b.
+#ifdef MXA2A_TRACE
+constexpr int kTraceCtas = 160;
+constexpr int kTraceCap = 4096;
+__device__ unsigned long long g_trace[kTraceCtas * kTraceCap * 2];
+__device__ unsigned g_trace_n[kTraceCtas];
+__shared__ unsigned s_trace_n;
+__device__ __forceinline__ void trace_ev(unsigned kind, unsigned a, unsigned b) {
+    if (blockIdx.x >= kTraceCtas) return;
+    const unsigned i = atomicAdd(&s_trace_n, 1u);
+    if (i >= kTraceCap) return;
+    unsigned long long* e = g_trace + ((size_t)blockIdx.x * kTraceCap + i) * 2;
+    e[0] = ((unsigned long long)kind << 56) | ((unsigned long long)(a & 0xFFFFFFFu) << 28) | (b & 0xFFFFFFFu);
+    e[1] = globaltimer();
+}
+#define TRACE(k, a, b) trace_ev((k), (unsigned)(a), (unsigned)(b))
+#else
+#define TRACE(k, a, b) ((void)0)
+#endif
+
 struct __align__(8) SmemCtl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t peer_full[kMaxStages];   // pair kernel, even CTA: the odd CTA's stage landed
     uint64_t acc_full;
     uint64_t acc_empty;
+    uint64_t acc_empty_peer;          // pair kernel, even CTA: the odd CTA drained its TMEM
     uint64_t drain;
     uint32_t tmem_base;
     volatile int abort;
-    volatile int issued;     // stages issued by the TMA producer
+    volatile int issued[kProducers];   // per producer: 1 + index of its last issued stage
     volatile int consumed;   // stages whose full barrier the MMA thread has passed
     volatile int copy_go;    // copy-role broadcast
     volatile int copy_task;
@@ -60,38 +88,69 @@ struct __align__(8) SmemCtl {
     volatile int epi_warp_ok[kEpiWarps];
 };
 
-constexpr size_t kSmemA = 0;
-constexpr size_t kSmemB = kSmemA + (size_t)kStages * kAStageBytes;
-constexpr size_t kSmemSfa = kSmemB + (size_t)kStages * kBStageBytes;
-constexpr size_t kSmemSfb = kSmemSfa + (size_t)kStages * kSfaStageBytes;
-constexpr size_t kSmemCtl = kSmemSfb + (size_t)kStages * kSfbStageBytes;
-constexpr size_t kSmemTotal = kSmemCtl + sizeof(SmemCtl) + 1024;   // + runtime 1 KiB alignment
-
-size_t mxgemm_smem_bytes() { return kSmemTotal; }
+// Shared-memory layout of one CTA: [A stages][B stages][SFA stages][SFB stages][control]
+template <bool kPair>
+struct Lay {
+    static constexpr int kStg = kPair ? kStagesPair : kStagesSingle;
+    static constexpr int kBRows = kPair ? BN / 2 : BN;       // rows of B this CTA loads per stage
+    static constexpr int kBStage = kPair ? kBStageBytesPair : kBStageBytesSingle;
+    static constexpr size_t A = 0;
+    static constexpr size_t B = A + (size_t)kStg * kAStageBytes;
+    static constexpr size_t Sfa = B + (size_t)kStg * kBStage;
+    static constexpr size_t Sfb = Sfa + (size_t)kStg * kSfaStageBytes;
+    static constexpr size_t Ctl = Sfb + (size_t)kStg * kSfbStageBytes;
+    static constexpr size_t Total = Ctl + sizeof(SmemCtl) + 1024;   // + runtime 1 KiB alignment
+};
+static_assert(Lay<false>::Total <= 227 * 1024 && Lay<true>::Total <= 227 * 1024, "shared memory");
+static_assert(kTmemSfCol + kMaxStages * kTmemSfColsPerStage <= kTmemCols, "TMEM columns");
 
 // ------------------------------------------------------------------ work items
 struct Item {
     int mt, nt, q, seg_lo, nseg, rot;
 };
 
-// Flattened work id -> (m-tile, n-tile, K split).  Items are ordered m-tile
-// major so the staging steps are consumed in order; inside an m-tile the
-// n-tiles run forward on even m-tiles and backward on odd ones (zigzag), so
-// consecutive m-tiles reuse the B tiles still in L2.  Each item starts its
-// K loop at a rotated segment so concurrent items read different segments.
+// Flattened work id -> (m row, n-tile, K split), where the m row is an m-tile
+// (or, in the CTA-pair kernel, a pair of m-tiles).  Items are rastered in
+// groups of group_m m rows: group after group (so the staging steps are
+// consumed in order), inside a group n-tile outer and m row inner (so the
+// CTAs running at the same time share a few B tiles and a few A rows in
+// L2), with the n direction reversed on odd groups (zigzag) so a group starts
+// on the B tiles the previous one ended on.  On the fused path a group is
+// whole staging steps that fit in the ring together.  The K split is the
+// innermost index; each item may start its K loop at a rotated segment.
 __device__ __forceinline__ Item decode_item(const GemmParams& p, int w) {
     Item it;
-    const int per_m = p.Nt * p.S;
-    it.mt = w / per_m;
-    const int rem = w - it.mt * per_m;
-    const int ntl = rem / p.S;
-    it.q = rem - ntl * p.S;
-    it.nt = (p.zigzag && (it.mt & 1)) ? (p.Nt - 1 - ntl) : ntl;
+    const int rows = p.pair ? p.Mt / 2 : p.Mt;
+    const int per_group = p.group_m * p.Nt * p.S;
+    const int g = w / per_group;
+    const int gm = min(p.group_m, rows - g * p.group_m);     // m rows in this group
+    const int rem = w - g * per_group;
+    const int ntl = rem / (gm * p.S);
+    const int rem2 = rem - ntl * (gm * p.S);
+    it.mt = g * p.group_m + rem2 / p.S;
+    it.q = rem2 % p.S;
+    it.nt = (p.zigzag && (g & 1)) ? (p.Nt - 1 - ntl) : ntl;
     it.seg_lo = it.q * p.R / p.S;
     const int seg_hi = (it.q + 1) * p.R / p.S;
     it.nseg = seg_hi - it.seg_lo;
     it.rot = p.rotate ? (it.mt + it.nt) % it.nseg : 0;
     return it;
+}
+
+// The m-tile a CTA works on for an item.
+template <bool kPair>
+__device__ __forceinline__ int cta_mtile(const Item& item, uint32_t rank) {
+    return kPair ? 2 * item.mt + (int)rank : item.mt;
+}
+
+// First work item of this CTA (or CTA pair) and the stride between its items.
+template <bool kPair>
+__device__ __forceinline__ int first_item() {
+    return kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+}
+template <bool kPair>
+__device__ __forceinline__ int item_stride() {
+    return kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 }
 
 __device__ __forceinline__ int num_boxes(const GemmParams& p, int mt) {
@@ -204,33 +263,61 @@ __device__ __forceinline__ void named_barrier_sync(int id, int count) {
 }
 
 // ------------------------------------------------------------------ roles
+template <bool kPair>
 __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const CUtensorMap* tmb,
                               uint8_t* sA, uint8_t* sB, uint8_t* sSfa, uint8_t* sSfb, SmemCtl* ctl,
-                              bool fused) {
-    int it = 0;
-    for (int w = blockIdx.x; w < p.W; w += gridDim.x) {
+                              bool fused, uint32_t rank, int pid) {
+    using L = Lay<kPair>;
+    int it = 0;   // global stage sequence number; this producer issues it % kProducers == pid
+    for (int w = first_item<kPair>(); w < p.W; w += item_stride<kPair>()) {
         const Item item = decode_item(p, w);
-        const int nbox = fused ? num_boxes(p, item.mt) : 1;
+        const int mt = cta_mtile<kPair>(item, rank);
+        const int nbox = fused ? num_boxes(p, mt) : 1;
         const uint32_t a_bytes = fused ? (uint32_t)(nbox * p.box_m * BK) : (uint32_t)kAStageBytes;
-        const uint32_t bytes = a_bytes + kBStageBytes + kSfaStageBytes + kSfbStageBytes;
+        const uint32_t bytes = a_bytes + L::kBStage + kSfaStageBytes + kSfbStageBytes;
+        const int b_row = item.nt * BN + (kPair ? (int)rank * (BN / 2) : 0);
+        // One load per step first: when the copy role is ahead every segment
+        // of the item's steps is already staged and the per-segment checks
+        // (a round trip to L2 each) are skipped.  Only without a K split: then
+        // every reader reads every segment, so no segment of the slot's next
+        // step can be published (and counted) before this item has read it.
+        if (pid == 0) TRACE(4, w, 0);
+        bool all_staged = !fused;
+        if (fused && p.S == 1) {
+            all_staged = true;
+            int last_s = -1;
+            for (int b = 0; b < nbox && all_staged; ++b) {
+                const int s = (mt * BM + b * p.box_m) / p.cm;
+                if (s == last_s) continue;
+                last_s = s;
+                const unsigned long long need = (unsigned long long)(s / p.bn + 1) * (unsigned long long)p.R;
+                all_staged = ld_acquire_u64(p.flags + FlagLayout::staged(s % p.bn, p.bn, p.R)) >= need;
+            }
+            if (all_staged) fence_proxy_async_global();
+            if (pid == 0) TRACE(5, w, all_staged ? 1000 : 2000);
+        }
         for (int i = 0; i < item.nseg; ++i) {
             const int r = item.seg_lo + (i + item.rot) % item.nseg;
-            if (fused) {
-                for (int b = 0; b < nbox; ++b) {
-                    const int row0 = item.mt * BM + b * p.box_m;
-                    const int s = row0 / p.cm;
-                    const int slot = s % p.bn;
-                    const unsigned long long target =
-                        (unsigned long long)(s / p.bn + 1) * (unsigned long long)p.chunks_per_seg;
-                    if (!wait_counter(p, ctl, p.flags + FlagLayout::filled(slot, r, p.R), target, kRoleTma, s, r,
-                                      slot))
-                        return;
+            bool published = all_staged;
+            for (int kb = 0; kb < p.kb_per_seg; ++kb, ++it) {
+                if (it % kProducers != pid) continue;
+                if (!published) {
+                    for (int b = 0; b < nbox; ++b) {
+                        const int row0 = mt * BM + b * p.box_m;
+                        const int s = row0 / p.cm;
+                        const int slot = s % p.bn;
+                        const unsigned long long target =
+                            (unsigned long long)(s / p.bn + 1) * (unsigned long long)p.chunks_per_seg;
+                        if (!wait_counter(p, ctl, p.flags + FlagLayout::filled(slot, r, p.R), target, kRoleTma, s,
+                                          r, slot))
+                            return;
+                    }
+                    fence_proxy_async_global();   // the ring was written through the generic proxy
+                    published = true;
+                    TRACE(5, w, r);
                 }
-                fence_proxy_async_global();   // the ring was written through the generic proxy
-            }
-            for (int kb = 0; kb < p.kb_per_seg; ++kb) {
-                const int stage = it % kStages;
-                const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                const int stage = it % L::kStg;
+                const uint32_t ph = (uint32_t)(it / L::kStg) & 1u;
                 if (!wait_mbar(p, ctl, &ctl->empty[stage], ph ^ 1u, kRoleTma)) return;
                 uint64_t* bar = &ctl->full[stage];
                 mbar_arrive_expect_tx(bar, bytes);
@@ -239,64 +326,97 @@ __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const
                 uint8_t* a_dst = sA + (size_t)stage * kAStageBytes;
                 if (fused) {
                     for (int b = 0; b < nbox; ++b) {
-                        const int row0 = item.mt * BM + b * p.box_m;
+                        const int row0 = mt * BM + b * p.box_m;
                         const int s = row0 / p.cm;
                         const int ring_row = ((s % p.bn) * p.R + r) * p.cm + (row0 - s * p.cm);
                         tma_load_2d(a_dst + (size_t)b * p.box_m * BK, tma, bar, kx, ring_row);
                     }
                 } else {
-                    tma_load_2d(a_dst, tma, bar, kg, item.mt * BM);
+                    tma_load_2d(a_dst, tma, bar, kg, mt * BM);
                 }
-                tma_load_2d(sB + (size_t)stage * kBStageBytes, tmb, bar, kg, item.nt * BN);
+                tma_load_2d(sB + (size_t)stage * L::kBStage, tmb, bar, kg, b_row);
                 const int kbg = kg / BK;
                 bulk_load(sSfa + (size_t)stage * kSfaStageBytes,
-                          p.sfa + ((size_t)kbg * p.Mg + item.mt) * kSfAtomBytes, kSfaStageBytes, bar);
+                          p.sfa + ((size_t)kbg * p.Mg + mt) * kSfAtomBytes, kSfaStageBytes, bar);
+                // the scales of all 256 columns: each CTA's MMA share needs them in its own TMEM
                 bulk_load(sSfb + (size_t)stage * kSfbStageBytes,
                           p.sfb + ((size_t)kbg * p.Ng2 + 2 * item.nt) * kSfAtomBytes, kSfbStageBytes, bar);
-                ++it;
-                ctl->issued = it;
+                ctl->issued[pid] = it + 1;
             }
         }
     }
 }
 
+// Return the credit of segment r of the staging steps an m-tile's rows came from.
+__device__ __forceinline__ void return_segment_credit(const GemmParams& p, int mt, int r) {
+    const int nbox = num_boxes(p, mt);
+    int last_s = -1;
+    for (int b = 0; b < nbox; ++b) {
+        const int s = (mt * BM + b * p.box_m) / p.cm;
+        if (s != last_s) {
+            red_relaxed_add_u64(p.flags + FlagLayout::drained(s % p.bn, r, p.bn, p.R), 1ull);
+            last_s = s;
+        }
+    }
+}
+
+template <bool kPair>
 __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_t* sB, uint8_t* sSfa,
                          uint8_t* sSfb, SmemCtl* ctl, bool fused) {
+    using L = Lay<kPair>;
     // Instruction descriptor, kind::mxf8f6f4 with block scaling: A/B E4M3 (0),
     // both K-major, N>>3 at [17,23), scale type UE8M0 at bit 23, M>>4 at
-    // [24,29); B/A scale-factor byte ids at [4,6) and [29,31) select which of
-    // the four 32-wide K blocks held in each 32-bit TMEM scale column is used.
-    const uint32_t idesc_base = ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(BM >> 4) << 24);
+    // [24,29) (M = 256 for a CTA pair); B/A scale-factor byte ids at [4,6) and
+    // [29,31) select which of the four 32-wide K blocks held in each 32-bit
+    // TMEM scale column is used.
+    constexpr uint32_t kM = kPair ? 2 * BM : BM;
+    const uint32_t idesc_base = ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((kM >> 4) << 24);
     int it = 0;
     uint32_t acc_ph = 0;
-    for (int w = blockIdx.x; w < p.W; w += gridDim.x) {
+    for (int w = first_item<kPair>(); w < p.W; w += item_stride<kPair>()) {
         const Item item = decode_item(p, w);
         if (!wait_mbar(p, ctl, &ctl->acc_empty, acc_ph ^ 1u, kRoleMma)) return;
+        if (kPair && !wait_mbar(p, ctl, &ctl->acc_empty_peer, acc_ph ^ 1u, kRoleMma)) return;
         tc_fence_after();
+        TRACE(1, w, 0);
         const int total = item.nseg * p.kb_per_seg;
-        const int nbox = fused ? num_boxes(p, item.mt) : 0;
         for (int j = 0; j < total; ++j) {
-            const int stage = it % kStages;
-            const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+            const int stage = it % L::kStg;
+            const uint32_t ph = (uint32_t)(it / L::kStg) & 1u;
             if (!wait_mbar(p, ctl, &ctl->full[stage], ph, kRoleMma)) return;
+            if (kPair && !wait_mbar(p, ctl, &ctl->peer_full[stage], ph, kRoleMma)) return;
             ctl->consumed = it + 1;
+            if (j == 0) TRACE(2, w, 0);
             tc_fence_after();
             const uint32_t sf_t = tmem + kTmemSfCol + (uint32_t)stage * kTmemSfColsPerStage;
             const uint32_t sfa_s = smem_u32(sSfa + (size_t)stage * kSfaStageBytes);
             const uint32_t sfb_s = smem_u32(sSfb + (size_t)stage * kSfbStageBytes);
-            tc_cp_32x128b_warpx4(sf_t, smem_desc(sfa_s, 0, 128, kLayoutNone));
-            tc_cp_32x128b_warpx4(sf_t + 4, smem_desc(sfb_s, 0, 128, kLayoutNone));
-            tc_cp_32x128b_warpx4(sf_t + 8, smem_desc(sfb_s + kSfAtomBytes, 0, 128, kLayoutNone));
             const uint64_t adesc = smem_desc(smem_u32(sA + (size_t)stage * kAStageBytes), 16, 1024, kLayoutSw128);
-            const uint64_t bdesc = smem_desc(smem_u32(sB + (size_t)stage * kBStageBytes), 16, 1024, kLayoutSw128);
+            const uint64_t bdesc = smem_desc(smem_u32(sB + (size_t)stage * L::kBStage), 16, 1024, kLayoutSw128);
+            if (kPair) {
+                tc_cp_32x128b_warpx4_pair(sf_t, smem_desc(sfa_s, 0, 128, kLayoutNone));
+                tc_cp_32x128b_warpx4_pair(sf_t + 4, smem_desc(sfb_s, 0, 128, kLayoutNone));
+                tc_cp_32x128b_warpx4_pair(sf_t + 8, smem_desc(sfb_s + kSfAtomBytes, 0, 128, kLayoutNone));
 #pragma unroll
-            for (int k = 0; k < BK / 32; ++k) {
-                const uint32_t idesc = idesc_base | ((uint32_t)k << 4) | ((uint32_t)k << 29);
-                // +32 bytes along K inside the 128-byte swizzle atom = +2 in the encoded start address
-                mma_mxf8f6f4(tmem + kTmemAccCol, adesc + 2ull * k, bdesc + 2ull * k, idesc, sf_t, sf_t + 4,
-                             (j | k) != 0);
+                for (int k = 0; k < BK / 32; ++k) {
+                    const uint32_t idesc = idesc_base | ((uint32_t)k << 4) | ((uint32_t)k << 29);
+                    mma_mxf8f6f4_pair(tmem + kTmemAccCol, adesc + 2ull * k, bdesc + 2ull * k, idesc, sf_t, sf_t + 4,
+                                      (j | k) != 0);
+                }
+                tc_commit_pair_multicast(&ctl->empty[stage], 0x3);
+            } else {
+                tc_cp_32x128b_warpx4(sf_t, smem_desc(sfa_s, 0, 128, kLayoutNone));
+                tc_cp_32x128b_warpx4(sf_t + 4, smem_desc(sfb_s, 0, 128, kLayoutNone));
+                tc_cp_32x128b_warpx4(sf_t + 8, smem_desc(sfb_s + kSfAtomBytes, 0, 128, kLayoutNone));
+#pragma unroll
+                for (int k = 0; k < BK / 32; ++k) {
+                    const uint32_t idesc = idesc_base | ((uint32_t)k << 4) | ((uint32_t)k << 29);
+                    // +32 bytes along K inside the 128-byte swizzle atom = +2 in the encoded start address
+                    mma_mxf8f6f4(tmem + kTmemAccCol, adesc + 2ull * k, bdesc + 2ull * k, idesc, sf_t, sf_t + 4,
+                                 (j | k) != 0);
+                }
+                tc_commit(&ctl->empty[stage]);
             }
-            tc_commit(&ctl->empty[stage]);
             ++it;
             if (fused && (j % p.kb_per_seg) == p.kb_per_seg - 1) {
                 // Every TMA read of this segment of the ring has landed in shared
@@ -306,18 +426,47 @@ __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_
                 // thread wait for its in-flight tensor-core work first.
                 const int i = j / p.kb_per_seg;
                 const int r = item.seg_lo + (i + item.rot) % item.nseg;
-                int last_s = -1;
-                for (int b = 0; b < nbox; ++b) {
-                    const int s = (item.mt * BM + b * p.box_m) / p.cm;
-                    if (s != last_s) {
-                        red_relaxed_add_u64(p.flags + FlagLayout::drained(s % p.bn, r, p.bn, p.R), 1ull);
-                        last_s = s;
-                    }
-                }
+                return_segment_credit(p, cta_mtile<kPair>(item, 0), r);
+                if (kPair) return_segment_credit(p, cta_mtile<kPair>(item, 1), r);
             }
         }
-        tc_commit(&ctl->acc_full);
+        if (kPair)
+            tc_commit_pair_multicast(&ctl->acc_full, 0x3);
+        else
+            tc_commit(&ctl->acc_full);
+        TRACE(3, w, 0);
         acc_ph ^= 1u;
+    }
+}
+
+// CTA-pair kernel, odd CTA: its MMAs are issued by the even CTA, which must
+// know when this CTA's stages have landed and when its TMEM share is drained.
+// Walks the same item and stage sequence and forwards every completed phase of
+// its local full[] and acc_empty barriers, one arrive each, to the even CTA's
+// peer_full[] and acc_empty_peer barriers.  Before item i (i >= 1) the even
+// CTA waits for phase i-1 of acc_empty_peer, i.e. the drain of item i-1.
+__device__ void forwarder_role(const GemmParams& p, SmemCtl* ctl) {
+    using L = Lay<true>;
+    const uint32_t leader_full = mapa_shared(smem_u32(&ctl->peer_full[0]), 0);
+    const uint32_t leader_acc = mapa_shared(smem_u32(&ctl->acc_empty_peer), 0);
+    int it = 0;
+    int n_items = 0;
+    for (int w = first_item<true>(); w < p.W; w += item_stride<true>(), ++n_items) {
+        const Item item = decode_item(p, w);
+        if (n_items > 0) {
+            // this CTA's epilogue drained item n_items-1 (phase n_items-1 of acc_empty)
+            if (!wait_mbar(p, ctl, &ctl->acc_empty, (uint32_t)(n_items - 1) & 1u, kRoleMma)) return;
+            mbar_arrive_remote(leader_acc);
+        }
+        const int total = item.nseg * p.kb_per_seg;
+        for (int j = 0; j < total; ++j) {
+            const int stage = it % L::kStg;
+            const uint32_t ph = (uint32_t)(it / L::kStg) & 1u;
+            if (!wait_mbar(p, ctl, &ctl->full[stage], ph, kRoleMma)) return;
+            ctl->consumed = it + 1;
+            mbar_arrive_remote(leader_full + (uint32_t)(stage * sizeof(uint64_t)));
+            ++it;
+        }
     }
 }
 
@@ -332,14 +481,16 @@ __device__ __forceinline__ void wait_value_u64(const GemmParams& p, SmemCtl* ctl
     if (!wait_counter(p, ctl, ptr, want, kRoleEpi, -1, -1, -1)) *ok = false;
 }
 
-__device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, int warp, int lane) {
+template <bool kPair>
+__device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, int warp, int lane, uint32_t rank) {
     const int ep = warp - kWarpEpi0;         // 0..7
     const int quarter = warp & 3;            // TMEM lanes this warp may access: 32*quarter .. +31
     const int half = ep >> 2;                // accumulator columns 128*half .. +127
     const bool leader = (ep == 0 && lane == 0);
     uint32_t acc_ph = 0;
-    for (int w = blockIdx.x; w < p.W; w += gridDim.x) {
+    for (int w = first_item<kPair>(); w < p.W; w += item_stride<kPair>()) {
         const Item item = decode_item(p, w);
+        const int mt = cta_mtile<kPair>(item, rank);
         const bool got = wait_mbar_warp(p, ctl, &ctl->acc_full, acc_ph, kRoleEpi);
         if (p.S > 1) {
             // the split path synchronises the 8 epilogue warps on a named barrier:
@@ -353,9 +504,10 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
         } else if (!got) {
             return;
         }
+        if (leader) TRACE(6, w, 0);
         tc_fence_after();
         const int lrow = quarter * 32 + lane;            // row inside the tile
-        const int row = item.mt * BM + lrow;
+        const int row = mt * BM + lrow;
         const int tcol = half * (BN / 2);                // first accumulator column of this warp
         const int col0 = item.nt * BN + tcol;
         const uint32_t tbase = tmem + kTmemAccCol + ((uint32_t)(quarter * 32) << 16) + (uint32_t)tcol;
@@ -372,6 +524,7 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
             }
             tc_fence_before();
             mbar_arrive(&ctl->acc_empty);   // TMEM may now take the next item
+            if (leader) TRACE(7, w, 0);
             if (row < p.M) {
                 uint16_t* dst = p.C + (size_t)row * p.N + col0;
 #pragma unroll
@@ -382,7 +535,7 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
                 }
             }
         } else {
-            const size_t tile = (size_t)item.mt * p.Nt + item.nt;
+            const size_t tile = (size_t)mt * p.Nt + item.nt;
             if (leader) ctl->ticket = (int)atomicAdd(&p.tile_cnt[tile], 1u);
             named_barrier_sync(2, kEpiThreads);
             const bool last = ctl->ticket == p.S - 1;
@@ -507,6 +660,7 @@ __device__ void copy_role(const GemmParams& p, SmemCtl* ctl, int ctid) {
         if (ctid == 0) {
             int t = ctl->abort ? p.n_copy_tasks : (int)atomicAdd(next, 1ull);
             bool ok = t < p.n_copy_tasks;
+            if (ok) TRACE(8, t, 0);
             if (ok) {
                 const int s = t / per_step;
                 const int r = (t - s * per_step) / p.chunks_per_seg;
@@ -518,6 +672,7 @@ __device__ void copy_role(const GemmParams& p, SmemCtl* ctl, int ctid) {
                                       kRoleCopy, s, r, slot);
                 }
             }
+            if (ok) TRACE(9, t, 0);
             ctl->copy_task = t;
             ctl->copy_go = ok ? 1 : 0;
         }
@@ -547,81 +702,118 @@ __device__ void copy_role(const GemmParams& p, SmemCtl* ctl, int ctid) {
         __threadfence();
         fence_proxy_async_global();
         named_barrier_sync(1, kCopyThreads);
-        if (ctid == 0 && s != p.fault_skip_step)
-            red_release_add_u64(p.flags + FlagLayout::filled(slot, r, p.R), 1ull);
+        if (ctid == 0 && s != p.fault_skip_step) {
+            // the chunk that completes the segment also counts it as staged
+            const unsigned long long before =
+                atom_acq_rel_add_u64(p.flags + FlagLayout::filled(slot, r, p.R), 1ull);
+            if (before + 1 == (unsigned long long)(s / p.bn + 1) * (unsigned long long)p.chunks_per_seg)
+                red_release_add_u64(p.flags + FlagLayout::staged(slot, p.bn, p.R), 1ull);
+            TRACE(10, t, 0);
+        }
     }
 }
 
 // ------------------------------------------------------------------ kernel
-template <bool kFused>
+template <bool kFused, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     mxgemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_a,
                   const __grid_constant__ CUtensorMap tmap_b) {
+    using L = Lay<kPair>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA = smem + kSmemA;
-    uint8_t* sB = smem + kSmemB;
-    uint8_t* sSfa = smem + kSmemSfa;
-    uint8_t* sSfb = smem + kSmemSfb;
-    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + kSmemCtl);
+    uint8_t* sA = smem + L::A;
+    uint8_t* sB = smem + L::B;
+    uint8_t* sSfa = smem + L::Sfa;
+    uint8_t* sSfb = smem + L::Sfb;
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + L::Ctl);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;   // 0 = the CTA that issues the MMAs
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < L::kStg; ++s) {
             mbar_init(&ctl->full[s], 1);
             mbar_init(&ctl->empty[s], 1);
+            mbar_init(&ctl->peer_full[s], 1);
         }
         mbar_init(&ctl->acc_full, 1);
         mbar_init(&ctl->acc_empty, kEpiThreads);
+        mbar_init(&ctl->acc_empty_peer, 1);
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
-        ctl->issued = 0;
+        for (int i = 0; i < kProducers; ++i) ctl->issued[i] = 0;
         ctl->consumed = 0;
         ctl->copy_go = 0;
+#ifdef MXA2A_TRACE
+        s_trace_n = 0;
+#endif
         fence_mbarrier_init();
     }
     if (warp == kWarpMma) {
-        tmem_alloc(&ctl->tmem_base, kTmemCols);
-        tmem_relinquish();
+        if (kPair) {
+            tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&ctl->tmem_base, kTmemCols);
+            tmem_relinquish();
+        }
     }
-    if (warp == kWarpTma && lane == 0) {
+    if ((warp == kWarpTma || warp == kWarpTma1) && lane == 0) {
         prefetch_tensormap(&tmap_a);
         prefetch_tensormap(&tmap_b);
     }
     tc_fence_before();
     __syncthreads();
+    if (kPair) cluster_sync();   // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
 
-    if (warp == kWarpTma) {
-        if (lane == 0 && !p.exchange_only) producer_role(p, &tmap_a, &tmap_b, sA, sB, sSfa, sSfb, ctl, kFused);
+    if (warp == kWarpTma || warp == kWarpTma1) {
+        if (lane == 0 && !p.exchange_only)
+            producer_role<kPair>(p, &tmap_a, &tmap_b, sA, sB, sSfa, sSfb, ctl, kFused, rank,
+                                 warp == kWarpTma ? 0 : 1);
     } else if (warp == kWarpMma) {
-        if (lane == 0 && !p.exchange_only) mma_role(p, tmem, sA, sB, sSfa, sSfb, ctl, kFused);
+        if (lane == 0 && !p.exchange_only) {
+            if (rank == 0)
+                mma_role<kPair>(p, tmem, sA, sB, sSfa, sSfb, ctl, kFused);
+            else
+                forwarder_role(p, ctl);
+        }
     } else if (warp < kWarpCopy0) {
-        if (!p.exchange_only) epilogue_role(p, tmem, ctl, warp, lane);
-    } else if (kFused) {
+        if (!p.exchange_only) epilogue_role<kPair>(p, tmem, ctl, warp, lane, rank);
+    } else if (kFused && warp < kWarpCopy0 + kCopyThreads / 32) {
         copy_role(p, ctl, threadIdx.x - kWarpCopy0 * 32);
     }
     __syncwarp();
     __syncthreads();
 
-    // After an abort, let every TMA load already issued land before the CTA exits.
-    if (warp == kWarpTma && lane == 0 && ctl->abort) {
-        for (int i = ctl->consumed; i < ctl->issued; ++i)
-            wait_mbar_plain(p, &ctl->full[i % kStages], (uint32_t)(i / kStages) & 1u);
+    // After an abort, let every TMA load already issued land before the CTA exits
+    // (each producer waits for its own stages beyond those the MMA side consumed).
+    if ((warp == kWarpTma || warp == kWarpTma1) && lane == 0 && ctl->abort) {
+        const int pid = warp == kWarpTma ? 0 : 1;
+        for (int i = ctl->consumed; i < ctl->issued[pid]; ++i)
+            if (i % kProducers == pid) wait_mbar_plain(p, &ctl->full[i % L::kStg], (uint32_t)(i / L::kStg) & 1u);
     }
-    // All MMAs of this CTA complete before TMEM is released.
+    // All MMAs complete before TMEM is released (in a pair, the even CTA's
+    // commit arrives on both CTAs' drain barriers).
     if (warp == kWarpMma && lane == 0) {
-        tc_commit(&ctl->drain);
+        if (kPair) {
+            if (rank == 0) tc_commit_pair_multicast(&ctl->drain, 0x3);
+        } else {
+            tc_commit(&ctl->drain);
+        }
         wait_mbar_plain(p, &ctl->drain, 0);
     }
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    if (kPair) cluster_sync();   // no CTA leaves while its partner may still touch its memory
     if (warp == kWarpMma) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        if (kPair)
+            tmem_dealloc_pair(tmem, kTmemCols);
+        else
+            tmem_dealloc(tmem, kTmemCols);
     }
     if ((kFused || p.S > 1) && threadIdx.x == 0) {
         // The last CTA to finish zeroes the staging credits for the next launch,
@@ -634,6 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kFused) {
                 atomicExch(p.flags + FlagLayout::copy_next(p.bn, p.R), 0ull);
                 for (int slot = 0; slot < p.bn; ++slot) {
+                    atomicExch(p.flags + FlagLayout::staged(slot, p.bn, p.R), 0ull);
                     for (int r = 0; r < p.R; ++r) {
                         atomicExch(p.flags + FlagLayout::filled(slot, r, p.R), 0ull);
                         atomicExch(p.flags + FlagLayout::drained(slot, r, p.bn, p.R), 0ull);
@@ -648,34 +841,102 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-cudaError_t launch_mxgemm(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, int grid,
-                          bool fused, cudaStream_t stream) {
+namespace {
+template <bool kFused, bool kPair>
+cudaError_t prepare(int dev) {
     // the large dynamic shared memory opt-in is per device and per kernel
-    static bool attr_set[64][2] = {};
+    static bool done[64] = {};
+    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&mxgemm_kernel<kFused, kPair>),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay<kPair>::Total);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    return e;
+}
+
+template <bool kFused, bool kPair>
+cudaError_t launch_one(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, int grid,
+                       cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const void* fn = fused ? reinterpret_cast<const void*>(&mxgemm_kernel<true>)
-                           : reinterpret_cast<const void*>(&mxgemm_kernel<false>);
-    if (dev < 0 || dev >= 64 || !attr_set[dev][fused ? 1 : 0]) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTotal);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_set[dev][fused ? 1 : 0] = true;
-    }
+    if ((e = prepare<kFused, kPair>(dev)) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemTotal;
+    cfg.dynamicSmemBytes = Lay<kPair>::Total;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    // The fused kernel's CTAs wait on each other's credits: they must all be
-    // resident at once, which a cooperative launch guarantees (or refuses).
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    if (kPair) {
+        // CTA pairs of a cluster; the grid never exceeds the pairs that can be
+        // resident together, which the fused kernel's credit waits rely on
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+    } else {
+        // The fused kernel's CTAs wait on each other's credits: they must all be
+        // resident at once, which a cooperative launch guarantees (or refuses).
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = fused ? 1 : 0;
-    if (fused) return cudaLaunchKernelEx(&cfg, &mxgemm_kernel<true>, p, tmap_a, tmap_b);
-    return cudaLaunchKernelEx(&cfg, &mxgemm_kernel<false>, p, tmap_a, tmap_b);
+    cfg.numAttrs = (kPair || kFused) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, &mxgemm_kernel<kFused, kPair>, p, tmap_a, tmap_b);
+}
+
+template <bool kFused>
+int max_pairs_impl() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || prepare<kFused, true>(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Lay<true>::Total;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(&mxgemm_kernel<kFused, true>), &cfg) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+}  // namespace
+
+#ifdef MXA2A_TRACE
+// Trace access for the traced build: copy out and clear.
+extern "C" int mxa2a_trace_read(void* host, size_t bytes) {
+    if (bytes > sizeof(g_trace)) bytes = sizeof(g_trace);
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbol(host, g_trace, bytes) != cudaSuccess) return -1;
+    static unsigned char zeros[sizeof(g_trace_n)] = {};
+    if (cudaMemcpyToSymbol(g_trace_n, zeros, sizeof zeros) != cudaSuccess) return -1;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_trace) != cudaSuccess || cudaMemset(ptr, 0, sizeof(g_trace)) != cudaSuccess)
+        return -1;
+    return kTraceCap;
+}
+#endif
+
+int mxgemm_max_pairs(bool fused) { return fused ? max_pairs_impl<true>() : max_pairs_impl<false>(); }
+
+cudaError_t launch_mxgemm(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, int grid,
+                          bool fused, cudaStream_t stream) {
+    if (p.pair) {
+        if (fused) return launch_one<true, true>(p, tmap_a, tmap_b, grid, stream);
+        return launch_one<false, true>(p, tmap_a, tmap_b, grid, stream);
+    }
+    if (fused) return launch_one<true, false>(p, tmap_a, tmap_b, grid, stream);
+    return launch_one<false, false>(p, tmap_a, tmap_b, grid, stream);
 }
 
 }  // namespace mxa2a

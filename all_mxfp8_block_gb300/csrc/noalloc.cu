@@ -163,6 +163,7 @@ extern "C" int mxa2a_run_noalloc(int R, int64_t M, int64_t kPerRank, int64_t N, 
     g.box_m = (commMSize % BM == 0) ? BM : 64;
     g.zigzag = 1;
     g.rotate = 0;
+    g.group_m = 1;
     int64_t want = std::max<int64_t>(1, 8192 / kPerRank);
     int rpc = 1;
     for (int64_t d = 1; d <= commMSize; ++d)

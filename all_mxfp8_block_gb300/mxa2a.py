@@ -36,6 +36,8 @@ MXA2A_OPT_EXCHANGE_ONLY = 6
 MXA2A_OPT_FAULT_SKIP_STEP = 7
 MXA2A_OPT_GRID = 8
 MXA2A_OPT_CHUNK_BYTES = 9
+MXA2A_OPT_CTA_PAIR = 10
+MXA2A_OPT_GROUP_M = 11
 MXA2A_INFO_STEPS = 100
 MXA2A_INFO_MTILES = 101
 MXA2A_INFO_NTILES = 102
@@ -49,6 +51,10 @@ MXA2A_INFO_WORKSPACE_BYTES = 109
 MXA2A_INFO_SM_COUNT = 110
 MXA2A_INFO_LAUNCHES = 111
 MXA2A_INFO_SPLITS_UNFUSED = 112
+MXA2A_INFO_CTA_PAIR = 113
+MXA2A_INFO_CTA_PAIR_UNFUSED = 114
+MXA2A_INFO_GROUP_FUSED = 115
+MXA2A_INFO_GROUP_UNFUSED = 116
 
 MXA2A_WS_RING = 1
 MXA2A_WS_SFA = 2

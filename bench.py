@@ -253,6 +253,10 @@ def run_ours(args, w):
     plan.set_option(mxa2a.MXA2A_OPT_RECORD_EVENTS, min(4096, max(1, args.steps)))
     if args.split:
         plan.set_option(mxa2a.MXA2A_OPT_SPLIT_K, args.split)
+    if args.single_cta:
+        plan.set_option(mxa2a.MXA2A_OPT_CTA_PAIR, 0)
+    if args.group_m:
+        plan.set_option(mxa2a.MXA2A_OPT_GROUP_M, args.group_m)
     run = plan.run if args.path == "fused" else plan.run_unfused
 
     def timed_loop(fn, steps, warmup, sampler=None):
@@ -347,8 +351,12 @@ def run_ours(args, w):
                    "commMSize": w.commMSize, "buffer_num": w.buffer_num, "seed": w.seed,
                    "path": args.path, "parallelism": "replicas" if ws > 1 else "single",
                    "splits": plan.get_option(mxa2a.MXA2A_INFO_SPLITS),
+                   "cta_pair": plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR if args.path == "fused"
+                                               else mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED),
                    "grid": plan.get_option(mxa2a.MXA2A_INFO_GRID_FUSED if args.path == "fused"
                                            else mxa2a.MXA2A_INFO_GRID_UNFUSED),
+                   "raster_group_m": plan.get_option(mxa2a.MXA2A_INFO_GROUP_FUSED if args.path == "fused"
+                                                     else mxa2a.MXA2A_INFO_GROUP_UNFUSED),
                    "l2": f"flushed before every step ({flush_bytes >> 20} MiB write, 2x L2), outside the events",
                    "timer": "CUDA events on the launch stream around each library call"},
         "roofline_pct": 100.0 * t_roof / (ms_per_step / 1e3),
@@ -394,6 +402,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--split", type=int, default=0, help="force the K split of both paths (0 = automatic)")
+    ap.add_argument("--single-cta", action="store_true", help="never use the CTA-pair kernel")
+    ap.add_argument("--group-m", type=int, default=0, help="largest unfused raster group in m-tiles (0 = library default)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

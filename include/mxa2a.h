@@ -152,6 +152,13 @@ enum mxa2a_option {
     MXA2A_OPT_FAULT_SKIP_STEP = 7, /* test knob: never publish staging step k (-1 = off); waits then time out */
     MXA2A_OPT_GRID = 8,            /* cap on persistent CTAs (0 = one per SM) */
     MXA2A_OPT_CHUNK_BYTES = 9,     /* target staging copy chunk (default 8192) */
+    MXA2A_OPT_CTA_PAIR = 10,       /* 1: use the CTA-pair kernel (256-row tiles, one tcgen05
+                                      cta_group::2 MMA stream per pair) when M/128 is even and, on the
+                                      fused path, buffer_num covers the steps of a 256-row tile;
+                                      0 (default): the single-CTA kernel */
+    MXA2A_OPT_GROUP_M = 11,        /* largest raster group of the unfused path, in m rows
+                                      (128-row tiles, or tile pairs), default 16; the fused path
+                                      always consumes the staging steps one m row at a time */
     /* read-only plan facts (mxa2a_get_option only) */
     MXA2A_INFO_STEPS = 100,        /* M / commMSize */
     MXA2A_INFO_MTILES = 101,
@@ -165,7 +172,11 @@ enum mxa2a_option {
     MXA2A_INFO_WORKSPACE_BYTES = 109,
     MXA2A_INFO_SM_COUNT = 110,
     MXA2A_INFO_LAUNCHES = 111,     /* kernels launched by the last run call */
-    MXA2A_INFO_SPLITS_UNFUSED = 112  /* effective K split of the unfused path */
+    MXA2A_INFO_SPLITS_UNFUSED = 112, /* effective K split of the unfused path */
+    MXA2A_INFO_CTA_PAIR = 113,     /* 1 if the fused path runs the CTA-pair kernel */
+    MXA2A_INFO_CTA_PAIR_UNFUSED = 114, /* 1 if the unfused path runs the CTA-pair kernel */
+    MXA2A_INFO_GROUP_FUSED = 115,  /* raster group of the fused path (m rows) */
+    MXA2A_INFO_GROUP_UNFUSED = 116 /* raster group of the unfused path (m rows) */
 };
 
 int mxa2a_set_option(mxa2a_plan *plan, int key, int64_t value);

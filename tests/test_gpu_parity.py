@@ -55,10 +55,12 @@ def _check_full(w, fused=True, **opts):
 # --- targeted layout checks: exact results ------------------------------------------------
 
 @pytest.mark.parametrize("fused", [True, False])
-def test_identity_B_reproduces_A(fused):
+@pytest.mark.parametrize("M", [128, 256])
+def test_identity_B_reproduces_A(fused, M):
     """B = I (K = N): C must equal A times its scales exactly; any mix-up of
-    rows, K order, swizzle or scale-factor placement shows up here."""
-    R, M, ka = 2, 128, 128
+    rows, K order, swizzle or scale-factor placement shows up here.  M = 256
+    runs the CTA-pair kernel (two 128-row halves, B split across the pair)."""
+    R, ka = 2, 128
     K = N = R * ka
     w = inputs.Workload("identity", R, M, ka, N, 64, 2, 0)
     A = inputs.random_codes((M, K), 101)
@@ -80,10 +82,11 @@ def test_identity_B_reproduces_A(fused):
     assert np.array_equal(gv, rv), f"{np.sum(gv != rv)} of {gv.size} differ"
 
 
-def test_scale_factors_per_block_and_column():
+@pytest.mark.parametrize("M", [128, 256])
+def test_scale_factors_per_block_and_column(M):
     """One-hot B with varied B scales per 32-block and column: exercises every
     scale-factor lane/column/byte position of both operands."""
-    R, M, ka, N = 2, 128, 256, 256
+    R, ka, N = 2, 256, 256
     K = R * ka
     w = inputs.Workload("onehot", R, M, ka, N, 128, 2, 0)
     rng = np.random.default_rng(7)
@@ -172,9 +175,49 @@ def test_automatic_split_small_m():
     _check_full(w, fused=True)
 
 
+@pytest.mark.parametrize("fused", [True, False])
+def test_cta_pair_kernel_against_single_cta_kernel(fused):
+    """The CTA-pair kernel (256-row tiles, .cta_group::2 MMAs issued by the even
+    CTA) and the single-CTA kernel agree with the oracle and with each other."""
+    w = inputs.Workload("pair", 3, 768, 256, 1040, 128, 2, 59)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    outs = {}
+    for pair in (1, 0):
+        with _plan(w, cta_pair=pair, split_k=1) as p:
+            assert p.get_option(mxa2a.MXA2A_INFO_CTA_PAIR if fused else mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED) == pair
+            C = gu.run_gpu(p, d, w.M, w.N, fused=fused)
+            torch.cuda.synchronize()
+            _status_ok(p)
+            outs[pair] = gu.host_bits(C)
+    ref = gu.oracle_full(x)
+    gu.assert_parity(outs[1], ref, f"pair fused={fused}")
+    gu.assert_parity(outs[0], ref, f"single fused={fused}")
+    diff = gu.parity_stats(outs[1], outs[0])
+    assert diff["fail"] == 0, diff
+
+
 def test_zigzag_rotation_off_same_tolerance():
     w = inputs.Workload("noswizzle", 4, 512, 256, 768, 128, 2, 19)
     _check_full(w, fused=True, zigzag=0, rotate=0)
+
+
+def test_unfused_raster_groups_same_bits():
+    """The raster group only reorders the work items: group sizes 1, 3 (a
+    ragged last group over 7 m-tiles) and 16 give identical bits."""
+    w = inputs.Workload("groups", 2, 896, 256, 1536, 128, 2, 61)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    outs = []
+    for g in (1, 3, 16):
+        with _plan(w, group_m=g, split_k=1, grid=5) as p:
+            assert p.get_option(mxa2a.MXA2A_INFO_GROUP_UNFUSED) == min(g, 7)
+            outs.append(gu.host_bits(gu.run_gpu(p, d, w.M, w.N, fused=False)))
+            torch.cuda.synchronize()
+            _status_ok(p)
+    gu.assert_parity(outs[0], gu.oracle_full(x), "raster group 1")
+    for o in outs[1:]:
+        assert np.array_equal(outs[0], o)
 
 
 def test_small_grid_many_items_per_cta():
