@@ -38,6 +38,7 @@ constexpr int kBStageBytesPair = BN / 2 * BK;      // 16 KiB
 constexpr int kSfAtomBytes = 512;            // 128 rows x 4 E8M0 bytes (one 128-K block)
 constexpr int kSfaStageBytes = kSfAtomBytes;
 constexpr int kSfbStageBytes = 2 * kSfAtomBytes;
+constexpr int kEpiBufBytes = 32 * 32 * 2;    // per epilogue warp: one 32x32 BF16 chunk of C
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemAccCol = 0;          // 256 fp32 accumulator columns
@@ -110,8 +111,9 @@ struct GemmParams {
 };
 
 // Launchers (mxgemm.cu / aux_kernels.cu).  All return cudaError_t of the launch.
-cudaError_t launch_mxgemm(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, int grid,
-                          bool fused, cudaStream_t stream);
+// tmap_c: C as bf16 [M][N], box 32 rows x 32 columns, 64-byte swizzle (the epilogue's TMA stores)
+cudaError_t launch_mxgemm(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                          const CUtensorMap& tmap_c, int grid, bool fused, cudaStream_t stream);
 // CTA pairs of the pair kernel that can be resident at once (0 if it cannot run)
 int mxgemm_max_pairs(bool fused);
 cudaError_t launch_pack_a(const GemmParams& p, uint8_t* a_packed, int grid, cudaStream_t stream);

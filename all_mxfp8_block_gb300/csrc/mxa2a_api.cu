@@ -51,6 +51,20 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
     return r == CUDA_SUCCESS;
 }
 
+// C: bf16 [M][N] (N contiguous), box 32 rows x 32 columns, 64-byte swizzle
+// (the epilogue's TMA stores; see store_c_chunk).
+bool encode_c(CUtensorMap* map, void* C, uint64_t M, uint64_t N) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {N, M};
+    cuuint64_t strides[1] = {N * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int tile_span(int64_t M, int64_t cm, int64_t rows = BM) {
@@ -102,6 +116,8 @@ struct mxa2a_plan {
     size_t ring_bytes = 0, sfa_bytes = 0, sfb_bytes = 0, apacked_bytes = 0, partial_bytes = 0, flags_bytes = 0;
     CUtensorMap tmap_ring, tmap_apacked, tmap_b, tmap_b_half;
     const void* tmap_b_ptr = nullptr;
+    CUtensorMap tmap_c;                     // for the C pointer of the last run
+    const void* tmap_c_ptr = nullptr;
     unsigned long long launch_id = 0, checked_launch = 0;
     // ring of (start, end) events around the main GEMM kernel of the last runs
     static constexpr int kEvRing = 4096;
@@ -300,6 +316,10 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
     if (rc) return rc;
     if ((rc = check_device(p))) return rc;
     if ((rc = refresh_b_map(p, B))) return rc;
+    if (p->tmap_c_ptr != C) {
+        if (!encode_c(&p->tmap_c, C, (uint64_t)p->M, (uint64_t)p->N)) return MXA2A_ERR_CUDA;
+        p->tmap_c_ptr = C;
+    }
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
     int launches = 0;
     if ((rc = cuda_rc(launch_pack_sfb(static_cast<const uint8_t*>(B_sf), (int)p->N, (int)p->K, p->Ng2, p->sfb,
@@ -315,7 +335,7 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
     const int ev_slot = p->record_events ? (int)(p->ev_recorded % p->record_events) : 0;
     if (p->record_events && (rc = cuda_rc(cudaEventRecord(p->ev0[ev_slot], stream)))) return rc;
     rc = cuda_rc(launch_mxgemm(g, fused ? p->tmap_ring : p->tmap_apacked, g.pair ? p->tmap_b_half : p->tmap_b,
-                               fused ? p->grid_fused : p->grid_unfused, fused, stream));
+                               p->tmap_c, fused ? p->grid_fused : p->grid_unfused, fused, stream));
     if (rc) return rc;
     ++launches;
     if (p->record_events) {
@@ -451,6 +471,7 @@ int mxa2a_run_host(mxa2a_plan* p, const void* const* A_seg_h, const void* const*
         }
         p->io_bytes = need;
         p->tmap_b_ptr = nullptr;
+        p->tmap_c_ptr = nullptr;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream_v);
     const void* dA[kMaxSegments];

@@ -98,7 +98,8 @@ struct Lay {
     static constexpr size_t B = A + (size_t)kStg * kAStageBytes;
     static constexpr size_t Sfa = B + (size_t)kStg * kBStage;
     static constexpr size_t Sfb = Sfa + (size_t)kStg * kSfaStageBytes;
-    static constexpr size_t Ctl = Sfb + (size_t)kStg * kSfbStageBytes;
+    static constexpr size_t Epi = Sfb + (size_t)kStg * kSfbStageBytes;   // one C staging buffer per epilogue warp
+    static constexpr size_t Ctl = Epi + (size_t)kEpiWarps * kEpiBufBytes;
     static constexpr size_t Total = Ctl + sizeof(SmemCtl) + 1024;   // + runtime 1 KiB alignment
 };
 static_assert(Lay<false>::Total <= 227 * 1024 && Lay<true>::Total <= 227 * 1024, "shared memory");
@@ -475,6 +476,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bi
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// Store one 32-row x 32-column BF16 chunk of C: this warp's 32 rows (one per
+// lane, 16 packed words each) go to the warp's shared staging buffer as
+// 64-byte rows in the 64-byte swizzle (16-byte unit j of row r at unit
+// j ^ ((r >> 1) & 3), conflict-free for the 32 lanes), then lane 0 stores the
+// box with TMA at column x, row y; rows past M and columns past N are not
+// written.  Lane 0 owns the bulk group: before the buffer is rewritten its
+// previous store must have finished reading it.
+__device__ __forceinline__ void store_c_chunk(const GemmParams& p, const CUtensorMap* tmc, uint8_t* buf, int lane,
+                                              const uint32_t* w, int x, int y) {
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int pj = j ^ ((lane >> 1) & 3);
+        *reinterpret_cast<uint4*>(buf + lane * 64 + pj * 16) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    }
+    fence_proxy_async_shared();   // the generic-proxy writes, before the TMA (async proxy) reads them
+    __syncwarp();
+    if (lane == 0 && x < p.N && y < p.M) {
+        tma_store_2d(tmc, buf, x, y);
+        bulk_commit_group();
+    }
+}
+
 __device__ __forceinline__ void wait_value_u64(const GemmParams& p, SmemCtl* ctl, const unsigned long long* ptr,
                                                unsigned long long want, bool* ok) {
     // like wait_counter, for an exact epoch value
@@ -482,7 +507,8 @@ __device__ __forceinline__ void wait_value_u64(const GemmParams& p, SmemCtl* ctl
 }
 
 template <bool kPair>
-__device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, int warp, int lane, uint32_t rank) {
+__device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, int warp, int lane, uint32_t rank,
+                              const CUtensorMap* tmc, uint8_t* sEpi) {
     const int ep = warp - kWarpEpi0;         // 0..7
     const int quarter = warp & 3;            // TMEM lanes this warp may access: 32*quarter .. +31
     const int half = ep >> 2;                // accumulator columns 128*half .. +127
@@ -512,6 +538,9 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
         const int col0 = item.nt * BN + tcol;
         const uint32_t tbase = tmem + kTmemAccCol + ((uint32_t)(quarter * 32) << 16) + (uint32_t)tcol;
         constexpr int kChunks = BN / 2 / 32;             // 4 chunks of 32 columns
+        uint8_t* cbuf = sEpi + (size_t)ep * kEpiBufBytes;
+        const int row_w = mt * BM + quarter * 32;       // first row of this warp's 32 (M % 64 == 0: all
+                                                        // 32 rows are inside M or all past it)
         if (p.S == 1) {
             uint32_t packed[BN / 4];
 #pragma unroll
@@ -525,15 +554,8 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
             tc_fence_before();
             mbar_arrive(&ctl->acc_empty);   // TMEM may now take the next item
             if (leader) TRACE(7, w, 0);
-            if (row < p.M) {
-                uint16_t* dst = p.C + (size_t)row * p.N + col0;
 #pragma unroll
-                for (int j = 0; j < BN / 16; ++j) {
-                    if (col0 + j * 8 < p.N)
-                        *reinterpret_cast<uint4*>(dst + j * 8) =
-                            make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
-                }
-            }
+            for (int c = 0; c < kChunks; ++c) store_c_chunk(p, tmc, cbuf, lane, packed + c * 16, col0 + c * 32, row_w);
         } else {
             const size_t tile = (size_t)mt * p.Nt + item.nt;
             if (leader) ctl->ticket = (int)atomicAdd(&p.tile_cnt[tile], 1u);
@@ -574,14 +596,14 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
                     ctl->epi_ok = ok ? 1 : 0;
                 }
                 named_barrier_sync(2, kEpiThreads);
-                const bool ok = ctl->epi_ok != 0;
-                uint16_t* dst = p.C + (size_t)row * p.N + col0;
+                const bool ok = ctl->epi_ok != 0;   // uniform over the epilogue warps
 #pragma unroll 1
                 for (int c = 0; c < kChunks; ++c) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), v);
                     tc_wait_ld();
-                    if (ok && row < p.M) {
+                    // M is a multiple of 64, so a warp's 32 rows are all inside M or all past it
+                    if (ok && row_w < p.M) {
                         // fixed order q = 0..S-1, whichever split finished last
                         float acc[32];
 #pragma unroll
@@ -603,15 +625,11 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
                                 }
                             }
                         }
+                        uint32_t wds[16];
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            if (col0 + c * 32 + j * 8 < p.N)
-                                *reinterpret_cast<uint4*>(dst + c * 32 + j * 8) = make_uint4(
-                                    pack_bf16x2(__float_as_uint(acc[8 * j]), __float_as_uint(acc[8 * j + 1])),
-                                    pack_bf16x2(__float_as_uint(acc[8 * j + 2]), __float_as_uint(acc[8 * j + 3])),
-                                    pack_bf16x2(__float_as_uint(acc[8 * j + 4]), __float_as_uint(acc[8 * j + 5])),
-                                    pack_bf16x2(__float_as_uint(acc[8 * j + 6]), __float_as_uint(acc[8 * j + 7])));
-                        }
+                        for (int j = 0; j < 16; ++j)
+                            wds[j] = pack_bf16x2(__float_as_uint(acc[2 * j]), __float_as_uint(acc[2 * j + 1]));
+                        store_c_chunk(p, tmc, cbuf, lane, wds, col0 + c * 32, row_w);
                     }
                 }
                 tc_fence_before();
@@ -717,7 +735,7 @@ __device__ void copy_role(const GemmParams& p, SmemCtl* ctl, int ctid) {
 template <bool kFused, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     mxgemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_a,
-                  const __grid_constant__ CUtensorMap tmap_b) {
+                  const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_c) {
     using L = Lay<kPair>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -761,6 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((warp == kWarpTma || warp == kWarpTma1) && lane == 0) {
         prefetch_tensormap(&tmap_a);
         prefetch_tensormap(&tmap_b);
+        prefetch_tensormap(&tmap_c);
     }
     tc_fence_before();
     __syncthreads();
@@ -780,7 +799,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 forwarder_role(p, ctl);
         }
     } else if (warp < kWarpCopy0) {
-        if (!p.exchange_only) epilogue_role<kPair>(p, tmem, ctl, warp, lane, rank);
+        if (!p.exchange_only) {
+            epilogue_role<kPair>(p, tmem, ctl, warp, lane, rank, &tmap_c, smem + L::Epi);
+            if (lane == 0) bulk_wait_all();   // this warp's C stores are complete before the CTA ends
+        }
     } else if (kFused && warp < kWarpCopy0 + kCopyThreads / 32) {
         copy_role(p, ctl, threadIdx.x - kWarpCopy0 * 32);
     }
@@ -854,7 +876,8 @@ cudaError_t prepare(int dev) {
 }
 
 template <bool kFused, bool kPair>
-cudaError_t launch_one(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, int grid,
+cudaError_t launch_one(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                       const CUtensorMap& tmap_c, int grid,
                        cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -881,7 +904,7 @@ cudaError_t launch_one(const GemmParams& p, const CUtensorMap& tmap_a, const CUt
     }
     cfg.attrs = attr;
     cfg.numAttrs = (kPair || kFused) ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, &mxgemm_kernel<kFused, kPair>, p, tmap_a, tmap_b);
+    return cudaLaunchKernelEx(&cfg, &mxgemm_kernel<kFused, kPair>, p, tmap_a, tmap_b, tmap_c);
 }
 
 template <bool kFused>
@@ -929,14 +952,14 @@ extern "C" int mxa2a_trace_read(void* host, size_t bytes) {
 
 int mxgemm_max_pairs(bool fused) { return fused ? max_pairs_impl<true>() : max_pairs_impl<false>(); }
 
-cudaError_t launch_mxgemm(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, int grid,
-                          bool fused, cudaStream_t stream) {
+cudaError_t launch_mxgemm(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                          const CUtensorMap& tmap_c, int grid, bool fused, cudaStream_t stream) {
     if (p.pair) {
-        if (fused) return launch_one<true, true>(p, tmap_a, tmap_b, grid, stream);
-        return launch_one<false, true>(p, tmap_a, tmap_b, grid, stream);
+        if (fused) return launch_one<true, true>(p, tmap_a, tmap_b, tmap_c, grid, stream);
+        return launch_one<false, true>(p, tmap_a, tmap_b, tmap_c, grid, stream);
     }
-    if (fused) return launch_one<true, false>(p, tmap_a, tmap_b, grid, stream);
-    return launch_one<false, false>(p, tmap_a, tmap_b, grid, stream);
+    if (fused) return launch_one<true, false>(p, tmap_a, tmap_b, tmap_c, grid, stream);
+    return launch_one<false, false>(p, tmap_a, tmap_b, tmap_c, grid, stream);
 }
 
 }  // namespace mxa2a

@@ -76,6 +76,19 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// C: bf16 [M][N], box 32 rows x 32 columns, 64-byte swizzle (the epilogue's TMA stores)
+bool encode_c(CUtensorMap* map, void* C, uint64_t M, uint64_t N) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {N, M};
+    cuuint64_t strides[1] = {N * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -190,10 +203,10 @@ extern "C" int mxa2a_run_noalloc(int R, int64_t M, int64_t kPerRank, int64_t N, 
     }
     const int grid = std::max(1, std::min(sms, std::max(g.W, g.n_copy_tasks)));
 
-    CUtensorMap tmap_ring, tmap_b;
+    CUtensorMap tmap_ring, tmap_b, tmap_c;
     if (!encode_2d(&tmap_ring, g.ring, (uint64_t)kPerRank, (uint64_t)buffer_num * R * commMSize,
                    (uint32_t)g.box_m) ||
-        !encode_2d(&tmap_b, B, (uint64_t)K, (uint64_t)N, BN))
+        !encode_2d(&tmap_b, B, (uint64_t)K, (uint64_t)N, BN) || !encode_c(&tmap_c, C_bf16, (uint64_t)M, (uint64_t)N))
         return MXA2A_ERR_CUDA;
 
     // What must start at zero: the credit counters and the status block
@@ -203,6 +216,6 @@ extern "C" int mxa2a_run_noalloc(int R, int64_t M, int64_t kPerRank, int64_t N, 
     if (launch_pack_sfb(static_cast<const uint8_t*>(B_scale), (int)N, (int)K, g.Ng2, scratch + L.sfb, stream) !=
         cudaSuccess)
         return MXA2A_ERR_CUDA;
-    if (launch_mxgemm(g, tmap_ring, tmap_b, grid, true, stream) != cudaSuccess) return MXA2A_ERR_CUDA;
+    if (launch_mxgemm(g, tmap_ring, tmap_b, tmap_c, grid, true, stream) != cudaSuccess) return MXA2A_ERR_CUDA;
     return MXA2A_OK;
 }
