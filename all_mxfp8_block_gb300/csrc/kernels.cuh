@@ -9,41 +9,42 @@ namespace mxa2a {
 
 constexpr int kMaxSegments = 64;   // R limit (segment pointer tables live in kernel params)
 
-// GEMM tile per CTA: 128 rows (M) x 256 columns (N), 128-byte (= 128 FP8) K
-// blocks.  In the CTA-pair variant two CTAs compute a 256 x 256 tile with one
-// tcgen05 cta_group::2 MMA stream, each holding half of B, so a stage is
-// smaller and the ring deeper.
+// GEMM tile per CTA: 128 rows (M) x BN columns (N), 128-byte (= 128 FP8) K
+// blocks, with BN = 256 (the wide tile) or 128 (the narrow tile: twice the
+// tiles for a given rows-in-flight, and two TMEM accumulators so a tile's
+// epilogue overlaps the next tile's MMAs).  In the CTA-pair variant two CTAs
+// compute a 256 x 256 tile with one tcgen05 cta_group::2 MMA stream, each
+// holding half of B, so a stage is smaller and the ring deeper.
 constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BN = 256;            // the wide tile (also the padding unit of the B scale atoms)
+constexpr int BN_NARROW = 128;
 constexpr int BK = 128;
-constexpr int kStagesSingle = 4;
+constexpr int kStagesSingle = 4;   // wide tile: 49.5 KiB stages
+constexpr int kStagesNarrow = 6;   // narrow tile: 33 KiB stages
 constexpr int kStagesPair = 6;
 constexpr int kMaxStages = 6;
+constexpr int kMaxAccBufs = 2;
 constexpr int kThreads = 416;      // 13 warps, roles below
 constexpr int kWarpTma = 0;        // TMA producer 0 (one elected lane): even stages
 constexpr int kWarpMma = 1;        // TMEM allocator + MMA issuer (one elected lane)
 constexpr int kWarpEpi0 = 2;       // warps 2..9: epilogue, warp w drains TMEM lane quarter w%4,
 constexpr int kEpiWarps = 8;       //   column half (w-2)/4 of the accumulator
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kWarpCopy0 = 10;     // warps 10..11: staging copy (fused kernel only)
-constexpr int kCopyThreads = 64;
+constexpr int kWarpCopy0 = 10;     // warps 10..11: staging copy workers, one per warp (fused kernel only)
+constexpr int kCopyWarps = 2;
 constexpr int kWarpTma1 = 12;      // TMA producer 1 (one elected lane): odd stages
 // One thread's TMA loads overlap poorly (about one stage per 0.4 us per
 // thread on this GPU); two issuing warps double the per-SM load rate.
 constexpr int kProducers = 2;
 
 constexpr int kAStageBytes = BM * BK;        // 16 KiB
-constexpr int kBStageBytesSingle = BN * BK;        // 32 KiB
-constexpr int kBStageBytesPair = BN / 2 * BK;      // 16 KiB
 constexpr int kSfAtomBytes = 512;            // 128 rows x 4 E8M0 bytes (one 128-K block)
 constexpr int kSfaStageBytes = kSfAtomBytes;
-constexpr int kSfbStageBytes = 2 * kSfAtomBytes;
 constexpr int kEpiBufBytes = 32 * 32 * 2;    // per epilogue warp: one 32x32 BF16 chunk of C
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemAccCol = 0;          // 256 fp32 accumulator columns
-constexpr uint32_t kTmemSfCol = 256;         // per stage: 4 SFA + 8 SFB columns
-constexpr uint32_t kTmemSfColsPerStage = 12;
+constexpr uint32_t kTmemAccCol = 0;          // accumulators: 1 x 256 (wide) or 2 x 128 (narrow) fp32 columns
+constexpr uint32_t kTmemSfCol = 256;         // per stage: 4 SFA + 4 per 128 B columns
 
 // Device error codes written to the status block (same numbers as the C ABI).
 constexpr int kErrTimeout = 6;
@@ -61,10 +62,11 @@ struct DevStatus {
 // Monotonic credit counters of the staging ring, each on its own 128-byte line.
 // filled[slot][r]:  staging copy chunks published for (slot, segment r)
 // drained[slot][r]: work items that finished reading segment r of the slot
-// staged[slot]:     segments of the slot completely published (all chunks);
-//                   lets a reader check a whole step with one load
+// staged[slot]:     chunks of all segments of the slot published; lets a
+//                   reader check a whole step with one load
 // cta_done:         CTAs that reached the end (the last one zeroes everything)
 // copy_next:        next staging copy task to claim (tasks are claimed in order)
+// sfb_done:         CTAs that finished their slice of the B scale pack (kernel prologue)
 struct FlagLayout {
     static constexpr int kLine = 16;  // 16 x u64 = 128 bytes
     __host__ __device__ static size_t filled(int slot, int r, int R) { return (size_t)(slot * R + r) * kLine; }
@@ -74,13 +76,15 @@ struct FlagLayout {
     __host__ __device__ static size_t staged(int slot, int bn, int R) { return (size_t)(2 * bn * R + slot) * kLine; }
     __host__ __device__ static size_t cta_done(int bn, int R) { return (size_t)(2 * bn * R + bn) * kLine; }
     __host__ __device__ static size_t copy_next(int bn, int R) { return (size_t)(2 * bn * R + bn + 1) * kLine; }
-    __host__ __device__ static size_t words(int bn, int R) { return (size_t)(2 * bn * R + bn + 2) * kLine; }
+    __host__ __device__ static size_t sfb_done(int bn, int R) { return (size_t)(2 * bn * R + bn + 2) * kLine; }
+    __host__ __device__ static size_t words(int bn, int R) { return (size_t)(2 * bn * R + bn + 3) * kLine; }
 };
 
 struct GemmParams {
     int R, M, N, ka, K, cm, bn, steps;
     int Mt, Nt, S, W;           // m-tiles, n-tiles, K splits, work items
     int pair;                   // 1: CTA-pair kernel, work items are pairs of m-tiles (Mt even)
+    int tile_n;                 // BN of this launch: 256 or 128 (Nt = ceil(N / tile_n))
     int kb_per_seg;             // ka / 128
     int Mg, Ng2;                // 128-row groups of A (scale atoms), 128-col groups of B (padded to 256)
     int box_m;                  // rows per A TMA box: 128 or 64
@@ -88,12 +92,17 @@ struct GemmParams {
     int group_m;                // m rows (tiles, or tile pairs) per raster group
     const uint8_t* sfa;         // A scales, MMA atom layout [K/128][Mg][512]
     const uint8_t* sfb;         // B scales, MMA atom layout [K/128][Ng2][512]
+    // sfb_inline: the kernel's prologue packs B_scale ([N][K/32] E8M0) into sfb
+    // (every CTA a slice, counted on the sfb_done flag) instead of a separate
+    // pack kernel; needs all CTAs resident (cooperative launch)
+    int sfb_inline;
+    const uint8_t* B_scale;
     uint16_t* C;                // bf16 [M][N]
     // split-K (S > 1): items of one output tile finish in any order; all but the
     // last write their fp32 tile to partial[tile][q] ([BM][BN]) and publish
     // ready[tile][q] = launch_id; the last (ticket S-1 of tile_cnt[tile]) sums
     // q = 0..S-1 in order, writes C and zeroes tile_cnt[tile]
-    float* partial;             // fp32 [Mt*Nt][S][BN/4][BM][4] (4-column chunks, row-contiguous)
+    float* partial;             // fp32 [Mt*Nt][S][tile_n/4][BM][4] (4-column chunks, row-contiguous)
     unsigned* tile_cnt;         // [Mt*Nt]
     unsigned long long* ready;  // [Mt*Nt][S]
     // fused staging

@@ -87,7 +87,10 @@ struct mxa2a_plan {
     int device = 0, sm_count = 0;
     // derived
     int64_t K = 0;
-    int steps = 0, Mt = 0, Nt = 0, Mg = 0, Ng2 = 0, box_m = 128, span = 1;
+    int steps = 0, Mt = 0, Nt = 0, Mg = 0, Ng2 = 0, box_m = 128, span = 1;   // Nt: wide (256-column) tiles
+    int tn_fused = BN, tn_unfused = BN;     // tile width per path (256, or 128 = the narrow tile)
+    int Nt_fused = 0, Nt_unfused = 0;       // n-tiles per path
+    int tile_opt = 0;                       // option: 0 automatic, 128 or 256 forced
     int S_fused = 1, S_unfused = 1, W_fused = 0, W_unfused = 0;   // K splits and work items per path
     int pair_fused = 0, pair_unfused = 0;   // CTA-pair kernel in use, per path
     int group_fused = 1, group_unfused = 1; // raster group, in m rows (tiles or tile pairs)
@@ -157,8 +160,6 @@ void derive(mxa2a_plan* p) {
         return std::max(1, S);
     };
     const int window_mtiles = (int)std::min<int64_t>(p->Mt, (p->bn * p->cm + BM - 1) / BM);
-    p->S_fused = split_for(window_mtiles * p->Nt);
-    p->S_unfused = split_for(p->Mt * p->Nt);
     // The CTA-pair kernel computes 256-row tiles with one 2-CTA MMA stream; it
     // needs an even number of 128-row tiles and clusters of two resident CTAs.
     // Both halves of a pair tile are consumed in lock step, so the fused path
@@ -166,8 +167,25 @@ void derive(mxa2a_plan* p) {
     const bool pair_ok = p->allow_pair && p->Mt % 2 == 0;
     p->pair_unfused = (pair_ok && p->max_pairs_unfused > 0) ? 1 : 0;
     p->pair_fused = (pair_ok && p->max_pairs_fused > 0 && p->bn >= tile_span(p->M, p->cm, 2 * BM)) ? 1 : 0;
-    p->W_fused = (p->pair_fused ? p->Mt / 2 : p->Mt) * p->Nt * p->S_fused;
-    p->W_unfused = (p->pair_unfused ? p->Mt / 2 : p->Mt) * p->Nt * p->S_unfused;
+    // Tile width.  The narrow 128-column tile gives twice the work items for
+    // the same rows in flight (the fused path can only work on the rows in the
+    // staging ring) and double-buffers the TMEM accumulator, at 1.33x the
+    // operand bytes per flop.  Measured on GB300 a K block costs nearly as much
+    // time narrow as wide (the per-stage load and issue work does not shrink
+    // with the tile), so the wide tile is the default and the narrow one an
+    // option.  The CTA-pair kernel has wide tiles only.
+    auto pick = [&](bool pair) {
+        if (pair) return BN;
+        return p->tile_opt ? p->tile_opt : BN;
+    };
+    p->tn_fused = pick(p->pair_fused);
+    p->tn_unfused = pick(p->pair_unfused);
+    p->Nt_fused = (int)((p->N + p->tn_fused - 1) / p->tn_fused);
+    p->Nt_unfused = (int)((p->N + p->tn_unfused - 1) / p->tn_unfused);
+    p->S_fused = split_for(window_mtiles * p->Nt_fused);
+    p->S_unfused = split_for(p->Mt * p->Nt_unfused);
+    p->W_fused = (p->pair_fused ? p->Mt / 2 : p->Mt) * p->Nt_fused * p->S_fused;
+    p->W_unfused = (p->pair_unfused ? p->Mt / 2 : p->Mt) * p->Nt_unfused * p->S_unfused;
     // Raster groups (m rows processed n-tile outer inside a group).  Unfused:
     // up to group_cap m rows, so the CTAs in flight share a few B tiles and A
     // rows in L2.  Fused: one m row.  A fused group must be whole staging
@@ -236,7 +254,8 @@ void fill_params(mxa2a_plan* p, GemmParams& g, const void* const* A_seg, const v
     g.bn = p->bn;
     g.steps = p->steps;
     g.Mt = p->Mt;
-    g.Nt = p->Nt;
+    g.Nt = fused ? p->Nt_fused : p->Nt_unfused;
+    g.tile_n = fused ? p->tn_fused : p->tn_unfused;
     g.S = fused ? p->S_fused : p->S_unfused;
     g.W = fused ? p->W_fused : p->W_unfused;
     g.pair = fused ? p->pair_fused : p->pair_unfused;
@@ -286,8 +305,10 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MXA2A_OK : MXA2A_ERR_CUDA
 int ensure_partials(mxa2a_plan* p) {
     const int S = std::max(p->S_fused, p->S_unfused);
     if (S <= 1) return MXA2A_OK;
-    const size_t tiles = (size_t)p->Mt * p->Nt;
-    const size_t part = tiles * S * BM * BN * sizeof(float);
+    // tile t of a path's Mt x Nt tiles holds S partials of BM x tile_n floats;
+    // Nt * tile_n <= Ng2 * 128 for both tile widths
+    const size_t tiles = (size_t)p->Mt * std::max(p->Nt_fused, p->Nt_unfused);
+    const size_t part = (size_t)p->Mt * S * BM * ((size_t)p->Ng2 * 128) * sizeof(float);
     const size_t cnt = align_up(tiles * sizeof(unsigned), 256);
     const size_t rdy = tiles * S * sizeof(unsigned long long);
     const size_t need = part + cnt + rdy;
@@ -322,19 +343,26 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
     }
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
     int launches = 0;
-    if ((rc = cuda_rc(launch_pack_sfb(static_cast<const uint8_t*>(B_sf), (int)p->N, (int)p->K, p->Ng2, p->sfb,
-                                      stream))))
-        return rc;
-    ++launches;
     GemmParams g;
     fill_params(p, g, A_seg, A_sf, C, fused);
+    // The B scale pack runs in the GEMM kernel's prologue (a cooperative
+    // launch); the CTA-pair kernel (a cluster launch) keeps the separate kernel.
+    g.B_scale = static_cast<const uint8_t*>(B_sf);
+    g.sfb_inline = g.pair ? 0 : 1;
+    if (!g.sfb_inline) {
+        if ((rc = cuda_rc(launch_pack_sfb(static_cast<const uint8_t*>(B_sf), (int)p->N, (int)p->K, p->Ng2, p->sfb,
+                                          stream))))
+            return rc;
+        ++launches;
+    }
     if (!fused) {
         if ((rc = cuda_rc(launch_pack_a(g, p->a_packed, 0, stream)))) return rc;
         ++launches;
     }
     const int ev_slot = p->record_events ? (int)(p->ev_recorded % p->record_events) : 0;
     if (p->record_events && (rc = cuda_rc(cudaEventRecord(p->ev0[ev_slot], stream)))) return rc;
-    rc = cuda_rc(launch_mxgemm(g, fused ? p->tmap_ring : p->tmap_apacked, g.pair ? p->tmap_b_half : p->tmap_b,
+    rc = cuda_rc(launch_mxgemm(g, fused ? p->tmap_ring : p->tmap_apacked,
+                               (g.pair || g.tile_n == BN_NARROW) ? p->tmap_b_half : p->tmap_b,
                                p->tmap_c, fused ? p->grid_fused : p->grid_unfused, fused, stream));
     if (rc) return rc;
     ++launches;
@@ -589,6 +617,10 @@ int mxa2a_set_option(mxa2a_plan* p, int key, int64_t v) {
             if (v < 1 || v > 4096) return MXA2A_ERR_INVALID_OPTION;
             p->group_cap = (int)v;
             break;
+        case MXA2A_OPT_TILE_N:
+            if (v != 0 && v != BN_NARROW && v != BN) return MXA2A_ERR_INVALID_OPTION;
+            p->tile_opt = (int)v;
+            break;
         default:
             return MXA2A_ERR_INVALID_OPTION;
     }
@@ -610,13 +642,16 @@ int mxa2a_get_option(mxa2a_plan* p, int key, int64_t* v) {
         case MXA2A_OPT_CHUNK_BYTES: *v = p->chunk_bytes; break;
         case MXA2A_OPT_CTA_PAIR: *v = p->allow_pair; break;
         case MXA2A_OPT_GROUP_M: *v = p->group_cap; break;
+        case MXA2A_OPT_TILE_N: *v = p->tile_opt; break;
         case MXA2A_INFO_GROUP_FUSED: *v = p->group_fused; break;
         case MXA2A_INFO_GROUP_UNFUSED: *v = p->group_unfused; break;
         case MXA2A_INFO_CTA_PAIR: *v = p->pair_fused; break;
         case MXA2A_INFO_CTA_PAIR_UNFUSED: *v = p->pair_unfused; break;
         case MXA2A_INFO_STEPS: *v = p->steps; break;
         case MXA2A_INFO_MTILES: *v = p->Mt; break;
-        case MXA2A_INFO_NTILES: *v = p->Nt; break;
+        case MXA2A_INFO_NTILES: *v = p->Nt_fused; break;
+        case MXA2A_INFO_TILE_N_FUSED: *v = p->tn_fused; break;
+        case MXA2A_INFO_TILE_N_UNFUSED: *v = p->tn_unfused; break;
         case MXA2A_INFO_SPLITS: *v = p->S_fused; break;
         case MXA2A_INFO_ITEMS: *v = p->W_fused; break;
         case MXA2A_INFO_SPLITS_UNFUSED: *v = p->S_unfused; break;

@@ -73,37 +73,46 @@ struct __align__(8) SmemCtl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
     uint64_t peer_full[kMaxStages];   // pair kernel, even CTA: the odd CTA's stage landed
-    uint64_t acc_full;
-    uint64_t acc_empty;
+    uint64_t acc_full[kMaxAccBufs];    // per TMEM accumulator buffer
+    uint64_t acc_empty[kMaxAccBufs];
     uint64_t acc_empty_peer;          // pair kernel, even CTA: the odd CTA drained its TMEM
     uint64_t drain;
     uint32_t tmem_base;
     volatile int abort;
     volatile int issued[kProducers];   // per producer: 1 + index of its last issued stage
     volatile int consumed;   // stages whose full barrier the MMA thread has passed
-    volatile int copy_go;    // copy-role broadcast
-    volatile int copy_task;
     volatile int ticket;     // split-K arrival order of the current tile (epilogue broadcast)
     volatile int epi_ok;     // epilogue broadcast: the other partials of the tile are ready
     volatile int epi_warp_ok[kEpiWarps];
 };
 
-// Shared-memory layout of one CTA: [A stages][B stages][SFA stages][SFB stages][control]
-template <bool kPair>
+// Per kernel variant (CTA pair or not, tile width kBN): pipeline depth, stage
+// sizes, TMEM use, and the shared-memory layout of one CTA:
+// [A stages][B stages][SFA stages][SFB stages][C staging][control]
+template <bool kPair, int kBN>
 struct Lay {
-    static constexpr int kStg = kPair ? kStagesPair : kStagesSingle;
-    static constexpr int kBRows = kPair ? BN / 2 : BN;       // rows of B this CTA loads per stage
-    static constexpr int kBStage = kPair ? kBStageBytesPair : kBStageBytesSingle;
+    static_assert(kBN == BN || (kBN == BN_NARROW && !kPair), "tile width");
+    static constexpr int kStg = kPair ? kStagesPair : (kBN == BN ? kStagesSingle : kStagesNarrow);
+    static constexpr int kBRows = kPair ? kBN / 2 : kBN;     // rows of B this CTA loads per stage
+    static constexpr int kBStage = kBRows * BK;
+    static constexpr int kSfbAtoms = kBN / 128;              // B scale atoms of the tile's columns (each
+                                                             // CTA of a pair needs all of them in its TMEM)
+    static constexpr int kSfbStage = kSfbAtoms * kSfAtomBytes;
+    static constexpr int kAccBufs = kBN == BN_NARROW ? 2 : 1;   // TMEM accumulators (512 columns hold
+                                                                 // 2 x 128 + scales, not 2 x 256 + scales)
+    static constexpr uint32_t kSfCols = 4 + 4 * kSfbAtoms;   // TMEM scale columns per stage
     static constexpr size_t A = 0;
     static constexpr size_t B = A + (size_t)kStg * kAStageBytes;
     static constexpr size_t Sfa = B + (size_t)kStg * kBStage;
     static constexpr size_t Sfb = Sfa + (size_t)kStg * kSfaStageBytes;
-    static constexpr size_t Epi = Sfb + (size_t)kStg * kSfbStageBytes;   // one C staging buffer per epilogue warp
+    static constexpr size_t Epi = Sfb + (size_t)kStg * kSfbStage;   // one C staging buffer per epilogue warp
     static constexpr size_t Ctl = Epi + (size_t)kEpiWarps * kEpiBufBytes;
     static constexpr size_t Total = Ctl + sizeof(SmemCtl) + 1024;   // + runtime 1 KiB alignment
+    static_assert(Total <= 227 * 1024, "shared memory");
+    static_assert(kStg <= kMaxStages && kAccBufs <= kMaxAccBufs, "barrier arrays");
+    static_assert(kAccBufs * kBN <= (int)kTmemSfCol && kTmemSfCol + kStg * kSfCols <= kTmemCols, "TMEM columns");
+    static_assert(Epi % 1024 == 0, "C staging buffers need 512-byte alignment for the 64-byte swizzle");
 };
-static_assert(Lay<false>::Total <= 227 * 1024 && Lay<true>::Total <= 227 * 1024, "shared memory");
-static_assert(kTmemSfCol + kMaxStages * kTmemSfColsPerStage <= kTmemCols, "TMEM columns");
 
 // ------------------------------------------------------------------ work items
 struct Item {
@@ -264,19 +273,28 @@ __device__ __forceinline__ void named_barrier_sync(int id, int count) {
 }
 
 // ------------------------------------------------------------------ roles
-template <bool kPair>
+template <bool kPair, int kBN>
 __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const CUtensorMap* tmb,
                               uint8_t* sA, uint8_t* sB, uint8_t* sSfa, uint8_t* sSfb, SmemCtl* ctl,
                               bool fused, uint32_t rank, int pid) {
-    using L = Lay<kPair>;
+    using L = Lay<kPair, kBN>;
+    // B tiles are re-read by every m-tile: keep them in L2; A (ring or packed) is read by one
+    // row of tiles at a time
+    const uint64_t pol_keep = l2_policy_evict_last();
+    const uint64_t pol_stream = l2_policy_evict_first();
     int it = 0;   // global stage sequence number; this producer issues it % kProducers == pid
+    if (p.sfb_inline) {
+        if (!wait_counter(p, ctl, p.flags + FlagLayout::sfb_done(p.bn, p.R), gridDim.x, kRoleTma, -1, -1, -1))
+            return;
+        fence_proxy_async_global();   // the atoms were written through the generic proxy; TMA reads them
+    }
     for (int w = first_item<kPair>(); w < p.W; w += item_stride<kPair>()) {
         const Item item = decode_item(p, w);
         const int mt = cta_mtile<kPair>(item, rank);
         const int nbox = fused ? num_boxes(p, mt) : 1;
         const uint32_t a_bytes = fused ? (uint32_t)(nbox * p.box_m * BK) : (uint32_t)kAStageBytes;
-        const uint32_t bytes = a_bytes + L::kBStage + kSfaStageBytes + kSfbStageBytes;
-        const int b_row = item.nt * BN + (kPair ? (int)rank * (BN / 2) : 0);
+        const uint32_t bytes = a_bytes + L::kBStage + kSfaStageBytes + L::kSfbStage;
+        const int b_row = item.nt * kBN + (kPair ? (int)rank * (kBN / 2) : 0);
         // One load per step first: when the copy role is ahead every segment
         // of the item's steps is already staged and the per-segment checks
         // (a round trip to L2 each) are skipped.  Only without a K split: then
@@ -291,7 +309,8 @@ __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const
                 const int s = (mt * BM + b * p.box_m) / p.cm;
                 if (s == last_s) continue;
                 last_s = s;
-                const unsigned long long need = (unsigned long long)(s / p.bn + 1) * (unsigned long long)p.R;
+                const unsigned long long need =
+                    (unsigned long long)(s / p.bn + 1) * (unsigned long long)(p.R * p.chunks_per_seg);
                 all_staged = ld_acquire_u64(p.flags + FlagLayout::staged(s % p.bn, p.bn, p.R)) >= need;
             }
             if (all_staged) fence_proxy_async_global();
@@ -330,18 +349,19 @@ __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const
                         const int row0 = mt * BM + b * p.box_m;
                         const int s = row0 / p.cm;
                         const int ring_row = ((s % p.bn) * p.R + r) * p.cm + (row0 - s * p.cm);
-                        tma_load_2d(a_dst + (size_t)b * p.box_m * BK, tma, bar, kx, ring_row);
+                        tma_load_2d_hint(a_dst + (size_t)b * p.box_m * BK, tma, bar, kx, ring_row, pol_stream);
                     }
                 } else {
-                    tma_load_2d(a_dst, tma, bar, kg, mt * BM);
+                    tma_load_2d_hint(a_dst, tma, bar, kg, mt * BM, pol_stream);
                 }
-                tma_load_2d(sB + (size_t)stage * L::kBStage, tmb, bar, kg, b_row);
+                tma_load_2d_hint(sB + (size_t)stage * L::kBStage, tmb, bar, kg, b_row, pol_keep);
                 const int kbg = kg / BK;
                 bulk_load(sSfa + (size_t)stage * kSfaStageBytes,
                           p.sfa + ((size_t)kbg * p.Mg + mt) * kSfAtomBytes, kSfaStageBytes, bar);
-                // the scales of all 256 columns: each CTA's MMA share needs them in its own TMEM
-                bulk_load(sSfb + (size_t)stage * kSfbStageBytes,
-                          p.sfb + ((size_t)kbg * p.Ng2 + 2 * item.nt) * kSfAtomBytes, kSfbStageBytes, bar);
+                // the scales of all the tile's columns: each CTA's MMA share needs them in its own TMEM
+                bulk_load(sSfb + (size_t)stage * L::kSfbStage,
+                          p.sfb + ((size_t)kbg * p.Ng2 + (size_t)item.nt * L::kSfbAtoms) * kSfAtomBytes, L::kSfbStage,
+                          bar);
                 ctl->issued[pid] = it + 1;
             }
         }
@@ -361,22 +381,25 @@ __device__ __forceinline__ void return_segment_credit(const GemmParams& p, int m
     }
 }
 
-template <bool kPair>
+template <bool kPair, int kBN>
 __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_t* sB, uint8_t* sSfa,
                          uint8_t* sSfb, SmemCtl* ctl, bool fused) {
-    using L = Lay<kPair>;
+    using L = Lay<kPair, kBN>;
     // Instruction descriptor, kind::mxf8f6f4 with block scaling: A/B E4M3 (0),
     // both K-major, N>>3 at [17,23), scale type UE8M0 at bit 23, M>>4 at
     // [24,29) (M = 256 for a CTA pair); B/A scale-factor byte ids at [4,6) and
     // [29,31) select which of the four 32-wide K blocks held in each 32-bit
     // TMEM scale column is used.
     constexpr uint32_t kM = kPair ? 2 * BM : BM;
-    const uint32_t idesc_base = ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((kM >> 4) << 24);
+    const uint32_t idesc_base = ((uint32_t)(kBN >> 3) << 17) | (1u << 23) | ((kM >> 4) << 24);
     int it = 0;
-    uint32_t acc_ph = 0;
-    for (int w = first_item<kPair>(); w < p.W; w += item_stride<kPair>()) {
+    int n = 0;   // items done; item n accumulates in buffer n % kAccBufs
+    for (int w = first_item<kPair>(); w < p.W; w += item_stride<kPair>(), ++n) {
         const Item item = decode_item(p, w);
-        if (!wait_mbar(p, ctl, &ctl->acc_empty, acc_ph ^ 1u, kRoleMma)) return;
+        const int buf = n % L::kAccBufs;
+        const uint32_t acc_ph = (uint32_t)(n / L::kAccBufs) & 1u;
+        const uint32_t acc_col = tmem + kTmemAccCol + (uint32_t)(buf * kBN);
+        if (!wait_mbar(p, ctl, &ctl->acc_empty[buf], acc_ph ^ 1u, kRoleMma)) return;
         if (kPair && !wait_mbar(p, ctl, &ctl->acc_empty_peer, acc_ph ^ 1u, kRoleMma)) return;
         tc_fence_after();
         TRACE(1, w, 0);
@@ -389,32 +412,32 @@ __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_
             ctl->consumed = it + 1;
             if (j == 0) TRACE(2, w, 0);
             tc_fence_after();
-            const uint32_t sf_t = tmem + kTmemSfCol + (uint32_t)stage * kTmemSfColsPerStage;
+            const uint32_t sf_t = tmem + kTmemSfCol + (uint32_t)stage * L::kSfCols;
             const uint32_t sfa_s = smem_u32(sSfa + (size_t)stage * kSfaStageBytes);
-            const uint32_t sfb_s = smem_u32(sSfb + (size_t)stage * kSfbStageBytes);
+            const uint32_t sfb_s = smem_u32(sSfb + (size_t)stage * L::kSfbStage);
             const uint64_t adesc = smem_desc(smem_u32(sA + (size_t)stage * kAStageBytes), 16, 1024, kLayoutSw128);
             const uint64_t bdesc = smem_desc(smem_u32(sB + (size_t)stage * L::kBStage), 16, 1024, kLayoutSw128);
             if (kPair) {
                 tc_cp_32x128b_warpx4_pair(sf_t, smem_desc(sfa_s, 0, 128, kLayoutNone));
-                tc_cp_32x128b_warpx4_pair(sf_t + 4, smem_desc(sfb_s, 0, 128, kLayoutNone));
-                tc_cp_32x128b_warpx4_pair(sf_t + 8, smem_desc(sfb_s + kSfAtomBytes, 0, 128, kLayoutNone));
+#pragma unroll
+                for (int a = 0; a < L::kSfbAtoms; ++a)
+                    tc_cp_32x128b_warpx4_pair(sf_t + 4 + 4 * a, smem_desc(sfb_s + a * kSfAtomBytes, 0, 128, kLayoutNone));
 #pragma unroll
                 for (int k = 0; k < BK / 32; ++k) {
                     const uint32_t idesc = idesc_base | ((uint32_t)k << 4) | ((uint32_t)k << 29);
-                    mma_mxf8f6f4_pair(tmem + kTmemAccCol, adesc + 2ull * k, bdesc + 2ull * k, idesc, sf_t, sf_t + 4,
-                                      (j | k) != 0);
+                    mma_mxf8f6f4_pair(acc_col, adesc + 2ull * k, bdesc + 2ull * k, idesc, sf_t, sf_t + 4, (j | k) != 0);
                 }
                 tc_commit_pair_multicast(&ctl->empty[stage], 0x3);
             } else {
                 tc_cp_32x128b_warpx4(sf_t, smem_desc(sfa_s, 0, 128, kLayoutNone));
-                tc_cp_32x128b_warpx4(sf_t + 4, smem_desc(sfb_s, 0, 128, kLayoutNone));
-                tc_cp_32x128b_warpx4(sf_t + 8, smem_desc(sfb_s + kSfAtomBytes, 0, 128, kLayoutNone));
+#pragma unroll
+                for (int a = 0; a < L::kSfbAtoms; ++a)
+                    tc_cp_32x128b_warpx4(sf_t + 4 + 4 * a, smem_desc(sfb_s + a * kSfAtomBytes, 0, 128, kLayoutNone));
 #pragma unroll
                 for (int k = 0; k < BK / 32; ++k) {
                     const uint32_t idesc = idesc_base | ((uint32_t)k << 4) | ((uint32_t)k << 29);
                     // +32 bytes along K inside the 128-byte swizzle atom = +2 in the encoded start address
-                    mma_mxf8f6f4(tmem + kTmemAccCol, adesc + 2ull * k, bdesc + 2ull * k, idesc, sf_t, sf_t + 4,
-                                 (j | k) != 0);
+                    mma_mxf8f6f4(acc_col, adesc + 2ull * k, bdesc + 2ull * k, idesc, sf_t, sf_t + 4, (j | k) != 0);
                 }
                 tc_commit(&ctl->empty[stage]);
             }
@@ -432,11 +455,10 @@ __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_
             }
         }
         if (kPair)
-            tc_commit_pair_multicast(&ctl->acc_full, 0x3);
+            tc_commit_pair_multicast(&ctl->acc_full[buf], 0x3);
         else
-            tc_commit(&ctl->acc_full);
+            tc_commit(&ctl->acc_full[buf]);
         TRACE(3, w, 0);
-        acc_ph ^= 1u;
     }
 }
 
@@ -447,7 +469,7 @@ __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_
 // peer_full[] and acc_empty_peer barriers.  Before item i (i >= 1) the even
 // CTA waits for phase i-1 of acc_empty_peer, i.e. the drain of item i-1.
 __device__ void forwarder_role(const GemmParams& p, SmemCtl* ctl) {
-    using L = Lay<true>;
+    using L = Lay<true, BN>;   // one accumulator buffer
     const uint32_t leader_full = mapa_shared(smem_u32(&ctl->peer_full[0]), 0);
     const uint32_t leader_acc = mapa_shared(smem_u32(&ctl->acc_empty_peer), 0);
     int it = 0;
@@ -456,7 +478,7 @@ __device__ void forwarder_role(const GemmParams& p, SmemCtl* ctl) {
         const Item item = decode_item(p, w);
         if (n_items > 0) {
             // this CTA's epilogue drained item n_items-1 (phase n_items-1 of acc_empty)
-            if (!wait_mbar(p, ctl, &ctl->acc_empty, (uint32_t)(n_items - 1) & 1u, kRoleMma)) return;
+            if (!wait_mbar(p, ctl, &ctl->acc_empty[0], (uint32_t)(n_items - 1) & 1u, kRoleMma)) return;
             mbar_arrive_remote(leader_acc);
         }
         const int total = item.nseg * p.kb_per_seg;
@@ -495,7 +517,7 @@ __device__ __forceinline__ void store_c_chunk(const GemmParams& p, const CUtenso
     fence_proxy_async_shared();   // the generic-proxy writes, before the TMA (async proxy) reads them
     __syncwarp();
     if (lane == 0 && x < p.N && y < p.M) {
-        tma_store_2d(tmc, buf, x, y);
+        tma_store_2d_hint(tmc, buf, x, y, l2_policy_evict_first());   // C is written once: do not keep it in L2
         bulk_commit_group();
     }
 }
@@ -506,18 +528,21 @@ __device__ __forceinline__ void wait_value_u64(const GemmParams& p, SmemCtl* ctl
     if (!wait_counter(p, ctl, ptr, want, kRoleEpi, -1, -1, -1)) *ok = false;
 }
 
-template <bool kPair>
+template <bool kPair, int kBN>
 __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, int warp, int lane, uint32_t rank,
                               const CUtensorMap* tmc, uint8_t* sEpi) {
+    using L = Lay<kPair, kBN>;
     const int ep = warp - kWarpEpi0;         // 0..7
     const int quarter = warp & 3;            // TMEM lanes this warp may access: 32*quarter .. +31
-    const int half = ep >> 2;                // accumulator columns 128*half .. +127
+    const int half = ep >> 2;                // accumulator columns (kBN/2)*half .. +kBN/2-1
     const bool leader = (ep == 0 && lane == 0);
-    uint32_t acc_ph = 0;
-    for (int w = first_item<kPair>(); w < p.W; w += item_stride<kPair>()) {
+    int n = 0;   // items done; item n is in accumulator buffer n % kAccBufs
+    for (int w = first_item<kPair>(); w < p.W; w += item_stride<kPair>(), ++n) {
         const Item item = decode_item(p, w);
         const int mt = cta_mtile<kPair>(item, rank);
-        const bool got = wait_mbar_warp(p, ctl, &ctl->acc_full, acc_ph, kRoleEpi);
+        const int buf = n % L::kAccBufs;
+        const uint32_t acc_ph = (uint32_t)(n / L::kAccBufs) & 1u;
+        const bool got = wait_mbar_warp(p, ctl, &ctl->acc_full[buf], acc_ph, kRoleEpi);
         if (p.S > 1) {
             // the split path synchronises the 8 epilogue warps on a named barrier:
             // leave only all together
@@ -534,15 +559,16 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
         tc_fence_after();
         const int lrow = quarter * 32 + lane;            // row inside the tile
         const int row = mt * BM + lrow;
-        const int tcol = half * (BN / 2);                // first accumulator column of this warp
-        const int col0 = item.nt * BN + tcol;
-        const uint32_t tbase = tmem + kTmemAccCol + ((uint32_t)(quarter * 32) << 16) + (uint32_t)tcol;
-        constexpr int kChunks = BN / 2 / 32;             // 4 chunks of 32 columns
+        const int tcol = half * (kBN / 2);               // first accumulator column of this warp
+        const int col0 = item.nt * kBN + tcol;
+        const uint32_t tbase =
+            tmem + kTmemAccCol + (uint32_t)(buf * kBN) + ((uint32_t)(quarter * 32) << 16) + (uint32_t)tcol;
+        constexpr int kChunks = kBN / 2 / 32;            // chunks of 32 columns per warp
         uint8_t* cbuf = sEpi + (size_t)ep * kEpiBufBytes;
         const int row_w = mt * BM + quarter * 32;       // first row of this warp's 32 (M % 64 == 0: all
                                                         // 32 rows are inside M or all past it)
         if (p.S == 1) {
-            uint32_t packed[BN / 4];
+            uint32_t packed[kBN / 4];
 #pragma unroll
             for (int c = 0; c < kChunks; ++c) {
                 uint32_t v[32];
@@ -552,7 +578,7 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
                 for (int j = 0; j < 16; ++j) packed[c * 16 + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
             }
             tc_fence_before();
-            mbar_arrive(&ctl->acc_empty);   // TMEM may now take the next item
+            mbar_arrive(&ctl->acc_empty[buf]);   // this accumulator may now take a later item
             if (leader) TRACE(7, w, 0);
 #pragma unroll
             for (int c = 0; c < kChunks; ++c) store_c_chunk(p, tmc, cbuf, lane, packed + c * 16, col0 + c * 32, row_w);
@@ -561,12 +587,12 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
             if (leader) ctl->ticket = (int)atomicAdd(&p.tile_cnt[tile], 1u);
             named_barrier_sync(2, kEpiThreads);
             const bool last = ctl->ticket == p.S - 1;
-            // partial tile layout [BN/4][BM][4]: thread `lrow` of a warp stores the
+            // partial tile layout [kBN/4][BM][4]: thread `lrow` of a warp stores the
             // float4 of columns 4g..4g+3 at (g*BM + lrow)*4, so each warp store
             // covers 512 contiguous bytes
-            float* part_tile = p.partial + tile * (size_t)p.S * (BM * BN);
+            float* part_tile = p.partial + tile * (size_t)p.S * (BM * kBN);
             if (!last) {
-                float* dst = part_tile + (size_t)item.q * (BM * BN) + ((size_t)(tcol / 4) * BM + lrow) * 4;
+                float* dst = part_tile + (size_t)item.q * (BM * kBN) + ((size_t)(tcol / 4) * BM + lrow) * 4;
 #pragma unroll 1
                 for (int c = 0; c < kChunks; ++c) {
                     uint32_t v[32];
@@ -580,7 +606,7 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&ctl->acc_empty);
+                mbar_arrive(&ctl->acc_empty[buf]);
                 __threadfence();
                 named_barrier_sync(2, kEpiThreads);
                 if (leader)
@@ -613,7 +639,7 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
 #pragma unroll
                                 for (int e = 0; e < 32; ++e) acc[e] += __uint_as_float(v[e]);
                             } else {
-                                const float* src = part_tile + (size_t)q * (BM * BN) +
+                                const float* src = part_tile + (size_t)q * (BM * kBN) +
                                                    ((size_t)(tcol / 4 + c * 8) * BM + lrow) * 4;
 #pragma unroll
                                 for (int j = 0; j < 8; ++j) {
@@ -633,70 +659,110 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&ctl->acc_empty);
+                mbar_arrive(&ctl->acc_empty[buf]);
                 if (leader) p.tile_cnt[tile] = 0u;   // ready for the next launch
                 if (!ok) return;
             }
         }
-        acc_ph ^= 1u;
     }
 }
 
-__device__ __forceinline__ void copy_bytes(const uint8_t* src, uint8_t* dst, long long bytes, int tid) {
-    constexpr int U = 8;
+// One warp copies `bytes` (a multiple of 16): 16 loads of 16 bytes in flight
+// per lane (8 KiB per round), then the stores.
+__device__ __forceinline__ void copy_bytes(const uint8_t* src, uint8_t* dst, long long bytes, int lane) {
+    constexpr int U = 16;
     const long long n16 = bytes >> 4;
     const uint4* s = reinterpret_cast<const uint4*>(src);
     uint4* d = reinterpret_cast<uint4*>(dst);
-    for (long long base = tid; base < n16; base += (long long)kCopyThreads * U) {
+    for (long long base = lane; base < n16; base += 32LL * U) {
         uint4 v[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const long long i = base + (long long)u * kCopyThreads;
+            const long long i = base + (long long)u * 32;
             if (i < n16) v[u] = ld_nc_v4(s + i);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const long long i = base + (long long)u * kCopyThreads;
+            const long long i = base + (long long)u * 32;
             if (i < n16) d[i] = v[u];
         }
     }
+}
+
+// Copy task t = (step, segment, chunk) in that order.  It may overwrite its
+// ring slot once every reader of that segment of the earlier steps that used
+// the slot has returned its credit.
+__device__ __forceinline__ bool copy_task_ready(const GemmParams& p, int t, int per_step,
+                                                unsigned long long* observed, unsigned long long* target) {
+    const int s = t / per_step;
+    if (s < p.bn || p.exchange_only) return true;
+    const int r = (t - s * per_step) / p.chunks_per_seg;
+    const int slot = s % p.bn;
+    unsigned long long need = 0;
+    for (int s2 = slot; s2 < s; s2 += p.bn) need += readers_of_segment(p, s2);
+    const unsigned long long v = ld_acquire_u64(p.flags + FlagLayout::drained(slot, r, p.bn, p.R));
+    *observed = v;
+    *target = need;
+    return v >= need;
 }
 
 // The exchange of the pages (AllToAllComm::PutToAllRanks, one put per peer
 // and step) becomes: for each (step, segment, chunk) in step order, wait for
 // the slot's credit, copy commMSize/chunks rows of A_seg[r] into
 // ring[slot][r], scatter their scales into the MMA scale layout, publish.
-__device__ void copy_role(const GemmParams& p, SmemCtl* ctl, int ctid) {
+//
+// Each copy warp of a CTA is an independent worker that claims one task at a
+// time from a global counter (so a segment's chunks spread over many workers
+// when its slot drains) and waits for the task's credit in place.  A task
+// costs a few memory round trips of latency (claim, credit check, copy,
+// publish), so the exchange keeps up by having many workers and a short
+// publish: lane 0 releases the counters without waiting for a reply.
+// (Measured on GB300 against holding several claimed tasks per worker and
+// against claiming in pairs: both lengthen the copy of a freshly drained
+// segment, which sits on the critical path of the staging ring.)
+__device__ void copy_role(const GemmParams& p, SmemCtl* ctl, int lane) {
     const int per_step = p.R * p.chunks_per_seg;
     const long long chunk_bytes = (long long)p.rows_per_chunk * p.ka;
     const int sf_cols = p.ka / 32;
     unsigned long long* next = p.flags + FlagLayout::copy_next(p.bn, p.R);
     for (;;) {
-        // Tasks are claimed from one global counter in (step, segment, chunk)
-        // order, so a copy role waiting for one slot's credit never holds back
-        // tasks that another CTA could already copy.
-        if (ctid == 0) {
-            int t = ctl->abort ? p.n_copy_tasks : (int)atomicAdd(next, 1ull);
-            bool ok = t < p.n_copy_tasks;
-            if (ok) TRACE(8, t, 0);
-            if (ok) {
-                const int s = t / per_step;
-                const int r = (t - s * per_step) / p.chunks_per_seg;
-                const int slot = s % p.bn;
-                if (s >= p.bn && !p.exchange_only) {
-                    unsigned long long target = 0;
-                    for (int s2 = slot; s2 < s; s2 += p.bn) target += readers_of_segment(p, s2);
-                    ok = wait_counter(p, ctl, p.flags + FlagLayout::drained(slot, r, p.bn, p.R), target,
-                                      kRoleCopy, s, r, slot);
+        int chosen = -1;
+        if (lane == 0 && !ctl->abort) {
+            const int t = (int)atomicAdd(next, 1ull);
+            if (t < p.n_copy_tasks) {
+                TRACE(8, t, 0);
+                unsigned long long obs = 0, tgt = 0;
+                bool ok = copy_task_ready(p, t, per_step, &obs, &tgt);
+                const uint64_t t0 = globaltimer();
+                uint32_t nap = 64;   // back-off keeps the pollers off the counters' L2 lines
+                for (uint32_t n = 1; !ok; ++n) {
+                    __nanosleep(nap);
+                    if (nap < 1024) nap <<= 1;
+                    ok = copy_task_ready(p, t, per_step, &obs, &tgt);
+                    if (ok) break;
+                    if (ctl->abort) break;
+                    if ((n & 15) == 0) {
+                        if (globaltimer() - t0 > (uint64_t)p.timeout_ns) {
+                            const int s = t / per_step;
+                            const int r = (t - s * per_step) / p.chunks_per_seg;
+                            record_error(p, kErrTimeout, kRoleCopy, s, r, s % p.bn, (long long)obs, (long long)tgt);
+                            ctl->abort = 1;
+                            break;
+                        }
+                        if (launch_failed(p)) {
+                            ctl->abort = 1;
+                            break;
+                        }
+                    }
+                }
+                if (ok) {
+                    chosen = t;
+                    TRACE(9, t, 0);
                 }
             }
-            if (ok) TRACE(9, t, 0);
-            ctl->copy_task = t;
-            ctl->copy_go = ok ? 1 : 0;
         }
-        named_barrier_sync(1, kCopyThreads);
-        if (!ctl->copy_go) return;   // uniform over the 64 copy threads
-        const int t = ctl->copy_task;
+        const int t = __shfl_sync(0xffffffffu, chosen, 0);
+        if (t < 0) return;   // uniform over the warp
         const int s = t / per_step;
         const int rem = t - s * per_step;
         const int r = rem / p.chunks_per_seg;
@@ -705,11 +771,11 @@ __device__ void copy_role(const GemmParams& p, SmemCtl* ctl, int ctid) {
         const int row0 = s * p.cm + c * p.rows_per_chunk;
         copy_bytes(p.A_seg[r] + (size_t)row0 * p.ka,
                    p.ring + ((size_t)(slot * p.R + r) * p.cm + (size_t)c * p.rows_per_chunk) * p.ka, chunk_bytes,
-                   ctid);
+                   lane);
         // scales of these rows: one u32 (4 E8M0 bytes = one 128-K block) per
         // (row, K block), placed at (row%32)*4 + (row%128)/32 of the block's atom
         const int nsf = p.rows_per_chunk * p.kb_per_seg;
-        for (int i = ctid; i < nsf; i += kCopyThreads) {
+        for (int i = lane; i < nsf; i += 32) {
             const int kb = i / p.rows_per_chunk;
             const int m = row0 + (i - kb * p.rows_per_chunk);
             const uint32_t v = ld_nc_u32(p.A_sf_seg[r] + (size_t)m * sf_cols + kb * 4);
@@ -717,26 +783,43 @@ __device__ void copy_role(const GemmParams& p, SmemCtl* ctl, int ctid) {
             uint32_t* atom = reinterpret_cast<uint32_t*>(p.sfa_stage + ((size_t)kbg * p.Mg + m / BM) * kSfAtomBytes);
             atom[(m & 31) * 4 + ((m & 127) >> 5)] = v;
         }
-        __threadfence();
+        // Publish: the warp barrier orders every lane's stores before lane 0's
+        // release (cumulative at gpu scope); readers acquire the counter and
+        // then read the ring through the async proxy (TMA).
         fence_proxy_async_global();
-        named_barrier_sync(1, kCopyThreads);
-        if (ctid == 0 && s != p.fault_skip_step) {
-            // the chunk that completes the segment also counts it as staged
-            const unsigned long long before =
-                atom_acq_rel_add_u64(p.flags + FlagLayout::filled(slot, r, p.R), 1ull);
-            if (before + 1 == (unsigned long long)(s / p.bn + 1) * (unsigned long long)p.chunks_per_seg)
-                red_release_add_u64(p.flags + FlagLayout::staged(slot, p.bn, p.R), 1ull);
+        __syncwarp();
+        if (lane == 0 && s != p.fault_skip_step) {
+            __threadfence();
+            red_release_add_u64(p.flags + FlagLayout::filled(slot, r, p.R), 1ull);
+            red_release_add_u64(p.flags + FlagLayout::staged(slot, p.bn, p.R), 1ull);
             TRACE(10, t, 0);
         }
     }
 }
 
+// A slice of the B scale pack (the same byte permutation as pack_sfb_kernel):
+// word (kbg, n) of the atoms = the 4 E8M0 bytes of column n for 128-wide K
+// block kbg, at (n%32)*4 + (n%128)/32 of atom (kbg, n/128); columns past N
+// get 0.
+__device__ void pack_sfb_slice(const GemmParams& p) {
+    uint32_t* sfb = reinterpret_cast<uint32_t*>(const_cast<uint8_t*>(p.sfb));   // written only here
+    const int cols = p.Ng2 * 128;
+    const long long total = (long long)(p.K / BK) * cols;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int n = (int)(i % cols);
+        const int kbg = (int)(i / cols);
+        const uint32_t v = n < p.N ? ld_nc_u32(p.B_scale + (size_t)n * (p.K / 32) + (size_t)kbg * 4) : 0u;
+        sfb[((size_t)kbg * p.Ng2 + (size_t)(n >> 7)) * (kSfAtomBytes / 4) + (size_t)((n & 31) * 4 + ((n & 127) >> 5))] = v;
+    }
+}
+
 // ------------------------------------------------------------------ kernel
-template <bool kFused, bool kPair>
+template <bool kFused, bool kPair, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
     mxgemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_a,
                   const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_c) {
-    using L = Lay<kPair>;
+    using L = Lay<kPair, kBN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem + L::A;
@@ -754,14 +837,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ctl->empty[s], 1);
             mbar_init(&ctl->peer_full[s], 1);
         }
-        mbar_init(&ctl->acc_full, 1);
-        mbar_init(&ctl->acc_empty, kEpiThreads);
+        for (int b = 0; b < L::kAccBufs; ++b) {
+            mbar_init(&ctl->acc_full[b], 1);
+            mbar_init(&ctl->acc_empty[b], kEpiThreads);
+        }
         mbar_init(&ctl->acc_empty_peer, 1);
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
         for (int i = 0; i < kProducers; ++i) ctl->issued[i] = 0;
         ctl->consumed = 0;
-        ctl->copy_go = 0;
 #ifdef MXA2A_TRACE
         s_trace_n = 0;
 #endif
@@ -786,25 +870,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kPair) cluster_sync();   // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
+    if (p.sfb_inline) {
+        // every CTA packs its slice of the B scales; the producers wait for all
+        // of them before their first load (the CTAs are co-resident)
+        pack_sfb_slice(p);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            red_release_add_u64(p.flags + FlagLayout::sfb_done(p.bn, p.R), 1ull);
+        }
+    }
 
     if (warp == kWarpTma || warp == kWarpTma1) {
         if (lane == 0 && !p.exchange_only)
-            producer_role<kPair>(p, &tmap_a, &tmap_b, sA, sB, sSfa, sSfb, ctl, kFused, rank,
+            producer_role<kPair, kBN>(p, &tmap_a, &tmap_b, sA, sB, sSfa, sSfb, ctl, kFused, rank,
                                  warp == kWarpTma ? 0 : 1);
     } else if (warp == kWarpMma) {
         if (lane == 0 && !p.exchange_only) {
             if (rank == 0)
-                mma_role<kPair>(p, tmem, sA, sB, sSfa, sSfb, ctl, kFused);
+                mma_role<kPair, kBN>(p, tmem, sA, sB, sSfa, sSfb, ctl, kFused);
             else
                 forwarder_role(p, ctl);
         }
     } else if (warp < kWarpCopy0) {
         if (!p.exchange_only) {
-            epilogue_role<kPair>(p, tmem, ctl, warp, lane, rank, &tmap_c, smem + L::Epi);
+            epilogue_role<kPair, kBN>(p, tmem, ctl, warp, lane, rank, &tmap_c, smem + L::Epi);
             if (lane == 0) bulk_wait_all();   // this warp's C stores are complete before the CTA ends
         }
-    } else if (kFused && warp < kWarpCopy0 + kCopyThreads / 32) {
-        copy_role(p, ctl, threadIdx.x - kWarpCopy0 * 32);
+    } else if (kFused && warp < kWarpCopy0 + kCopyWarps) {
+        copy_role(p, ctl, lane);
     }
     __syncwarp();
     __syncthreads();
@@ -837,9 +931,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
             tmem_dealloc(tmem, kTmemCols);
     }
-    if ((kFused || p.S > 1) && threadIdx.x == 0) {
-        // The last CTA to finish zeroes the staging credits for the next launch,
-        // and, if this launch gave up somewhere, the split-K tile counters.
+    if ((kFused || p.S > 1 || p.sfb_inline) && threadIdx.x == 0) {
+        // The last CTA to finish zeroes the staging credits and the scale-pack
+        // count for the next launch, and, if this launch gave up somewhere, the
+        // split-K tile counters.
         __threadfence();
         unsigned long long* done = p.flags + FlagLayout::cta_done(p.bn, p.R);
         const unsigned long long prev = atomicAdd(done, 1ull);
@@ -855,6 +950,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            if (p.sfb_inline) atomicExch(p.flags + FlagLayout::sfb_done(p.bn, p.R), 0ull);
             if (p.S > 1 && launch_failed(p))
                 for (int t = 0; t < p.Mt * p.Nt; ++t) atomicExch(&p.tile_cnt[t], 0u);
             atomicExch(done, 0ull);
@@ -864,29 +960,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 namespace {
-template <bool kFused, bool kPair>
+template <bool kFused, bool kPair, int kBN>
 cudaError_t prepare(int dev) {
     // the large dynamic shared memory opt-in is per device and per kernel
     static bool done[64] = {};
     if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&mxgemm_kernel<kFused, kPair>),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay<kPair>::Total);
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&mxgemm_kernel<kFused, kPair, kBN>),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay<kPair, kBN>::Total);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
     return e;
 }
 
-template <bool kFused, bool kPair>
+template <bool kFused, bool kPair, int kBN>
 cudaError_t launch_one(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                       const CUtensorMap& tmap_c, int grid,
-                       cudaStream_t stream) {
+                       const CUtensorMap& tmap_c, int grid, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if ((e = prepare<kFused, kPair>(dev)) != cudaSuccess) return e;
+    if ((e = prepare<kFused, kPair, kBN>(dev)) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Lay<kPair>::Total;
+    cfg.dynamicSmemBytes = Lay<kPair, kBN>::Total;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     if (kPair) {
@@ -897,27 +992,29 @@ cudaError_t launch_one(const GemmParams& p, const CUtensorMap& tmap_a, const CUt
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
     } else {
-        // The fused kernel's CTAs wait on each other's credits: they must all be
-        // resident at once, which a cooperative launch guarantees (or refuses).
+        // The fused kernel's CTAs wait on each other's credits, and with the
+        // scale pack in the prologue every producer waits for every CTA: they
+        // must all be resident at once, which a cooperative launch guarantees
+        // (or refuses).
         attr[0].id = cudaLaunchAttributeCooperative;
         attr[0].val.cooperative = 1;
     }
     cfg.attrs = attr;
-    cfg.numAttrs = (kPair || kFused) ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, &mxgemm_kernel<kFused, kPair>, p, tmap_a, tmap_b, tmap_c);
+    cfg.numAttrs = (kPair || kFused || p.sfb_inline) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, &mxgemm_kernel<kFused, kPair, kBN>, p, tmap_a, tmap_b, tmap_c);
 }
 
 template <bool kFused>
 int max_pairs_impl() {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || prepare<kFused, true>(dev) != cudaSuccess) {
+    if (cudaGetDevice(&dev) != cudaSuccess || prepare<kFused, true, BN>(dev) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Lay<true>::Total;
+    cfg.dynamicSmemBytes = Lay<true, BN>::Total;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -926,7 +1023,7 @@ int max_pairs_impl() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(&mxgemm_kernel<kFused, true>), &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(&mxgemm_kernel<kFused, true, BN>), &cfg) !=
         cudaSuccess) {
         cudaGetLastError();
         return 0;
@@ -955,11 +1052,17 @@ int mxgemm_max_pairs(bool fused) { return fused ? max_pairs_impl<true>() : max_p
 cudaError_t launch_mxgemm(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                           const CUtensorMap& tmap_c, int grid, bool fused, cudaStream_t stream) {
     if (p.pair) {
-        if (fused) return launch_one<true, true>(p, tmap_a, tmap_b, tmap_c, grid, stream);
-        return launch_one<false, true>(p, tmap_a, tmap_b, tmap_c, grid, stream);
+        if (p.tile_n != BN) return cudaErrorInvalidValue;
+        if (fused) return launch_one<true, true, BN>(p, tmap_a, tmap_b, tmap_c, grid, stream);
+        return launch_one<false, true, BN>(p, tmap_a, tmap_b, tmap_c, grid, stream);
     }
-    if (fused) return launch_one<true, false>(p, tmap_a, tmap_b, tmap_c, grid, stream);
-    return launch_one<false, false>(p, tmap_a, tmap_b, tmap_c, grid, stream);
+    if (p.tile_n == BN_NARROW) {
+        if (fused) return launch_one<true, false, BN_NARROW>(p, tmap_a, tmap_b, tmap_c, grid, stream);
+        return launch_one<false, false, BN_NARROW>(p, tmap_a, tmap_b, tmap_c, grid, stream);
+    }
+    if (p.tile_n != BN) return cudaErrorInvalidValue;
+    if (fused) return launch_one<true, false, BN>(p, tmap_a, tmap_b, tmap_c, grid, stream);
+    return launch_one<false, false, BN>(p, tmap_a, tmap_b, tmap_c, grid, stream);
 }
 
 }  // namespace mxa2a

@@ -168,6 +168,7 @@ extern "C" int mxa2a_run_noalloc(int R, int64_t M, int64_t kPerRank, int64_t N, 
     g.steps = (int)(M / commMSize);
     g.Mt = (int)((M + BM - 1) / BM);
     g.Nt = (int)((N + BN - 1) / BN);
+    g.tile_n = BN;   // the wide tile: one accumulator, 4 pipeline stages
     g.S = 1;
     g.W = g.Mt * g.Nt;
     g.kb_per_seg = (int)(kPerRank / BK);

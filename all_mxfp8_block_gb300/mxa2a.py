@@ -38,6 +38,7 @@ MXA2A_OPT_GRID = 8
 MXA2A_OPT_CHUNK_BYTES = 9
 MXA2A_OPT_CTA_PAIR = 10
 MXA2A_OPT_GROUP_M = 11
+MXA2A_OPT_TILE_N = 13
 MXA2A_INFO_STEPS = 100
 MXA2A_INFO_MTILES = 101
 MXA2A_INFO_NTILES = 102
@@ -55,6 +56,8 @@ MXA2A_INFO_CTA_PAIR = 113
 MXA2A_INFO_CTA_PAIR_UNFUSED = 114
 MXA2A_INFO_GROUP_FUSED = 115
 MXA2A_INFO_GROUP_UNFUSED = 116
+MXA2A_INFO_TILE_N_FUSED = 117
+MXA2A_INFO_TILE_N_UNFUSED = 118
 
 MXA2A_WS_RING = 1
 MXA2A_WS_SFA = 2

@@ -159,6 +159,9 @@ enum mxa2a_option {
     MXA2A_OPT_GROUP_M = 11,        /* largest raster group of the unfused path, in m rows
                                       (128-row tiles, or tile pairs), default 16; the fused path
                                       always consumes the staging steps one m row at a time */
+    MXA2A_OPT_TILE_N = 13,         /* GEMM tile width: 0 (default: 256) or 128 / 256.  128 doubles the
+                                      tiles for the rows in flight and overlaps each tile's epilogue
+                                      with the next tile (two TMEM accumulators) */
     /* read-only plan facts (mxa2a_get_option only) */
     MXA2A_INFO_STEPS = 100,        /* M / commMSize */
     MXA2A_INFO_MTILES = 101,
@@ -176,7 +179,9 @@ enum mxa2a_option {
     MXA2A_INFO_CTA_PAIR = 113,     /* 1 if the fused path runs the CTA-pair kernel */
     MXA2A_INFO_CTA_PAIR_UNFUSED = 114, /* 1 if the unfused path runs the CTA-pair kernel */
     MXA2A_INFO_GROUP_FUSED = 115,  /* raster group of the fused path (m rows) */
-    MXA2A_INFO_GROUP_UNFUSED = 116 /* raster group of the unfused path (m rows) */
+    MXA2A_INFO_GROUP_UNFUSED = 116, /* raster group of the unfused path (m rows) */
+    MXA2A_INFO_TILE_N_FUSED = 117,  /* tile width of the fused path (128 or 256) */
+    MXA2A_INFO_TILE_N_UNFUSED = 118 /* tile width of the unfused path (128 or 256) */
 };
 
 int mxa2a_set_option(mxa2a_plan *plan, int key, int64_t value);

@@ -145,6 +145,40 @@ def test_small_shapes(case):
     assert np.array_equal(got_f, got_u), "fused and unfused differ"
 
 
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_narrow_tiles_match_wide(case):
+    """The 128-column tile (two TMEM accumulators, items alternating between
+    them) against the oracle and, bit for bit, against the 256-column tile: an
+    output element sees the same MMAs in the same K order either way."""
+    name, R, M, ka, N, cm, bn = case
+    w = inputs.Workload(name, R, M, ka, N, cm, bn, 11)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    ref = gu.oracle_full(x)
+    outs = {}
+    for tile in (128, 256):
+        # grid 2: each CTA runs several items, so both accumulators are reused
+        with _plan(w, tile_n=tile, split_k=1, grid=2) as p:
+            assert p.get_option(mxa2a.MXA2A_INFO_TILE_N_FUSED) == tile
+            assert p.get_option(mxa2a.MXA2A_INFO_TILE_N_UNFUSED) == tile
+            for fused in (True, False):
+                outs[(tile, fused)] = gu.host_bits(gu.run_gpu(p, d, M, N, fused=fused))
+                torch.cuda.synchronize()
+                _status_ok(p)
+    gu.assert_parity(outs[(128, True)], ref, f"{name} narrow fused")
+    gu.assert_parity(outs[(128, False)], ref, f"{name} narrow unfused")
+    for fused in (True, False):
+        assert np.array_equal(outs[(128, fused)], outs[(256, fused)]), f"narrow != wide, fused={fused}"
+
+
+@pytest.mark.parametrize("split", [2, 3])
+def test_narrow_tiles_split_k(split):
+    w = inputs.Workload("nsplit", 6, 256, 256, 640, 128, 2, 71)
+    got_f, _ = _check_full(w, fused=True, split_k=split, tile_n=128)
+    got_u, _ = _check_full(w, fused=False, split_k=split, tile_n=128)
+    assert np.array_equal(got_f, got_u)
+
+
 @pytest.mark.parametrize("split", [2, 3, 6])
 def test_forced_split_k(split):
     w = inputs.Workload("split", 6, 256, 256, 512, 128, 2, 13)
