@@ -345,6 +345,11 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
     int launches = 0;
     GemmParams g;
     fill_params(p, g, A_seg, A_sf, C, fused);
+    // Split partials are tagged with this run's launch index, which a graph
+    // replays unchanged: a split plan must not be captured.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return MXA2A_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone && g.S > 1) return MXA2A_ERR_CAPTURE_SPLIT;
     // The B scale pack runs in the GEMM kernel's prologue (a cooperative
     // launch); the CTA-pair kernel (a cluster launch) keeps the separate kernel.
     g.B_scale = static_cast<const uint8_t*>(B_sf);
@@ -748,6 +753,7 @@ const char* mxa2a_strerror(int code) {
         case MXA2A_ERR_DEVICE_CHECK: return "device consistency check failed";
         case MXA2A_ERR_WRONG_DEVICE: return "current device differs from the plan's device";
         case MXA2A_ERR_SCRATCH_TOO_SMALL: return "problem needs more scratch than the allocation-free entry point holds";
+        case MXA2A_ERR_CAPTURE_SPLIT: return "a K-split run cannot be captured into a CUDA graph";
         default: return "unknown error";
     }
 }

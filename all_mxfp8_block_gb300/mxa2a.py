@@ -26,6 +26,7 @@ MXA2A_ERR_INVALID_OPTION = 7
 MXA2A_ERR_DEVICE_CHECK = 8
 MXA2A_ERR_WRONG_DEVICE = 9
 MXA2A_ERR_SCRATCH_TOO_SMALL = 10
+MXA2A_ERR_CAPTURE_SPLIT = 11
 
 MXA2A_OPT_TIMEOUT_NS = 1
 MXA2A_OPT_SPLIT_K = 2

@@ -222,6 +222,55 @@ def run_reference(args, w):
 
 
 # ----------------------------------------------------------------------------- GPU arm
+def time_tiny_graph(dev, runs: int = 200):
+    """The smallest workload is launch-latency bound: time it back to back as
+    eager library calls and as replays of one CUDA graph holding the call (no
+    L2 flush; CUDA events around all runs), after checking the replay
+    reproduces the eager bits."""
+    import torch
+    from all_mxfp8_block_gb300 import inputs, mxa2a
+    w0 = inputs.workload(0)
+    x0 = inputs.make_inputs(w0)
+    dA = [a.to(dev) for a in x0["A_seg"]]
+    dS = [s.to(dev) for s in x0["A_scale_seg"]]
+    dB, dBs = x0["B"].to(dev), x0["B_scale"].to(dev)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    C = torch.empty((w0.M, w0.N), dtype=torch.int16, device=dev)
+    with mxa2a.Plan(w0.R, w0.M, w0.kPerRank, w0.N, w0.commMSize, w0.buffer_num) as plan:
+        plan.set_option(mxa2a.MXA2A_OPT_SPLIT_K, 1)
+        out = {"workload": w0.name, "runs": runs, "splits": 1,
+               "timer": "CUDA events around the runs, back to back, no L2 flush"}
+        with torch.cuda.stream(side):
+            for _ in range(10):
+                plan.run(dA, dS, dB, dBs, C, side)
+            side.synchronize()
+            eager_bits = C.clone()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(side)
+            for _ in range(runs):
+                plan.run(dA, dS, dB, dBs, C, side)
+            e1.record(side)
+            side.synchronize()
+            out["eager_us_per_run"] = e0.elapsed_time(e1) * 1e3 / runs
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            plan.run(dA, dS, dB, dBs, C, side)
+        C.zero_()
+        g.replay()
+        torch.cuda.synchronize(dev)
+        out["replay_matches_eager"] = bool(torch.equal(C, eager_bits))
+        with torch.cuda.stream(side):
+            e0.record(side)
+            for _ in range(runs):
+                g.replay()
+            e1.record(side)
+            side.synchronize()
+        out["graph_us_per_run"] = e0.elapsed_time(e1) * 1e3 / runs
+        out["tflops_graph"] = 2.0 * w0.M * w0.N * w0.K / (out["graph_us_per_run"] * 1e-6) / 1e12
+    return out
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -325,6 +374,14 @@ def run_ours(args, w):
                "timer": "host wall clock per step (h2d copies + run + d2h copy + stream sync)",
                "steps": e2e_steps}
 
+    # the smallest workload, latency-bound: eager calls vs CUDA-graph replay
+    tiny_graph = None
+    if rank == 0 and not args.no_graph:
+        try:
+            tiny_graph = time_tiny_graph(dev)
+        except Exception as e:   # reported, not fatal: the headline line stands on its own
+            tiny_graph = {"error": str(e).splitlines()[0][:200]}
+
     bf16_tf, hbm, peak_src = measured_peaks()
     p_fp8 = bf16_tf * FP8_OVER_BF16
     t_roof, bound = roofline_terms(w, p_fp8, hbm)
@@ -374,6 +431,7 @@ def run_ours(args, w):
         "e2e": e2e,
         "gpu_launches": int(args.steps * (1 + launches_per_run)),
         "clocks": clocks,
+        "tiny_graph": tiny_graph,
     }
     print(json.dumps(line), flush=True)
     if ws > 1:
@@ -400,6 +458,7 @@ def main(argv=None):
     ap.add_argument("--path", choices=["fused", "unfused"], default="fused")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph timing of the smallest workload")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--split", type=int, default=0, help="force the K split of both paths (0 = automatic)")
     ap.add_argument("--single-cta", action="store_true", help="never use the CTA-pair kernel")

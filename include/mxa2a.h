@@ -57,7 +57,9 @@ enum mxa2a_error {
     MXA2A_ERR_INVALID_OPTION = 7,     /* unknown option key or value out of range */
     MXA2A_ERR_DEVICE_CHECK = 8,       /* device: an internal consistency check failed */
     MXA2A_ERR_WRONG_DEVICE = 9,       /* current device differs from the plan's */
-    MXA2A_ERR_SCRATCH_TOO_SMALL = 10  /* mxa2a_run_noalloc: the problem needs more than its static scratch */
+    MXA2A_ERR_SCRATCH_TOO_SMALL = 10, /* mxa2a_run_noalloc: the problem needs more than its static scratch */
+    MXA2A_ERR_CAPTURE_SPLIT = 11      /* a run with a K split was issued while its stream is being captured
+                                         into a CUDA graph (not supported, see mxa2a_run) */
 };
 
 typedef struct mxa2a_plan mxa2a_plan;   /* opaque */
@@ -104,12 +106,19 @@ int mxa2a_last_error(void);
 /*
  * The fused path: one persistent cooperative kernel stages A_seg[r] rows
  * (commMSize per step, buffer_num-slot ring, per-segment credits) and runs
- * the block-scaled GEMM on the staged slots as they fill, plus a small kernel
- * that reorders B_scale for the MMA.  When the ring holds too few output
- * tiles to fill the GPU, K is split over segment groups and the split
- * partials are summed inside the kernel in a fixed order (deterministic).
+ * the block-scaled GEMM on the staged slots as they fill; its prologue
+ * reorders B_scale for the MMA.  When the ring holds too few output tiles to
+ * fill the GPU, K is split over segment groups and the split partials are
+ * summed inside the kernel in a fixed order (deterministic).
  * A_seg / A_scale_seg are host arrays of R device pointers.  stream is a
  * cudaStream_t (NULL = legacy default stream).  Asynchronous.
+ * CUDA graphs: a run may be captured into a graph and replayed when its K
+ * split is 1 (MXA2A_INFO_SPLITS, or MXA2A_OPT_SPLIT_K = 1); with a split the
+ * call returns MXA2A_ERR_CAPTURE_SPLIT while the stream is capturing, since
+ * the partial tiles are tagged with the run's launch index, which a replay
+ * does not change.  Replays share that index: a device time-out in one of
+ * them stays reported (mxa2a_get_status) for the later ones, and
+ * mxa2a_kernel_times does not see replays.
  */
 int mxa2a_run(mxa2a_plan *plan, const void *const *A_seg, const void *const *A_scale_seg, const void *B,
               const void *B_scale, void *C_bf16, void *stream);
@@ -119,6 +128,7 @@ int mxa2a_run(mxa2a_plan *plan, const void *const *A_seg, const void *const *A_s
  * operand (and its scales), then run the same GEMM on it.  Same arguments;
  * the same result bits as mxa2a_run when both paths use the same K split
  * (MXA2A_OPT_SPLIT_K forces one; by default each path picks its own).
+ * The CUDA-graph rules of mxa2a_run apply (MXA2A_INFO_SPLITS_UNFUSED).
  */
 int mxa2a_run_unfused(mxa2a_plan *plan, const void *const *A_seg, const void *const *A_scale_seg, const void *B,
                       const void *B_scale, void *C_bf16, void *stream);

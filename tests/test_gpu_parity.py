@@ -254,6 +254,48 @@ def test_unfused_raster_groups_same_bits():
         assert np.array_equal(outs[0], o)
 
 
+@pytest.mark.parametrize("fused", [True, False])
+def test_cuda_graph_replay_matches_eager(fused):
+    """A run captured into a CUDA graph and replayed gives the eager run's bits
+    (the flags reset themselves at the end of every launch)."""
+    w = inputs.Workload("graph", 2, 256, 256, 512, 64, 2, 83)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w, split_k=1) as p:
+        eager = gu.host_bits(gu.run_gpu(p, d, w.M, w.N, fused=fused))
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        C = torch.full((w.M, w.N), -1, dtype=torch.int16, device="cuda")
+        fn = p.run if fused else p.run_unfused
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            fn(d["A_seg"], d["A_scale_seg"], d["B"], d["B_scale"], C, side)
+        for _ in range(3):
+            C.fill_(-1)
+            g.replay()
+            torch.cuda.synchronize()
+            assert np.array_equal(gu.host_bits(C), eager)
+        _status_ok(p)
+    gu.assert_parity(eager, gu.oracle_full(x), f"graph fused={fused}")
+
+
+def test_cuda_graph_capture_refuses_split():
+    w = inputs.Workload("graphsplit", 4, 128, 256, 256, 64, 2, 89)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w, split_k=2) as p:
+        gu.run_gpu(p, d, w.M, w.N)   # eager runs are fine
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        C = torch.empty((w.M, w.N), dtype=torch.int16, device="cuda")
+        g = torch.cuda.CUDAGraph()
+        with pytest.raises(mxa2a.Mxa2aError) as e:
+            with torch.cuda.graph(g, stream=side):
+                p.run(d["A_seg"], d["A_scale_seg"], d["B"], d["B_scale"], C, side)
+        assert e.value.code == mxa2a.MXA2A_ERR_CAPTURE_SPLIT
+
+
 def test_small_grid_many_items_per_cta():
     w = inputs.Workload("grid3", 3, 512, 128, 768, 64, 2, 23)
     _check_full(w, fused=True, grid=3)
