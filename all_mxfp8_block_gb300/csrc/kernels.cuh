@@ -24,15 +24,18 @@ constexpr int kStagesNarrow = 6;   // narrow tile: 33 KiB stages
 constexpr int kStagesPair = 6;
 constexpr int kMaxStages = 6;
 constexpr int kMaxAccBufs = 2;
-constexpr int kThreads = 416;      // 13 warps, roles below
+constexpr int kThreads = 512;      // 16 warps (4 per SM sub-partition: 128 registers each), roles below
 constexpr int kWarpTma = 0;        // TMA producer 0 (one elected lane): even stages
 constexpr int kWarpMma = 1;        // TMEM allocator + MMA issuer (one elected lane)
 constexpr int kWarpEpi0 = 2;       // warps 2..9: epilogue, warp w drains TMEM lane quarter w%4,
 constexpr int kEpiWarps = 8;       //   column half (w-2)/4 of the accumulator
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kWarpCopy0 = 10;     // warps 10..11: staging copy workers, one per warp (fused kernel only)
-constexpr int kCopyWarps = 2;
+constexpr int kWarpCopy0 = 10;     // warps 10, 11, 14, 15: staging copy workers, one per warp
+constexpr int kCopyWarps = 4;      //   (fused kernel only; idle in the unfused kernel)
 constexpr int kWarpTma1 = 12;      // TMA producer 1 (one elected lane): odd stages
+// Warp 13 stays idle: it would share an SM sub-partition (warp % 4) with the
+// MMA-issuing warp 1, and a busy copy warp there slows the MMA issue.
+__host__ __device__ constexpr bool is_copy_warp(int w) { return w == 10 || w == 11 || w >= 14; }
 // One thread's TMA loads overlap poorly (about one stage per 0.4 us per
 // thread on this GPU); two issuing warps double the per-SM load rate.
 constexpr int kProducers = 2;

@@ -103,7 +103,7 @@ struct mxa2a_plan {
     int64_t timeout_ns = 2000000000LL;
     int force_split = 0, zigzag = 1, rotate = 0, record_events = 0, exchange_only = 0;
     int fault_skip_step = -1, grid_cap = 0;
-    int64_t chunk_bytes = 8192;
+    int64_t chunk_bytes = 0;            // option: staging copy chunk, 0 = automatic
     // workspace
     uint8_t* ws = nullptr;
     size_t ws_bytes = 0;
@@ -198,8 +198,16 @@ void derive(mxa2a_plan* p) {
         p->group_unfused = std::max(1, std::min(rows_u, p->group_cap));
         p->group_fused = 1;
     }
-    // staging copy chunk: the largest divisor of commMSize rows within chunk_bytes
-    int64_t want = std::max<int64_t>(1, p->chunk_bytes / p->ka);
+    // Staging copy chunk: the largest divisor of commMSize rows within the
+    // chunk size.  Automatic: about two steps' tasks for all copy workers (a
+    // drained segment is then copied by many workers at once), 4..16 KiB
+    // (smaller chunks cost more per byte, larger ones fewer copiers).
+    int64_t chunk = p->chunk_bytes;
+    if (chunk <= 0) {
+        const int64_t step_bytes = (int64_t)p->R * p->cm * p->ka;
+        chunk = std::min<int64_t>(16384, std::max<int64_t>(4096, 2 * step_bytes / ((int64_t)kCopyWarps * p->sm_count)));
+    }
+    int64_t want = std::max<int64_t>(1, chunk / p->ka);
     int rpc = 1;
     for (int64_t d = 1; d <= p->cm; ++d)
         if (p->cm % d == 0 && d <= want) rpc = (int)d;
@@ -611,7 +619,7 @@ int mxa2a_set_option(mxa2a_plan* p, int key, int64_t v) {
             p->grid_cap = (int)v;
             break;
         case MXA2A_OPT_CHUNK_BYTES:
-            if (v < 16) return MXA2A_ERR_INVALID_OPTION;
+            if (v != 0 && v < 16) return MXA2A_ERR_INVALID_OPTION;
             p->chunk_bytes = v;
             break;
         case MXA2A_OPT_CTA_PAIR:

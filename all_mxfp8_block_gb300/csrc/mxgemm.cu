@@ -10,7 +10,7 @@
 // segments and returns the slot's credit.  On one GPU the segments are R
 // separate HBM buffers and the "exchange" is this kernel's own copy role.
 //
-// CTA roles (384 threads, one CTA per SM, persistent over work items):
+// CTA roles (512 threads = 16 warps, one CTA per SM, persistent over work items):
 //   warps 0, 12  TMA producers (even / odd stages): wait for a slot's segment
 //            to be published, then stream A (from the ring, or from the packed
 //            A when unfused), B and both scale tiles into a shared-memory ring
@@ -22,12 +22,15 @@
 //            In the CTA-pair kernel the even CTA issues 256x256x32 MMAs for
 //            both CTAs (.cta_group::2) and the odd CTA's warp 1 forwards its
 //            stage-full and accumulator-empty signals to the even CTA.
-//   warps 2-9 epilogue: TMEM -> registers -> BF16 -> global, or, for split
-//            K, the in-kernel fixed-order reduction of the split partials.
-//            Warp w drains TMEM lane quarter w%4, column half (w-2)/4.
-//   warps 10-11 staging copy (fused only): copy-tasks (step, segment, chunk)
-//            in step order; wait for the slot's credit, copy the rows of
-//            A_seg[r] and their scales, publish.
+//   warps 2-9 epilogue: TMEM -> registers -> BF16 -> shared staging -> TMA
+//            store, or, for split K, the in-kernel fixed-order reduction of
+//            the split partials.  Warp w drains TMEM lane quarter w%4, column
+//            half (w-2)/4.
+//   warps 10, 11, 14, 15 staging copy (fused only): four independent workers
+//            per CTA take copy tasks (step, segment, chunk) in step order,
+//            wait for the slot's credit, copy the rows of A_seg[r] and their
+//            scales, publish.  (Warp 13 idles: it would share an SM
+//            sub-partition with the MMA issuer.)
 //
 // Credits (the pages' per-slot signals with credit return, performance guide
 // 1.1/1.3, kept per segment as its fine-grained signals suggest) are
@@ -784,14 +787,15 @@ __device__ void copy_role(const GemmParams& p, SmemCtl* ctl, int lane) {
             atom[(m & 31) * 4 + ((m & 127) >> 5)] = v;
         }
         // Publish: the warp barrier orders every lane's stores before lane 0's
-        // release (cumulative at gpu scope); readers acquire the counter and
-        // then read the ring through the async proxy (TMA).
+        // acq_rel fence (cumulative at gpu scope), which orders them before the
+        // counter adds; readers acquire the counter and then read the ring
+        // through the async proxy (TMA).
         fence_proxy_async_global();
         __syncwarp();
         if (lane == 0 && s != p.fault_skip_step) {
-            __threadfence();
-            red_release_add_u64(p.flags + FlagLayout::filled(slot, r, p.R), 1ull);
-            red_release_add_u64(p.flags + FlagLayout::staged(slot, p.bn, p.R), 1ull);
+            fence_acq_rel_gpu();
+            red_relaxed_add_u64(p.flags + FlagLayout::filled(slot, r, p.R), 1ull);
+            red_relaxed_add_u64(p.flags + FlagLayout::staged(slot, p.bn, p.R), 1ull);
             TRACE(10, t, 0);
         }
     }
@@ -897,7 +901,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             epilogue_role<kPair, kBN>(p, tmem, ctl, warp, lane, rank, &tmap_c, smem + L::Epi);
             if (lane == 0) bulk_wait_all();   // this warp's C stores are complete before the CTA ends
         }
-    } else if (kFused && warp < kWarpCopy0 + kCopyWarps) {
+    } else if (kFused && is_copy_warp(warp)) {
         copy_role(p, ctl, lane);
     }
     __syncwarp();

@@ -161,7 +161,8 @@ enum mxa2a_option {
     MXA2A_OPT_EXCHANGE_ONLY = 6,   /* 1: fused runs only stage A into the ring (needs buffer_num >= steps) */
     MXA2A_OPT_FAULT_SKIP_STEP = 7, /* test knob: never publish staging step k (-1 = off); waits then time out */
     MXA2A_OPT_GRID = 8,            /* cap on persistent CTAs (0 = one per SM) */
-    MXA2A_OPT_CHUNK_BYTES = 9,     /* target staging copy chunk (default 8192) */
+    MXA2A_OPT_CHUNK_BYTES = 9,     /* target staging copy chunk in bytes; 0 (default): automatic,
+                                      about two staging steps' tasks for all copy workers, 4..16 KiB */
     MXA2A_OPT_CTA_PAIR = 10,       /* 1: use the CTA-pair kernel (256-row tiles, one tcgen05
                                       cta_group::2 MMA stream per pair) when M/128 is even and, on the
                                       fused path, buffer_num covers the steps of a 256-row tile;
