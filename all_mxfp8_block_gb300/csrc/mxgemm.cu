@@ -253,7 +253,7 @@ __device__ bool wait_counter(const GemmParams& p, SmemCtl* ctl, const unsigned l
     uint32_t nap = 64;   // exponential back-off keeps many pollers off the counter's L2 line
     for (uint32_t n = 1;; ++n) {
         __nanosleep(nap);
-        if (nap < 1024) nap <<= 1;
+        if (nap < 256) nap <<= 1;
         v = ld_acquire_u64(ctr);
         if (v >= target) return true;
         if (ctl->abort) return false;
@@ -740,7 +740,7 @@ __device__ void copy_role(const GemmParams& p, SmemCtl* ctl, int lane) {
                 uint32_t nap = 64;   // back-off keeps the pollers off the counters' L2 lines
                 for (uint32_t n = 1; !ok; ++n) {
                     __nanosleep(nap);
-                    if (nap < 1024) nap <<= 1;
+                    if (nap < 256) nap <<= 1;
                     ok = copy_task_ready(p, t, per_step, &obs, &tgt);
                     if (ok) break;
                     if (ctl->abort) break;
