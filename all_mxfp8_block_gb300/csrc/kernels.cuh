@@ -88,6 +88,7 @@ struct GemmParams {
     int Mt, Nt, S, W;           // m-tiles, n-tiles, K splits, work items
     int pair;                   // 1: CTA-pair kernel, work items are pairs of m-tiles (Mt even)
     int tile_n;                 // BN of this launch: 256 or 128 (Nt = ceil(N / tile_n))
+    int fmt_a, fmt_b;           // element formats (MMA type codes): 0 E4M3, 1 E5M2
     int kb_per_seg;             // ka / 128
     int Mg, Ng2;                // 128-row groups of A (scale atoms), 128-col groups of B (padded to 256)
     int box_m;                  // rows per A TMA box: 128 or 64

@@ -91,6 +91,7 @@ struct mxa2a_plan {
     int tn_fused = BN, tn_unfused = BN;     // tile width per path (256, or 128 = the narrow tile)
     int Nt_fused = 0, Nt_unfused = 0;       // n-tiles per path
     int tile_opt = 0;                       // option: 0 automatic, 128 or 256 forced
+    int elem_types = 0;                     // option: element-format pair (MXA2A_OPT_ELEM_TYPES)
     int S_fused = 1, S_unfused = 1, W_fused = 0, W_unfused = 0;   // K splits and work items per path
     int pair_fused = 0, pair_unfused = 0;   // CTA-pair kernel in use, per path
     int group_fused = 1, group_unfused = 1; // raster group, in m rows (tiles or tile pairs)
@@ -264,6 +265,10 @@ void fill_params(mxa2a_plan* p, GemmParams& g, const void* const* A_seg, const v
     g.Mt = p->Mt;
     g.Nt = fused ? p->Nt_fused : p->Nt_unfused;
     g.tile_n = fused ? p->tn_fused : p->tn_unfused;
+    // the pages' four kernel entries: E4M3E4M3, E5M2E5M2, E4M3E5M2, E5M2E4M3
+    static const int kFmtA[4] = {0, 1, 0, 1}, kFmtB[4] = {0, 1, 1, 0};
+    g.fmt_a = kFmtA[p->elem_types];
+    g.fmt_b = kFmtB[p->elem_types];
     g.S = fused ? p->S_fused : p->S_unfused;
     g.W = fused ? p->W_fused : p->W_unfused;
     g.pair = fused ? p->pair_fused : p->pair_unfused;
@@ -634,6 +639,10 @@ int mxa2a_set_option(mxa2a_plan* p, int key, int64_t v) {
             if (v != 0 && v != BN_NARROW && v != BN) return MXA2A_ERR_INVALID_OPTION;
             p->tile_opt = (int)v;
             break;
+        case MXA2A_OPT_ELEM_TYPES:
+            if (v < 0 || v > 3) return MXA2A_ERR_INVALID_OPTION;
+            p->elem_types = (int)v;
+            break;
         default:
             return MXA2A_ERR_INVALID_OPTION;
     }
@@ -656,6 +665,7 @@ int mxa2a_get_option(mxa2a_plan* p, int key, int64_t* v) {
         case MXA2A_OPT_CTA_PAIR: *v = p->allow_pair; break;
         case MXA2A_OPT_GROUP_M: *v = p->group_cap; break;
         case MXA2A_OPT_TILE_N: *v = p->tile_opt; break;
+        case MXA2A_OPT_ELEM_TYPES: *v = p->elem_types; break;
         case MXA2A_INFO_GROUP_FUSED: *v = p->group_fused; break;
         case MXA2A_INFO_GROUP_UNFUSED: *v = p->group_unfused; break;
         case MXA2A_INFO_CTA_PAIR: *v = p->pair_fused; break;

@@ -388,13 +388,14 @@ template <bool kPair, int kBN>
 __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_t* sB, uint8_t* sSfa,
                          uint8_t* sSfb, SmemCtl* ctl, bool fused) {
     using L = Lay<kPair, kBN>;
-    // Instruction descriptor, kind::mxf8f6f4 with block scaling: A/B E4M3 (0),
-    // both K-major, N>>3 at [17,23), scale type UE8M0 at bit 23, M>>4 at
-    // [24,29) (M = 256 for a CTA pair); B/A scale-factor byte ids at [4,6) and
-    // [29,31) select which of the four 32-wide K blocks held in each 32-bit
-    // TMEM scale column is used.
+    // Instruction descriptor, kind::mxf8f6f4 with block scaling: A / B element
+    // types at [7,10) / [10,13) (E4M3 0, E5M2 1), both K-major, N>>3 at
+    // [17,23), scale type UE8M0 at bit 23, M>>4 at [24,29) (M = 256 for a CTA
+    // pair); B/A scale-factor byte ids at [4,6) and [29,31) select which of the
+    // four 32-wide K blocks held in each 32-bit TMEM scale column is used.
     constexpr uint32_t kM = kPair ? 2 * BM : BM;
-    const uint32_t idesc_base = ((uint32_t)(kBN >> 3) << 17) | (1u << 23) | ((kM >> 4) << 24);
+    const uint32_t idesc_base = ((uint32_t)p.fmt_a << 7) | ((uint32_t)p.fmt_b << 10) |
+                                ((uint32_t)(kBN >> 3) << 17) | (1u << 23) | ((kM >> 4) << 24);
     int it = 0;
     int n = 0;   // items done; item n accumulates in buffer n % kAccBufs
     for (int w = first_item<kPair>(); w < p.W; w += item_stride<kPair>(), ++n) {

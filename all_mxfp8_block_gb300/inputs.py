@@ -31,6 +31,11 @@ import torch
 MX_BLOCK = 32          # elements per E8M0 scale along K
 E4M3_EMAX = 8          # exponent of the largest E4M3 binade (448 = 1.75 * 2^8)
 E4M3_MAX = 448.0
+E5M2_EMAX = 15         # exponent of the largest E5M2 binade (57344 = 1.75 * 2^15)
+E5M2_MAX = 57344.0
+# element formats: (largest binade exponent, largest value, torch dtype)
+FORMATS = {"e4m3": (E4M3_EMAX, E4M3_MAX, torch.float8_e4m3fn),
+           "e5m2": (E5M2_EMAX, E5M2_MAX, torch.float8_e5m2)}
 
 
 @dataclass(frozen=True)
@@ -46,6 +51,8 @@ class Workload:
     seed: int
     outliers: bool = False   # 1% x100 rows and 2^-6..2^6 per-block spread on A
     note: str = field(default="", compare=False)
+    a_fmt: str = "e4m3"      # element format of A ("e4m3" or "e5m2")
+    b_fmt: str = "e4m3"      # element format of B
 
     @property
     def K(self) -> int:
@@ -87,23 +94,26 @@ def workload(name_or_index) -> Workload:
     return WORKLOADS_BY_NAME[name_or_index]
 
 
-def quantize_mx_rows(x: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
-    """Quantise fp32 ``[rows][K]`` (K % 32 == 0) to (E4M3 codes, E8M0 bytes).
+def quantize_mx_rows(x: torch.Tensor, fmt: str = "e4m3") -> tuple[torch.Tensor, torch.Tensor]:
+    """Quantise fp32 ``[rows][K]`` (K % 32 == 0) to (element codes, E8M0 bytes),
+    OCP MX: per 32-block X = floor(log2 amax) - emax of the element format,
+    elements = round-to-nearest-even of clamp(v / 2^X, +-max).
 
     Returns ``codes`` uint8 ``[rows][K]`` and ``scales`` uint8 ``[rows][K/32]``.
     """
+    emax, vmax, dtype = FORMATS[fmt]
     assert x.dtype == torch.float32 and x.dim() == 2 and x.shape[1] % MX_BLOCK == 0
     rows, K = x.shape
     blocks = x.reshape(rows, K // MX_BLOCK, MX_BLOCK)
     amax = blocks.abs().amax(dim=2)
     # frexp: amax = mant * 2^e with mant in [0.5, 1)  =>  floor(log2 amax) = e - 1
     _, e = torch.frexp(amax)
-    X = (e.to(torch.int32) - 1) - E4M3_EMAX
+    X = (e.to(torch.int32) - 1) - emax
     X = torch.where(amax > 0, X, torch.full_like(X, -127))
     X = X.clamp(-127, 127)
     scaled = torch.ldexp(blocks, (-X).to(torch.float32).unsqueeze(2))
-    scaled = scaled.clamp(-E4M3_MAX, E4M3_MAX)
-    codes = scaled.to(torch.float8_e4m3fn).view(torch.uint8).reshape(rows, K)
+    scaled = scaled.clamp(-vmax, vmax)
+    codes = scaled.to(dtype).view(torch.uint8).reshape(rows, K)
     scales = (X + 127).to(torch.uint8)
     return codes.contiguous(), scales.contiguous()
 
@@ -132,10 +142,10 @@ def make_inputs(w: Workload) -> dict:
     B = torch.randn(w.K, w.N, generator=g, dtype=torch.float32) / math.sqrt(w.K)
     A_seg, A_sf = [], []
     for a in A:
-        c, s = quantize_mx_rows(a.contiguous())
+        c, s = quantize_mx_rows(a.contiguous(), w.a_fmt)
         A_seg.append(c)
         A_sf.append(s)
-    B_codes, B_sf = quantize_mx_rows(B.t().contiguous())
+    B_codes, B_sf = quantize_mx_rows(B.t().contiguous(), w.b_fmt)
     return {"A_seg": A_seg, "A_scale_seg": A_sf, "B": B_codes, "B_scale": B_sf,
             "workload": w}
 

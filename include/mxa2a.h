@@ -173,6 +173,10 @@ enum mxa2a_option {
     MXA2A_OPT_TILE_N = 13,         /* GEMM tile width: 0 (default: 256) or 128 / 256.  128 doubles the
                                       tiles for the rows in flight and overlaps each tile's epilogue
                                       with the next tile (two TMEM accumulators) */
+    MXA2A_OPT_ELEM_TYPES = 14,     /* element formats of A and B, the four kernel entries of the
+                                      all_to_all_matmul kernel (all_to_all_matmul_impl.h):
+                                      0 (default) E4M3 x E4M3, 1 E5M2 x E5M2, 2 E4M3 x E5M2,
+                                      3 E5M2 x E4M3.  Scales stay E8M0, one per 32 along K */
     /* read-only plan facts (mxa2a_get_option only) */
     MXA2A_INFO_STEPS = 100,        /* M / commMSize */
     MXA2A_INFO_MTILES = 101,

@@ -54,6 +54,15 @@ def _load():
                 ctypes.c_void_p, ctypes.c_void_p,
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_int]
+            lib.mxa2a_oracle_gemm_fmt.restype = ctypes.c_int
+            lib.mxa2a_oracle_gemm_fmt.argtypes = [
+                ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p),
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_int]
+            lib.mxa2a_oracle_decode_e5m2.restype = ctypes.c_double
+            lib.mxa2a_oracle_decode_e5m2.argtypes = [ctypes.c_uint8]
             lib.mxa2a_oracle_decode_e4m3.restype = ctypes.c_double
             lib.mxa2a_oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
             lib.mxa2a_oracle_decode_e8m0.restype = ctypes.c_double
@@ -77,6 +86,11 @@ def decode_e4m3(code: int) -> float:
     return _load().mxa2a_oracle_decode_e4m3(code)
 
 
+def decode_e5m2(code: int) -> float:
+    """Value of one E5M2 code; +-inf for 0x7C / 0xFC, NaN for the other exponent-31 codes."""
+    return _load().mxa2a_oracle_decode_e5m2(code)
+
+
 def decode_e8m0(code: int) -> float:
     """Value 2^(code-127) of one E8M0 scale byte; NaN for 0xFF."""
     return _load().mxa2a_oracle_decode_e8m0(code)
@@ -89,12 +103,18 @@ def round_bf16(negative: bool, digits: list[int], exp0: int) -> int:
     return int(_load().mxa2a_oracle_round_bf16(int(negative), arr, len(digits), exp0))
 
 
-def gemm(A_seg, A_scale_seg, B, B_scale, rows=None, cols=None, nthreads: int = 0) -> np.ndarray:
+FORMATS = {"e4m3": 0, "e5m2": 1}
+
+
+def gemm(A_seg, A_scale_seg, B, B_scale, rows=None, cols=None, nthreads: int = 0,
+         a_fmt: str = "e4m3", b_fmt: str = "e4m3") -> np.ndarray:
     """Exact ``C = bf16(concat_r(A_r * sA_r) @ (B * sB)^T)`` as uint16 BF16 bits.
 
     ``A_seg[r]`` uint8 [M][ka], ``A_scale_seg[r]`` uint8 [M][ka/32],
     ``B`` uint8 [N][R*ka] (B stored transposed), ``B_scale`` uint8 [N][R*ka/32].
     ``rows`` / ``cols`` select a sub-block of C (default: all of it).
+    ``a_fmt`` / ``b_fmt``: element format of A / B codes, "e4m3" or "e5m2"
+    (the kernel entries E4M3E4M3, E5M2E5M2, E4M3E5M2, E5M2E4M3).
     """
     lib = _load()
     A = [_np_u8(a) for a in A_seg]
@@ -113,8 +133,8 @@ def gemm(A_seg, A_scale_seg, B, B_scale, rows=None, cols=None, nthreads: int = 0
     out = np.zeros((nr, nc), dtype=np.uint16)
     a_ptrs = (ctypes.c_void_p * R)(*[a.ctypes.data for a in A])
     s_ptrs = (ctypes.c_void_p * R)(*[s.ctypes.data for s in S])
-    rc = lib.mxa2a_oracle_gemm(
-        R, M, ka, N, a_ptrs, s_ptrs, Bn.ctypes.data, Bs.ctypes.data,
+    rc = lib.mxa2a_oracle_gemm_fmt(
+        R, M, ka, N, a_ptrs, s_ptrs, Bn.ctypes.data, Bs.ctypes.data, FORMATS[a_fmt], FORMATS[b_fmt],
         None if r_arr is None else r_arr.ctypes.data, nr,
         None if c_arr is None else c_arr.ctypes.data, nc,
         out.ctypes.data, int(nthreads))

@@ -25,6 +25,16 @@ def e4m3_values(codes) -> np.ndarray:
     return t.view(torch.float8_e4m3fn).to(torch.float64).numpy()
 
 
+def e5m2_values(codes) -> np.ndarray:
+    """float64 values of E5M2 code bytes via torch.float8_e5m2 (exact; +-inf and NaN kept)."""
+    t = torch.as_tensor(np.ascontiguousarray(np.asarray(codes, dtype=np.uint8)))
+    return t.view(torch.float8_e5m2).to(torch.float64).numpy()
+
+
+def values_of(codes, fmt: str) -> np.ndarray:
+    return e5m2_values(codes) if fmt == "e5m2" else e4m3_values(codes)
+
+
 def e8m0_values(codes) -> np.ndarray:
     """float64 values 2^(c-127) of E8M0 bytes via torch.float8_e8m0fnu (exact)."""
     t = torch.as_tensor(np.ascontiguousarray(np.asarray(codes, dtype=np.uint8)))
@@ -86,14 +96,14 @@ def round_f64_to_bf16(x: np.ndarray) -> np.ndarray:
     return out.astype(np.uint16)
 
 
-def exact_gemm_fraction(A_seg, A_sf, B, B_sf) -> np.ndarray:
-    """Brute-force exact C (BF16 bits) with rational arithmetic; tiny shapes only."""
+def exact_gemm_fraction(A_seg, A_sf, B, B_sf, a_fmt: str = "e4m3", b_fmt: str = "e4m3") -> np.ndarray:
+    """Brute-force exact C (BF16 bits) with rational arithmetic; tiny shapes, finite codes only."""
     R = len(A_seg)
     M, ka = np.asarray(A_seg[0]).shape
     N, K = np.asarray(B).shape
-    av = np.concatenate([e4m3_values(a) for a in A_seg], axis=1)          # [M][K]
+    av = np.concatenate([values_of(a, a_fmt) for a in A_seg], axis=1)     # [M][K]
     asf = np.concatenate([np.asarray(s, dtype=np.uint8) for s in A_sf], axis=1)
-    bv = e4m3_values(B)
+    bv = values_of(B, b_fmt)
     bsf = np.asarray(B_sf, dtype=np.uint8)
     out = np.zeros((M, N), dtype=np.uint16)
     two = Fraction(2)

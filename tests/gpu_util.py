@@ -74,7 +74,9 @@ def assert_parity(gpu_bits, ref_bits, label=""):
 
 
 def oracle_full(x: dict) -> np.ndarray:
-    return oracle.gemm(x["A_seg"], x["A_scale_seg"], x["B"], x["B_scale"])
+    w = x.get("workload")
+    fmts = {"a_fmt": w.a_fmt, "b_fmt": w.b_fmt} if w is not None else {}
+    return oracle.gemm(x["A_seg"], x["A_scale_seg"], x["B"], x["B_scale"], **fmts)
 
 
 def sample_rows(M: int, n: int, seed: int) -> np.ndarray:

@@ -82,6 +82,57 @@ def test_identity_B_reproduces_A(fused, M):
     assert np.array_equal(gv, rv), f"{np.sum(gv != rv)} of {gv.size} differ"
 
 
+ELEM_PAIRS = [("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3")]
+
+
+def _finite(codes: torch.Tensor, fmt: str) -> torch.Tensor:
+    """Replace NaN / infinity codes of a format with small finite ones."""
+    c = codes.clone()
+    if fmt == "e5m2":
+        bad = ((c >> 2) & 0x1F) == 31
+        c[bad] = c[bad] & 0x83
+    else:
+        bad = (c & 0x7F) == 0x7F
+        c[bad] = c[bad] & 0xF8
+    return c
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("a_fmt,b_fmt", [("e4m3", "e5m2"), ("e5m2", "e4m3"), ("e5m2", "e5m2")])
+def test_identity_B_other_element_formats(a_fmt, b_fmt, fused):
+    """The element-type fields of the MMA: with B = I in its own format
+    (1.0 = 0x3C in E5M2, 0x38 in E4M3) C equals A, read in A's format, exactly."""
+    R, ka, M = 2, 128, 128
+    K = N = R * ka
+    w = inputs.Workload("identity_fmt", R, M, ka, N, 64, 2, 0, a_fmt=a_fmt, b_fmt=b_fmt)
+    A = _finite(inputs.random_codes((M, K), 111), a_fmt)
+    sA = inputs.random_scales((M, K // 32), 112, 117, 137)
+    B = torch.zeros((N, K), dtype=torch.uint8)
+    B[torch.arange(N), torch.arange(K)] = 0x3C if b_fmt == "e5m2" else 0x38
+    sB = torch.full((N, K // 32), 127, dtype=torch.uint8)
+    x = {"A_seg": [A[:, r * ka:(r + 1) * ka].contiguous() for r in range(R)],
+         "A_scale_seg": [sA[:, r * ka // 32:(r + 1) * ka // 32].contiguous() for r in range(R)],
+         "B": B, "B_scale": sB, "workload": w}
+    d = gu.to_device(x)
+    with _plan(w, elem_types=mxa2a.ELEM_TYPES[(a_fmt, b_fmt)]) as p:
+        C = gu.run_gpu(p, d, M, N, fused=fused)
+        torch.cuda.synchronize()
+        _status_ok(p)
+        got = gu.host_bits(C)
+    ref = gu.oracle_full(x)
+    gv, rv = gu.bits_to_f64(got), gu.bits_to_f64(ref)
+    assert np.array_equal(gv, rv), f"{np.sum(gv != rv)} of {gv.size} differ"
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("a_fmt,b_fmt", ELEM_PAIRS)
+def test_other_element_formats_against_oracle(a_fmt, b_fmt, fused):
+    """Quantised N(0,1) inputs in the other element formats, several tiles and
+    a ragged N tail, against the oracle element by element."""
+    w = inputs.Workload("fmt", 3, 384, 256, 528, 128, 2, 97, a_fmt=a_fmt, b_fmt=b_fmt)
+    _check_full(w, fused=fused, elem_types=mxa2a.ELEM_TYPES[(a_fmt, b_fmt)])
+
+
 @pytest.mark.parametrize("M", [128, 256])
 def test_scale_factors_per_block_and_column(M):
     """One-hot B with varied B scales per 32-block and column: exercises every

@@ -63,6 +63,82 @@ def test_e8m0_decode_exhaustive_vs_torch():
 
 # --- the single rounding step, against a search over the BF16 grid --------------------
 
+def test_e5m2_decode_exhaustive_vs_torch():
+    """All 256 E5M2 codes against torch.float8_e5m2 (infinities and NaNs included)."""
+    codes = np.arange(256, dtype=np.uint8)
+    want = _exact.e5m2_values(codes)
+    got = np.array([oracle.decode_e5m2(int(c)) for c in codes])
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+    assert got[0x7C] == np.inf and got[0xFC] == -np.inf and got[0x7B] == 57344.0
+
+
+def _finite_codes(shape, seed, fmt):
+    """Random codes of one element format without NaN / infinity codes."""
+    c = inputs.random_codes(shape, seed).numpy()
+    if fmt == "e5m2":
+        special = ((c >> 2) & 0x1F) == 31
+        c = np.where(special, c & 0x83, c)     # exponent 31 -> 0: a subnormal of the same sign
+    else:
+        c = np.where((c & 0x7F) == 0x7F, c & 0xF8, c)
+    return c.astype(np.uint8)
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", [("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3")])
+def test_bruteforce_element_formats(a_fmt, b_fmt):
+    """The other element-format pairs (the pages' E5M2E5M2, E4M3E5M2, E5M2E4M3
+    kernel entries) against exact rationals, scales spread widely."""
+    R, M, N, ka = 2, 3, 4, 64
+    K = R * ka
+    A = _finite_codes((M, K), 31, a_fmt)
+    B = _finite_codes((N, K), 32, b_fmt)
+    sA = inputs.random_scales((M, K // 32), 33, 40, 200).numpy()
+    sB = inputs.random_scales((N, K // 32), 34, 40, 200).numpy()
+    As, Ss = _split(A, sA, R, ka)
+    got = oracle.gemm(As, Ss, B, sB, a_fmt=a_fmt, b_fmt=b_fmt)
+    want = _exact.exact_gemm_fraction(As, Ss, B, sB, a_fmt=a_fmt, b_fmt=b_fmt)
+    assert np.array_equal(got, want)
+
+
+def test_e5m2_infinities_follow_ieee():
+    """E5M2 infinities: inf x finite = inf, inf x 0 = NaN, +inf + -inf = NaN,
+    checked against a float64 dot product (IEEE) of the decoded values."""
+    R, M, N, ka = 1, 5, 3, 64
+    K = R * ka
+    A = np.full((M, K), 0x3C, np.uint8)        # 1.0
+    B = np.full((N, K), 0x3C, np.uint8)
+    A[0, 0] = 0x7C                               # +inf in block 0
+    A[1, 0] = 0xFC                               # -inf
+    A[2, 0] = 0x7C; A[2, 40] = 0xFC              # +inf and -inf in different blocks
+    A[3, 5] = 0x7C
+    B[1, 5] = 0x00                               # ... times +0 in column 1
+    A[4, 7] = 0x7E                               # NaN code
+    sA = np.full((M, K // 32), 127, np.uint8)
+    sB = np.full((N, K // 32), 127, np.uint8)
+    got = oracle.gemm([A], [sA], B, sB, a_fmt="e5m2", b_fmt="e5m2")
+    with np.errstate(invalid="ignore"):
+        ref = _exact.e5m2_values(A) @ _exact.e5m2_values(B).T
+        want = np.where(np.isnan(ref), 0x7FC0, np.where(np.isinf(ref), np.where(ref > 0, 0x7F80, 0xFF80),
+                                                       _exact.round_f64_to_bf16(np.nan_to_num(ref))))
+    assert np.array_equal(got, want.astype(np.uint16)), (got, want)
+
+
+def test_mixed_formats_identity_B():
+    """E4M3 A times an E5M2 identity (1.0 = 0x3C) returns A exactly, and
+    E5M2 A times an E4M3 identity (0x38) too."""
+    M, K = 8, 64
+    for a_fmt, b_fmt, one in (("e4m3", "e5m2", 0x3C), ("e5m2", "e4m3", 0x38)):
+        A = _finite_codes((M, K), 41, a_fmt)
+        B = np.zeros((K, K), np.uint8)
+        np.fill_diagonal(B, one)
+        sA = np.full((M, K // 32), 127, np.uint8)
+        sB = np.full((K, K // 32), 127, np.uint8)
+        got = oracle.gemm([A], [sA], B, sB, a_fmt=a_fmt, b_fmt=b_fmt)
+        want = _exact.round_f64_to_bf16(_exact.values_of(A, a_fmt))
+        assert np.array_equal(got, want), (a_fmt, b_fmt)
+
+
 def test_round_bf16_random_vs_grid():
     rng = random.Random(7)
     for _ in range(3000):
@@ -292,6 +368,10 @@ MUTANTS = {
     "sign_dropped": ("else big_add_shifted(&neg, (uint64_t)(-s), shift);",
                      "else big_add_shifted(&pos, (uint64_t)(-s), shift);"),
     "subnormal_decode": ("if (e == 0) mag = m;", "if (e == 0) mag = 2 * m;"),
+    "e5m2_exponent_bias": ("else mag = (int64_t)(4 + m) << (e - 1);", "else mag = (int64_t)(4 + m) << e;"),
+    "e5m2_wide_units": ("int shift = (sa - 127) + (sb - 127) - 32 - UNIT_EXP;",
+                        "int shift = (sa - 127) + (sb - 127) - 25 - UNIT_EXP;"),
+    "mixed_units": ("shift -= j->uexp_fix;", "shift += j->uexp_fix;"),
 }
 
 
@@ -307,9 +387,11 @@ def test_planted_mistakes_are_caught(name, tmp_path):
     subprocess.check_call(["gcc", "-O1", "-std=c11", "-D_DEFAULT_SOURCE", "-shared", "-fPIC",
                            "-pthread", "-o", str(so), str(csrc)])
     lib = ctypes.CDLL(str(so))
-    lib.mxa2a_oracle_gemm.argtypes = oracle._load().mxa2a_oracle_gemm.argtypes
-    lib.mxa2a_oracle_round_bf16.argtypes = oracle._load().mxa2a_oracle_round_bf16.argtypes
-    lib.mxa2a_oracle_round_bf16.restype = ctypes.c_uint16
+    good = oracle._load()
+    for fn in ("mxa2a_oracle_gemm", "mxa2a_oracle_gemm_fmt", "mxa2a_oracle_round_bf16",
+               "mxa2a_oracle_decode_e4m3", "mxa2a_oracle_decode_e5m2", "mxa2a_oracle_decode_e8m0"):
+        getattr(lib, fn).argtypes = getattr(good, fn).argtypes
+        getattr(lib, fn).restype = getattr(good, fn).restype
 
     saved = oracle._lib
     oracle._lib = lib
@@ -320,7 +402,10 @@ def test_planted_mistakes_are_caught(name, tmp_path):
                       test_golden_handworked_fixtures,
                       test_round_bf16_ties_subnormals_overflow,
                       test_one_hot_B_selects_columns,
-                      test_unit_scales_equal_float64_matmul):
+                      test_unit_scales_equal_float64_matmul,
+                      test_e5m2_decode_exhaustive_vs_torch,
+                      lambda: test_bruteforce_element_formats("e5m2", "e5m2"),
+                      lambda: test_bruteforce_element_formats("e4m3", "e5m2")):
             try:
                 check()
             except AssertionError:
