@@ -101,6 +101,11 @@ struct GemmParams {
     // pack kernel; needs all CTAs resident (cooperative launch)
     int sfb_inline;
     const uint8_t* B_scale;
+    // direct (unfused kernel only): A is read in place from the R segment
+    // buffers through seg_maps[r] (tensor maps in global memory, 64-byte
+    // aligned), and the prologue also packs the A scales into sfa
+    int direct;
+    const CUtensorMap* seg_maps;
     uint16_t* C;                // bf16 [M][N]
     // split-K (S > 1): items of one output tile finish in any order; all but the
     // last write their fp32 tile to partial[tile][q] ([BM][BN]) and publish

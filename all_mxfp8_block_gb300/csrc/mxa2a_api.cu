@@ -122,6 +122,10 @@ struct mxa2a_plan {
     const void* tmap_b_ptr = nullptr;
     CUtensorMap tmap_c;                     // for the C pointer of the last run
     const void* tmap_c_ptr = nullptr;
+    // direct variant: one tensor map per segment, in the workspace (device)
+    CUtensorMap* seg_maps_dev = nullptr;
+    CUtensorMap seg_maps_host[kMaxSegments];
+    const void* seg_ptrs[kMaxSegments] = {};
     unsigned long long launch_id = 0, checked_launch = 0;
     // ring of (start, end) events around the main GEMM kernel of the last runs
     static constexpr int kEvRing = 4096;
@@ -344,8 +348,11 @@ int ensure_partials(mxa2a_plan* p) {
     return MXA2A_OK;
 }
 
+enum RunMode { kRunFused, kRunUnfused, kRunDirect };
+
 int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, const void* B, const void* B_sf,
-             void* C, void* stream_v, bool fused) {
+             void* C, void* stream_v, RunMode mode) {
+    const bool fused = mode == kRunFused;
     int rc = check_args(p, A_seg, A_sf, B, B_sf, C);
     if (rc) return rc;
     if ((rc = check_device(p))) return rc;
@@ -358,6 +365,25 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
     int launches = 0;
     GemmParams g;
     fill_params(p, g, A_seg, A_sf, C, fused);
+    if (mode == kRunDirect) {
+        // the single-CTA GEMM reading A in place: one tensor map per segment,
+        // re-encoded and copied to the workspace when the segment pointers change
+        if (g.pair) return MXA2A_ERR_INVALID_OPTION;
+        bool same = true;
+        for (int r = 0; r < p->R; ++r) same = same && p->seg_ptrs[r] == A_seg[r];
+        if (!same) {
+            for (int r = 0; r < p->R; ++r) {
+                if (!encode_2d(&p->seg_maps_host[r], A_seg[r], (uint64_t)p->ka, (uint64_t)p->M, BM))
+                    return MXA2A_ERR_CUDA;
+                p->seg_ptrs[r] = A_seg[r];
+            }
+            if ((rc = cuda_rc(cudaMemcpyAsync(p->seg_maps_dev, p->seg_maps_host, sizeof(CUtensorMap) * p->R,
+                                              cudaMemcpyHostToDevice, stream))))
+                return rc;
+        }
+        g.direct = 1;
+        g.seg_maps = p->seg_maps_dev;
+    }
     // Split partials are tagged with this run's launch index, which a graph
     // replays unchanged: a split plan must not be captured.
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
@@ -373,7 +399,7 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
             return rc;
         ++launches;
     }
-    if (!fused) {
+    if (mode == kRunUnfused) {
         if ((rc = cuda_rc(launch_pack_a(g, p->a_packed, 0, stream)))) return rc;
         ++launches;
     }
@@ -456,6 +482,7 @@ mxa2a_plan* mxa2a_create(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t 
     const size_t o_ap = off; off = align_up(off + p->apacked_bytes, 1024);
     const size_t o_flags = off; off = align_up(off + p->flags_bytes, 1024);
     const size_t o_status = off; off = align_up(off + sizeof(DevStatus), 1024);
+    const size_t o_maps = off; off = align_up(off + sizeof(CUtensorMap) * kMaxSegments, 1024);
     p->ws_bytes = off;
     if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -469,6 +496,7 @@ mxa2a_plan* mxa2a_create(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t 
     p->a_packed = p->ws + o_ap;
     p->flags = reinterpret_cast<unsigned long long*>(p->ws + o_flags);
     p->status = reinterpret_cast<DevStatus*>(p->ws + o_status);
+    p->seg_maps_dev = reinterpret_cast<CUtensorMap*>(p->ws + o_maps);
     bool ok = cudaMemset(p->ws + o_sfa, 0, p->sfa_bytes) == cudaSuccess &&
               cudaMemset(p->flags, 0, p->flags_bytes) == cudaSuccess &&
               cudaMemset(p->status, 0, sizeof(DevStatus)) == cudaSuccess &&
@@ -488,12 +516,17 @@ mxa2a_plan* mxa2a_create(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t 
 
 int mxa2a_run(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, const void* B, const void* B_sf,
               void* C, void* stream) {
-    return run_impl(p, A_seg, A_sf, B, B_sf, C, stream, true);
+    return run_impl(p, A_seg, A_sf, B, B_sf, C, stream, kRunFused);
 }
 
 int mxa2a_run_unfused(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, const void* B,
                       const void* B_sf, void* C, void* stream) {
-    return run_impl(p, A_seg, A_sf, B, B_sf, C, stream, false);
+    return run_impl(p, A_seg, A_sf, B, B_sf, C, stream, kRunUnfused);
+}
+
+int mxa2a_run_direct(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, const void* B,
+                     const void* B_sf, void* C, void* stream) {
+    return run_impl(p, A_seg, A_sf, B, B_sf, C, stream, kRunDirect);
 }
 
 int mxa2a_run_host(mxa2a_plan* p, const void* const* A_seg_h, const void* const* A_sf_h, const void* B_h,
@@ -539,7 +572,7 @@ int mxa2a_run_host(mxa2a_plan* p, const void* const* A_seg_h, const void* const*
     if (cudaMemcpyAsync(dB, B_h, b_b, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemcpyAsync(dBs, B_sf_h, bsf_b, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return MXA2A_ERR_CUDA;
-    rc = run_impl(p, dA, dS, dB, dBs, dC, stream_v, true);
+    rc = run_impl(p, dA, dS, dB, dBs, dC, stream_v, kRunFused);
     if (rc) return rc;
     if (cudaMemcpyAsync(C_h, dC, c_b, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MXA2A_ERR_CUDA;
     return MXA2A_OK;

@@ -286,7 +286,7 @@ __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const
     const uint64_t pol_keep = l2_policy_evict_last();
     const uint64_t pol_stream = l2_policy_evict_first();
     int it = 0;   // global stage sequence number; this producer issues it % kProducers == pid
-    if (p.sfb_inline) {
+    if (p.sfb_inline || p.direct) {
         if (!wait_counter(p, ctl, p.flags + FlagLayout::sfb_done(p.bn, p.R), gridDim.x, kRoleTma, -1, -1, -1))
             return;
         fence_proxy_async_global();   // the atoms were written through the generic proxy; TMA reads them
@@ -354,6 +354,9 @@ __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const
                         const int ring_row = ((s % p.bn) * p.R + r) * p.cm + (row0 - s * p.cm);
                         tma_load_2d_hint(a_dst + (size_t)b * p.box_m * BK, tma, bar, kx, ring_row, pol_stream);
                     }
+                } else if (p.direct) {
+                    // the A tile straight from segment r (no exchange, no pack)
+                    tma_load_2d_hint(a_dst, p.seg_maps + r, bar, kx, mt * BM, pol_stream);
                 } else {
                     tma_load_2d_hint(a_dst, tma, bar, kg, mt * BM, pol_stream);
                 }
@@ -819,6 +822,24 @@ __device__ void pack_sfb_slice(const GemmParams& p) {
     }
 }
 
+// A slice of the A scale pack for the direct variant (the scale part of
+// pack_a_kernel): word (kbg, m) = the 4 E8M0 bytes of row m for 128-wide K
+// block kbg, from segment kbg / kb_per_seg; rows past M get 0.
+__device__ void pack_sfa_slice(const GemmParams& p) {
+    uint32_t* sfa = reinterpret_cast<uint32_t*>(p.sfa_stage);
+    const int rows = p.Mg * BM;
+    const long long total = (long long)(p.K / BK) * rows;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int m = (int)(i % rows);
+        const int kbg = (int)(i / rows);
+        const int r = kbg / p.kb_per_seg;
+        const int kb = kbg - r * p.kb_per_seg;
+        const uint32_t v = m < p.M ? ld_nc_u32(p.A_sf_seg[r] + (size_t)m * (p.ka / 32) + (size_t)kb * 4) : 0u;
+        sfa[((size_t)kbg * p.Mg + (size_t)(m >> 7)) * (kSfAtomBytes / 4) + (size_t)((m & 31) * 4 + ((m & 127) >> 5))] = v;
+    }
+}
+
 // ------------------------------------------------------------------ kernel
 template <bool kFused, bool kPair, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -875,10 +896,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kPair) cluster_sync();   // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
-    if (p.sfb_inline) {
-        // every CTA packs its slice of the B scales; the producers wait for all
-        // of them before their first load (the CTAs are co-resident)
-        pack_sfb_slice(p);
+    if (p.sfb_inline || p.direct) {
+        // every CTA packs its slice of the B scales (and, direct, of the A
+        // scales); the producers wait for all of them before their first load
+        // (the CTAs are co-resident)
+        if (p.sfb_inline) pack_sfb_slice(p);
+        if (!kFused && p.direct) pack_sfa_slice(p);
         __syncthreads();
         if (threadIdx.x == 0) {
             __threadfence();
@@ -936,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
             tmem_dealloc(tmem, kTmemCols);
     }
-    if ((kFused || p.S > 1 || p.sfb_inline) && threadIdx.x == 0) {
+    if ((kFused || p.S > 1 || p.sfb_inline || p.direct) && threadIdx.x == 0) {
         // The last CTA to finish zeroes the staging credits and the scale-pack
         // count for the next launch, and, if this launch gave up somewhere, the
         // split-K tile counters.
@@ -955,7 +978,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (p.sfb_inline) atomicExch(p.flags + FlagLayout::sfb_done(p.bn, p.R), 0ull);
+            if (p.sfb_inline || p.direct) atomicExch(p.flags + FlagLayout::sfb_done(p.bn, p.R), 0ull);
             if (p.S > 1 && launch_failed(p))
                 for (int t = 0; t < p.Mt * p.Nt; ++t) atomicExch(&p.tile_cnt[t], 0u);
             atomicExch(done, 0ull);
@@ -1005,7 +1028,7 @@ cudaError_t launch_one(const GemmParams& p, const CUtensorMap& tmap_a, const CUt
         attr[0].val.cooperative = 1;
     }
     cfg.attrs = attr;
-    cfg.numAttrs = (kPair || kFused || p.sfb_inline) ? 1 : 0;
+    cfg.numAttrs = (kPair || kFused || p.sfb_inline || p.direct) ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, &mxgemm_kernel<kFused, kPair, kBN>, p, tmap_a, tmap_b, tmap_c);
 }
 

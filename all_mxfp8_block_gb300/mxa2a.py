@@ -93,6 +93,7 @@ _SIGS = [
     ("mxa2a_last_error", ctypes.c_int, []),
     ("mxa2a_run", ctypes.c_int, [_VP, _PP, _PP, _VP, _VP, _VP, _VP]),
     ("mxa2a_run_unfused", ctypes.c_int, [_VP, _PP, _PP, _VP, _VP, _VP, _VP]),
+    ("mxa2a_run_direct", ctypes.c_int, [_VP, _PP, _PP, _VP, _VP, _VP, _VP]),
     ("mxa2a_run_host", ctypes.c_int, [_VP, _PP, _PP, _VP, _VP, _VP, _VP]),
     ("mxa2a_get_status", ctypes.c_int, [_VP, ctypes.POINTER(mxa2a_status)]),
     ("mxa2a_set_option", ctypes.c_int, [_VP, ctypes.c_int, _I64]),
@@ -189,6 +190,11 @@ def mxa2a_run_unfused(plan, A_seg, A_scale_seg, B, B_scale, C_bf16, stream=None)
                                     _ptr(C_bf16), _stream(stream)), "mxa2a_run_unfused")
 
 
+def mxa2a_run_direct(plan, A_seg, A_scale_seg, B, B_scale, C_bf16, stream=None) -> None:
+    _check(load().mxa2a_run_direct(plan, _ptr_array(A_seg), _ptr_array(A_scale_seg), _ptr(B), _ptr(B_scale),
+                                   _ptr(C_bf16), _stream(stream)), "mxa2a_run_direct")
+
+
 def mxa2a_run_host(plan, A_seg, A_scale_seg, B, B_scale, C_bf16, stream=None) -> None:
     _check(load().mxa2a_run_host(plan, _ptr_array(A_seg), _ptr_array(A_scale_seg), _ptr(B), _ptr(B_scale),
                                  _ptr(C_bf16), _stream(stream)), "mxa2a_run_host")
@@ -267,6 +273,9 @@ class Plan:
 
     def run_unfused(self, A_seg, A_scale_seg, B, B_scale, C, stream=None):
         mxa2a_run_unfused(self.handle, A_seg, A_scale_seg, B, B_scale, C, stream)
+
+    def run_direct(self, A_seg, A_scale_seg, B, B_scale, C, stream=None):
+        mxa2a_run_direct(self.handle, A_seg, A_scale_seg, B, B_scale, C, stream)
 
     def run_host(self, A_seg, A_scale_seg, B, B_scale, C, stream=None):
         mxa2a_run_host(self.handle, A_seg, A_scale_seg, B, B_scale, C, stream)

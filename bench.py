@@ -341,6 +341,10 @@ def run_ours(args, w):
     other = plan.run_unfused if args.path == "fused" else plan.run
     other_steps = min(args.steps, 500)
     other_ms = timed_loop(other, other_steps, args.warmup)
+    # the direct-read ablation: A read in place, no exchange (same caliber)
+    direct_ms = None
+    if not plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED):
+        direct_ms = timed_loop(plan.run_direct, other_steps, args.warmup)
 
     t_local = sum(step_ms) / 1e3
     t_max, flops_total = reduce_max_sum(t_local, float(w.flops) * args.steps, dev if ws > 1 else None)
@@ -427,6 +431,10 @@ def run_ours(args, w):
         "unfused" if args.path == "fused" else "fused": {
             "ms_per_step": sum(other_ms) / len(other_ms), "steps": other_steps,
             "value": w.flops / (sum(other_ms) / len(other_ms) / 1e3) / 1e12},
+        "direct_read": None if direct_ms is None else {
+            "ms_per_step": sum(direct_ms) / len(direct_ms), "steps": other_steps,
+            "value": w.flops / (sum(direct_ms) / len(direct_ms) / 1e3) / 1e12,
+            "what": "A read in place from the segments (no staging ring, no pack): the exchange's cost"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": int(args.steps * (1 + launches_per_run)),

@@ -124,6 +124,22 @@ int mxa2a_run(mxa2a_plan *plan, const void *const *A_seg, const void *const *A_s
               const void *B_scale, void *C_bf16, void *stream);
 
 /*
+ * The direct-read variant (an ablation of the exchange): the GEMM reads each
+ * A_seg[r] in place with TMA, as the all_to_all_matmul kernel reads its own
+ * rank's block from local memory rather than from the receive buffer
+ * (all_to_all_matmul_impl.h, MatmulProcess / LocalParams); there is no
+ * staging ring, no credit protocol and no pack of A.  Its prologue packs the A
+ * and B scales.  Same arguments and result bits as mxa2a_run_unfused with the
+ * same K split; the single-CTA kernel only (MXA2A_ERR_INVALID_OPTION with
+ * MXA2A_OPT_CTA_PAIR = 1).  The tensor maps of the segments are encoded on the
+ * host and copied into the plan's workspace on the stream whenever the
+ * segment pointers differ from the previous direct run.  The CUDA-graph rules
+ * of mxa2a_run apply (MXA2A_INFO_SPLITS_UNFUSED).
+ */
+int mxa2a_run_direct(mxa2a_plan *plan, const void *const *A_seg, const void *const *A_scale_seg, const void *B,
+                     const void *B_scale, void *C_bf16, void *stream);
+
+/*
  * The unfused comparison path: first pack the R segments into one [M][K]
  * operand (and its scales), then run the same GEMM on it.  Same arguments;
  * the same result bits as mxa2a_run when both paths use the same K split

@@ -21,9 +21,10 @@ def to_device(x: dict, device="cuda") -> dict:
     }
 
 
-def run_gpu(plan: mxa2a.Plan, d: dict, M: int, N: int, fused: bool = True, stream=None) -> torch.Tensor:
+def run_gpu(plan: mxa2a.Plan, d: dict, M: int, N: int, fused=True, stream=None) -> torch.Tensor:
+    """One run; fused True = mxa2a_run, False = mxa2a_run_unfused, "direct" = mxa2a_run_direct."""
     C = torch.full((M, N), -1, dtype=torch.int16, device="cuda")   # 0xFFFF: a BF16 NaN until written
-    fn = plan.run if fused else plan.run_unfused
+    fn = plan.run_direct if fused == "direct" else (plan.run if fused else plan.run_unfused)
     if stream is not None:
         stream.wait_stream(torch.cuda.current_stream())   # inputs and C were written on it
     fn(d["A_seg"], d["A_scale_seg"], d["B"], d["B_scale"], C, stream)

@@ -222,6 +222,38 @@ def test_narrow_tiles_match_wide(case):
         assert np.array_equal(outs[(128, fused)], outs[(256, fused)]), f"narrow != wide, fused={fused}"
 
 
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_direct_read_matches_unfused(case):
+    """The direct-read variant (A read in place from the segments) against the
+    oracle and, bit for bit, against the unfused path at the same K split."""
+    name, R, M, ka, N, cm, bn = case
+    w = inputs.Workload(name, R, M, ka, N, cm, bn, 11)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w, split_k=1) as p:
+        got_d = gu.host_bits(gu.run_gpu(p, d, M, N, fused="direct"))
+        got_u = gu.host_bits(gu.run_gpu(p, d, M, N, fused=False))
+        torch.cuda.synchronize()
+        _status_ok(p)
+    gu.assert_parity(got_d, gu.oracle_full(x), f"{name} direct")
+    assert np.array_equal(got_d, got_u), "direct and unfused differ"
+
+
+def test_direct_read_split_and_new_segment_pointers():
+    """Split K, and a second run with other segment buffers (the tensor maps
+    are re-encoded)."""
+    w = inputs.Workload("direct_split", 4, 256, 256, 512, 128, 2, 73)
+    x1 = inputs.make_inputs(w)
+    x2 = inputs.make_inputs(inputs.Workload("direct_split", 4, 256, 256, 512, 128, 2, 74))
+    with _plan(w, split_k=2) as p:
+        for x in (x1, x2, x1):
+            d = gu.to_device(x)
+            got = gu.host_bits(gu.run_gpu(p, d, w.M, w.N, fused="direct"))
+            torch.cuda.synchronize()
+            _status_ok(p)
+            gu.assert_parity(got, gu.oracle_full(x), "direct split")
+
+
 @pytest.mark.parametrize("split", [2, 3])
 def test_narrow_tiles_split_k(split):
     w = inputs.Workload("nsplit", 6, 256, 256, 640, 128, 2, 71)
