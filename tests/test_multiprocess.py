@@ -1,0 +1,78 @@
+"""The N > 1 host path of the benchmark, on the CPU with the gloo backend.
+
+On a one-GPU-per-box pool the path does not shard across GPUs (the R segments
+are local buffers), so ``bench.py --gpus N`` runs N independent replicas: the
+only cross-rank logic is the timing reduction (slowest rank's time, summed
+work) and rank 0 printing the single JSON line.  Both are exercised here with
+two processes.
+"""
+from __future__ import annotations
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _reduce_worker(rank: int, world: int, port: int, out):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        t, w = bench.reduce_max_sum(float(rank + 1), 10.0 * (rank + 1))
+        out.put((rank, t, w))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_reduce_max_sum_two_ranks_gloo():
+    """Every rank sees the slowest rank's time and the total work."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_reduce_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    assert got == [(0, 2.0, 30.0), (1, 2.0, 30.0)]
+
+
+def test_reduce_max_sum_without_process_group_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.reduce_max_sum(3.0, 7.0) == (3.0, 7.0)
+
+
+def test_reference_arm_under_torchrun_two_ranks():
+    """``bench.py --impl reference`` launched like the driver's N=2 run: rank 0
+    alone prints one JSON line, every rank exits 0 (CPU only, tiny workload)."""
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3", "--workload", "0"]
+    res = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+    assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
