@@ -118,6 +118,8 @@ struct GemmParams {
     int fused, exchange_only;
     int rows_per_chunk, chunks_per_seg, n_copy_tasks;
     int fault_skip_step;        // test knob: never publish the fill of this step (-1 = off)
+    int step_credits;           // 1: whole-step fill and release (the pages' per-step protocol)
+    int copy_skew_ns;           // test knob: copy workers of every 4th CTA wait this long before each task
     uint8_t* ring;              // [bn][R][cm][ka]
     uint8_t* sfa_stage;         // writable alias of sfa (staged by the copy role)
     unsigned long long* flags;

@@ -92,6 +92,8 @@ struct mxa2a_plan {
     int Nt_fused = 0, Nt_unfused = 0;       // n-tiles per path
     int tile_opt = 0;                       // option: 0 automatic, 128 or 256 forced
     int elem_types = 0;                     // option: element-format pair (MXA2A_OPT_ELEM_TYPES)
+    int step_credits = 0;                   // option: whole-step staging credits
+    int copy_skew_ns = 0;                   // test knob: delay of every 4th CTA's copies
     int S_fused = 1, S_unfused = 1, W_fused = 0, W_unfused = 0;   // K splits and work items per path
     int pair_fused = 0, pair_unfused = 0;   // CTA-pair kernel in use, per path
     int group_fused = 1, group_unfused = 1; // raster group, in m rows (tiles or tile pairs)
@@ -295,6 +297,8 @@ void fill_params(mxa2a_plan* p, GemmParams& g, const void* const* A_seg, const v
     g.chunks_per_seg = p->chunks_per_seg;
     g.n_copy_tasks = p->n_copy_tasks;
     g.fault_skip_step = p->fault_skip_step;
+    g.step_credits = p->step_credits;
+    g.copy_skew_ns = p->copy_skew_ns;
     g.ring = p->ring;
     g.sfa_stage = p->sfa;
     g.flags = p->flags;
@@ -676,6 +680,14 @@ int mxa2a_set_option(mxa2a_plan* p, int key, int64_t v) {
             if (v < 0 || v > 3) return MXA2A_ERR_INVALID_OPTION;
             p->elem_types = (int)v;
             break;
+        case MXA2A_OPT_STEP_CREDITS:
+            if (v != 0 && v != 1) return MXA2A_ERR_INVALID_OPTION;
+            p->step_credits = (int)v;
+            break;
+        case MXA2A_OPT_COPY_SKEW_NS:
+            if (v < 0 || v > 1000000) return MXA2A_ERR_INVALID_OPTION;
+            p->copy_skew_ns = (int)v;
+            break;
         default:
             return MXA2A_ERR_INVALID_OPTION;
     }
@@ -699,6 +711,8 @@ int mxa2a_get_option(mxa2a_plan* p, int key, int64_t* v) {
         case MXA2A_OPT_GROUP_M: *v = p->group_cap; break;
         case MXA2A_OPT_TILE_N: *v = p->tile_opt; break;
         case MXA2A_OPT_ELEM_TYPES: *v = p->elem_types; break;
+        case MXA2A_OPT_STEP_CREDITS: *v = p->step_credits; break;
+        case MXA2A_OPT_COPY_SKEW_NS: *v = p->copy_skew_ns; break;
         case MXA2A_INFO_GROUP_FUSED: *v = p->group_fused; break;
         case MXA2A_INFO_GROUP_UNFUSED: *v = p->group_unfused; break;
         case MXA2A_INFO_CTA_PAIR: *v = p->pair_fused; break;

@@ -305,7 +305,24 @@ __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const
         // step can be published (and counted) before this item has read it.
         if (pid == 0) TRACE(4, w, 0);
         bool all_staged = !fused;
-        if (fused && p.S == 1) {
+        if (fused && p.step_credits) {
+            // whole-step fill: wait until every segment of the item's steps is staged
+            // (exact with step credits: a slot's next step is copied only after all of
+            // this step's segments were read, which needs them all published first)
+            int last_s = -1;
+            for (int b = 0; b < nbox; ++b) {
+                const int s = (mt * BM + b * p.box_m) / p.cm;
+                if (s == last_s) continue;
+                last_s = s;
+                const unsigned long long need =
+                    (unsigned long long)(s / p.bn + 1) * (unsigned long long)(p.R * p.chunks_per_seg);
+                if (!wait_counter(p, ctl, p.flags + FlagLayout::staged(s % p.bn, p.bn, p.R), need, kRoleTma, s, -1,
+                                  s % p.bn))
+                    return;
+            }
+            fence_proxy_async_global();
+            all_staged = true;
+        } else if (fused && p.S == 1) {
             all_staged = true;
             int last_s = -1;
             for (int b = 0; b < nbox && all_staged; ++b) {
@@ -707,6 +724,17 @@ __device__ __forceinline__ bool copy_task_ready(const GemmParams& p, int t, int 
     const int slot = s % p.bn;
     unsigned long long need = 0;
     for (int s2 = slot; s2 < s; s2 += p.bn) need += readers_of_segment(p, s2);
+    if (p.step_credits) {
+        // whole-step release: every segment of the slot's earlier steps read by all its readers
+        unsigned long long vmin = ~0ull;
+        for (int r2 = 0; r2 < p.R; ++r2) {
+            const unsigned long long v2 = ld_acquire_u64(p.flags + FlagLayout::drained(slot, r2, p.bn, p.R));
+            vmin = v2 < vmin ? v2 : vmin;
+        }
+        *observed = vmin;
+        *target = need;
+        return vmin >= need;
+    }
     const unsigned long long v = ld_acquire_u64(p.flags + FlagLayout::drained(slot, r, p.bn, p.R));
     *observed = v;
     *target = need;
@@ -770,6 +798,11 @@ __device__ void copy_role(const GemmParams& p, SmemCtl* ctl, int lane) {
         }
         const int t = __shfl_sync(0xffffffffu, chosen, 0);
         if (t < 0) return;   // uniform over the warp
+        if (p.copy_skew_ns > 0 && (blockIdx.x & 3) == 0) {
+            // test knob: a slow copier on every 4th CTA (a fixed delay, not a wait)
+            const uint64_t t0 = globaltimer();
+            while (globaltimer() - t0 < (uint64_t)p.copy_skew_ns) __nanosleep(256);
+        }
         const int s = t / per_step;
         const int rem = t - s * per_step;
         const int r = rem / p.chunks_per_seg;

@@ -346,6 +346,25 @@ def run_ours(args, w):
     if not plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED):
         direct_ms = timed_loop(plan.run_direct, other_steps, args.warmup)
 
+    # the staging protocol ablation (fused): per-segment credits against the
+    # whole-step protocol, each with and without slowed copies on every 4th CTA
+    credit_ablation = None
+    if args.path == "fused" and not args.no_ablation and not plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR):
+        credit_ablation = {"skew_ns": args.skew_ns, "steps": min(other_steps, 200),
+                           "what": "fused ms per step; skew: the copy workers of every 4th CTA wait skew_ns "
+                                   "before each copy task"}
+        for sc, name in ((0, "per_segment"), (1, "whole_step")):
+            for skew in (0, args.skew_ns):
+                plan.set_option(mxa2a.MXA2A_OPT_STEP_CREDITS, sc)
+                plan.set_option(mxa2a.MXA2A_OPT_COPY_SKEW_NS, skew)
+                ms = timed_loop(plan.run, credit_ablation["steps"], args.warmup)
+                credit_ablation[name + ("_skew_ms" if skew else "_ms")] = sum(ms) / len(ms)
+        plan.set_option(mxa2a.MXA2A_OPT_STEP_CREDITS, 0)
+        plan.set_option(mxa2a.MXA2A_OPT_COPY_SKEW_NS, 0)
+        st = plan.status()
+        if st["code"] != 0:
+            raise RuntimeError(f"device status after the credit ablation: {st}")
+
     t_local = sum(step_ms) / 1e3
     t_max, flops_total = reduce_max_sum(t_local, float(w.flops) * args.steps, dev if ws > 1 else None)
     value = flops_total / t_max / 1e12
@@ -435,6 +454,7 @@ def run_ours(args, w):
             "ms_per_step": sum(direct_ms) / len(direct_ms), "steps": other_steps,
             "value": w.flops / (sum(direct_ms) / len(direct_ms) / 1e3) / 1e12,
             "what": "A read in place from the segments (no staging ring, no pack): the exchange's cost"},
+        "credit_ablation": credit_ablation,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": int(args.steps * (1 + launches_per_run)),
@@ -467,6 +487,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph timing of the smallest workload")
+    ap.add_argument("--no-ablation", action="store_true", help="skip the staging-protocol ablation timings")
+    ap.add_argument("--skew-ns", type=int, default=4000, help="copy delay of every 4th CTA in the ablation")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--split", type=int, default=0, help="force the K split of both paths (0 = automatic)")
     ap.add_argument("--single-cta", action="store_true", help="never use the CTA-pair kernel")

@@ -193,6 +193,12 @@ enum mxa2a_option {
                                       all_to_all_matmul kernel (all_to_all_matmul_impl.h):
                                       0 (default) E4M3 x E4M3, 1 E5M2 x E5M2, 2 E4M3 x E5M2,
                                       3 E5M2 x E4M3.  Scales stay E8M0, one per 32 along K */
+    MXA2A_OPT_STEP_CREDITS = 15,   /* 1: whole-step staging protocol, as the all_to_all_matmul kernel's
+                                      AllToAllProcess / MatmulProcess (a slot's next step is copied once
+                                      every reader finished the whole previous step; a reader waits for
+                                      the whole step); 0 (default): per-segment credits */
+    MXA2A_OPT_COPY_SKEW_NS = 16,   /* test knob: the copy workers of every 4th CTA wait this many ns
+                                      before each copy task (0 = off, at most 1e6) */
     /* read-only plan facts (mxa2a_get_option only) */
     MXA2A_INFO_STEPS = 100,        /* M / commMSize */
     MXA2A_INFO_MTILES = 101,

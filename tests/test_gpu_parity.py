@@ -254,6 +254,40 @@ def test_direct_read_split_and_new_segment_pointers():
             gu.assert_parity(got, gu.oracle_full(x), "direct split")
 
 
+@pytest.mark.parametrize("split", [1, 2])
+def test_step_credits_and_copy_skew_same_bits(split):
+    """The whole-step staging protocol (a slot refilled only after every reader
+    finished the whole previous step; readers wait for the whole step) and the
+    per-segment credits, each with and without slowed copies on every 4th CTA:
+    the oracle's results and, bit for bit, one another.  8 steps through a
+    2-slot ring, so every slot is reused three times."""
+    w = inputs.Workload("stepcred", 4, 1024, 256, 768, 128, 2, 83)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    outs = {}
+    for sc in (0, 1):
+        for skew in (0, 20_000):
+            with _plan(w, split_k=split, grid=8, step_credits=sc, copy_skew_ns=skew) as p:
+                assert p.get_option(mxa2a.MXA2A_OPT_STEP_CREDITS) == sc
+                assert p.get_option(mxa2a.MXA2A_OPT_COPY_SKEW_NS) == skew
+                outs[(sc, skew)] = gu.host_bits(gu.run_gpu(p, d, w.M, w.N))
+                torch.cuda.synchronize()
+                _status_ok(p)
+    gu.assert_parity(outs[(1, 20_000)], gu.oracle_full(x), "whole-step credits with skew")
+    for k, v in outs.items():
+        assert np.array_equal(v, outs[(0, 0)]), f"step_credits, skew = {k} differs"
+
+
+def test_step_credit_options_validated():
+    w = inputs.workload(0)
+    with _plan(w) as p:
+        assert p.get_option(mxa2a.MXA2A_OPT_STEP_CREDITS) == 0
+        for key, bad in ((mxa2a.MXA2A_OPT_STEP_CREDITS, 2), (mxa2a.MXA2A_OPT_COPY_SKEW_NS, -1),
+                         (mxa2a.MXA2A_OPT_COPY_SKEW_NS, 2_000_000)):
+            with pytest.raises(mxa2a.Mxa2aError):
+                p.set_option(key, bad)
+
+
 @pytest.mark.parametrize("split", [2, 3])
 def test_narrow_tiles_split_k(split):
     w = inputs.Workload("nsplit", 6, 256, 256, 640, 128, 2, 71)
