@@ -173,3 +173,110 @@ def random_scales(shape, seed: int, lo: int = 0, hi: int = 254) -> torch.Tensor:
     """Uniformly random E8M0 scale bytes in ``[lo, hi]`` (255 = NaN excluded)."""
     g = torch.Generator().manual_seed(seed)
     return torch.randint(lo, hi + 1, shape, generator=g, dtype=torch.int32).to(torch.uint8)
+
+
+# --- the sibling fused operators ------------------------------------------------------
+
+@dataclass(frozen=True)
+class AllGatherWorkload:
+    """One problem size of AllGather + GEMM: R row blocks of rowsPerRank rows
+    (all K columns) stacked along M, times B [N][K]."""
+    name: str
+    R: int
+    rowsPerRank: int
+    K: int
+    N: int
+    commMSize: int
+    buffer_num: int
+    seed: int
+
+    @property
+    def M(self) -> int:
+        return self.R * self.rowsPerRank
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def bytes_alg(self) -> int:
+        M, K, N = self.M, self.K, self.N
+        return M * K + M * K // MX_BLOCK + N * K + N * K // MX_BLOCK + 2 * M * N
+
+
+@dataclass(frozen=True)
+class ReduceScatterWorkload:
+    """One problem size of GEMM + ReduceScatter, seen from rank ``rank`` of
+    ``R``: A [M][K], B [N][K], blocks of M / R rows."""
+    name: str
+    R: int
+    rank: int
+    M: int
+    K: int
+    N: int
+    seed: int
+
+    @property
+    def rows(self) -> int:
+        return self.M // self.R
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def bytes_alg(self) -> int:
+        """A, B and their scales once; R-1 received blocks, R-1 sent blocks and the output block (BF16)."""
+        M, K, N = self.M, self.K, self.N
+        return (M * K + M * K // MX_BLOCK + N * K + N * K // MX_BLOCK
+                + 2 * (2 * (self.R - 1) + 1) * self.rows * N)
+
+
+# The sibling workloads: a small one the oracle finishes at once, and one of
+# the headline's size (2048 x 4096 x 4096 flops, 4 ranks; the all-gather's
+# ring holds two 256-row steps, as the headline all-to-all's does).
+AG_WORKLOADS = [
+    AllGatherWorkload("ag_r3_m384_k384_n272", 3, 128, 384, 272, 64, 2, 20),
+    AllGatherWorkload("ag_r4_m2048_k4096_n4096", 4, 512, 4096, 4096, 256, 2, 21),
+]
+RS_WORKLOADS = [
+    ReduceScatterWorkload("rs_r3_m384_k384_n272", 3, 1, 384, 384, 272, 30),
+    ReduceScatterWorkload("rs_r4_m2048_k4096_n4096", 4, 1, 2048, 4096, 4096, 31),
+]
+
+
+def make_allgather_inputs(w: AllGatherWorkload) -> dict:
+    """Draw and quantise AllGather + GEMM inputs (CPU tensors).  Draw order:
+    ``A_j = randn(rowsPerRank, K)`` for j = 0..R-1, then ``B = randn(K, N) /
+    sqrt(K)``."""
+    g = torch.Generator().manual_seed(w.seed)
+    A = [torch.randn(w.rowsPerRank, w.K, generator=g, dtype=torch.float32) for _ in range(w.R)]
+    B = torch.randn(w.K, w.N, generator=g, dtype=torch.float32) / math.sqrt(w.K)
+    A_blk, A_sf = [], []
+    for a in A:
+        c, s = quantize_mx_rows(a.contiguous())
+        A_blk.append(c)
+        A_sf.append(s)
+    B_codes, B_sf = quantize_mx_rows(B.t().contiguous())
+    return {"A_blk": A_blk, "A_scale_blk": A_sf, "B": B_codes, "B_scale": B_sf, "workload": w}
+
+
+def make_reduce_scatter_inputs(w: ReduceScatterWorkload) -> dict:
+    """Draw GEMM + ReduceScatter inputs (CPU tensors).  Draw order: ``A =
+    randn(M, K)``, ``B = randn(K, N) / sqrt(K)`` (quantised to MXFP8 as for
+    the all-to-all), then for every peer j != rank in order the partial it
+    sent, ``randn(M/R, N)`` rounded to BF16 (the magnitude of a partial of
+    this shape), as int16 bit patterns; ``recv[rank]`` is None."""
+    g = torch.Generator().manual_seed(w.seed)
+    A = torch.randn(w.M, w.K, generator=g, dtype=torch.float32)
+    B = torch.randn(w.K, w.N, generator=g, dtype=torch.float32) / math.sqrt(w.K)
+    recv = []
+    for j in range(w.R):
+        if j == w.rank:
+            recv.append(None)
+        else:
+            r = torch.randn(w.rows, w.N, generator=g, dtype=torch.float32)
+            recv.append(r.to(torch.bfloat16).view(torch.int16).contiguous())
+    A_codes, A_sf = quantize_mx_rows(A)
+    B_codes, B_sf = quantize_mx_rows(B.t().contiguous())
+    return {"A": A_codes, "A_scale": A_sf, "B": B_codes, "B_scale": B_sf, "recv": recv, "workload": w}

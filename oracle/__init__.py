@@ -13,7 +13,12 @@ Every oracle function is pinned by tests in ``tests/test_oracle_pins.py``
 against things other than itself: torch's float8 decoders (exhaustive), exact
 rational brute force, float64 matmul of exactly representable cases, identity
 and one-hot operands, power-of-two scale invariance, segment-order
-permutation and hand-worked fixtures in ``tests/golden/``.
+permutation and hand-worked fixtures in ``tests/golden/``.  The two sibling
+fused operators (AllGather + GEMM, GEMM + ReduceScatter, the performance
+optimisation guide's section 3 cases) are compositions of :func:`gemm` with a
+row stack and with an exact sum rounded once; they are pinned in
+``tests/test_oracle_siblings.py`` (identity operands with known blocks, exact
+rational sums, torch's BF16 rounding).
 """
 from __future__ import annotations
 
@@ -146,3 +151,82 @@ def gemm(A_seg, A_scale_seg, B, B_scale, rows=None, cols=None, nthreads: int = 0
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     """Widen BF16 bit patterns to float32 (exact)."""
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def round_f64_to_bf16(x) -> np.ndarray:
+    """BF16 bit patterns (uint16) of float64 values, rounded to nearest with
+    ties to even.  BF16 keeps 8 significant bits; a finite x with
+    2^e <= |x| < 2^(e+1) is rounded to a multiple of 2^(e-7), and below the
+    smallest normal (2^-126) to a multiple of 2^-133 (the subnormal spacing).
+    Dividing by that power of two is exact in float64 and ``np.rint`` rounds
+    half to even, so the rounding is exact.  Magnitudes that round to 2^128 or
+    beyond become infinities; NaN stays NaN."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.float64)
+    finite = np.isfinite(x)
+    xf = np.where(finite, x, 0.0)
+    _, e = np.frexp(xf)                      # |x| = m 2^e, m in [0.5, 1): binade 2^(e-1)
+    q = np.maximum(e - 1 - 7, -133)          # exponent of the BF16 spacing there
+    r = np.rint(np.ldexp(xf, -q))            # exact scaling, ties to even
+    out[finite] = np.ldexp(r, q)[finite]
+    out[~finite] = x[~finite]
+    out = np.where(np.abs(out) >= 2.0 ** 128, np.copysign(np.inf, out), out)
+    f32 = out.astype(np.float32)             # exact: every BF16 value is a float32
+    return (f32.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Widen BF16 bit patterns to float64 (exact)."""
+    return bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def gemm_allgather(A_blk, A_scale_blk, B, B_scale, rows=None, cols=None, nthreads: int = 0,
+                   a_fmt: str = "e4m3", b_fmt: str = "e4m3") -> np.ndarray:
+    """AllGather + GEMM (performance optimisation guide, section 3.1, which
+    names the operator only): the R row blocks ``A_blk[j]`` ([rowsPerRank][K]
+    codes, scales [rowsPerRank][K/32]) are gathered, i.e. stacked along M with
+    block j at rows j*rowsPerRank.., and multiplied by B exactly as
+    :func:`gemm` does with a single K segment.  Returns BF16 bits [M][N] (or
+    the ``rows`` x ``cols`` sub-block)."""
+    A = np.concatenate([_np_u8(a) for a in A_blk], axis=0)
+    S = np.concatenate([_np_u8(s) for s in A_scale_blk], axis=0)
+    return gemm([A], [S], B, B_scale, rows=rows, cols=cols, nthreads=nthreads, a_fmt=a_fmt, b_fmt=b_fmt)
+
+
+def _exact_sum(terms):
+    """Sum float64 arrays in float64, asserting that no addition rounded
+    (Knuth's two-sum error term is zero wherever the result is finite)."""
+    s = np.zeros_like(terms[0])
+    for t in terms:
+        new = s + t
+        bp = new - s
+        err = (s - (new - bp)) + (t - bp)
+        ok = ~np.isfinite(new) | (err == 0)
+        assert np.all(ok), "oracle: the float64 sum is not exact for these inputs"
+        s = new
+    return s
+
+
+def gemm_reduce_scatter(A, A_scale, B, B_scale, recv, R: int, rank: int, nthreads: int = 0,
+                        a_fmt: str = "e4m3", b_fmt: str = "e4m3"):
+    """GEMM + ReduceScatter from rank ``rank`` of ``R`` (performance
+    optimisation guide, section 3.2, which names the operator only).  This
+    rank's partial is P = :func:`gemm` of its A [M][K] and B [N][K], as BF16
+    (the type the partials travel in).  Rows j*Mr .. (j+1)*Mr - 1 (Mr = M/R)
+    of P are the block sent to rank j; this rank's output is the sum over
+    ranks j of block ``rank`` of rank j's partial (``recv[j]``, BF16 bits
+    [Mr][N], for j != rank; P's own block for j == rank), computed exactly and
+    rounded once to BF16.  Returns ``(send, out)``: ``send`` a dict j -> BF16
+    bits [Mr][N] for j != rank, ``out`` BF16 bits [Mr][N]."""
+    P = gemm([A], [A_scale], B, B_scale, nthreads=nthreads, a_fmt=a_fmt, b_fmt=b_fmt)
+    M = P.shape[0]
+    assert M % R == 0 and 0 <= rank < R and len(recv) == R
+    Mr = M // R
+    send = {j: P[j * Mr:(j + 1) * Mr].copy() for j in range(R) if j != rank}
+    terms = []
+    for j in range(R):
+        blk = P[rank * Mr:(rank + 1) * Mr] if j == rank else np.asarray(recv[j]).view(np.uint16)
+        assert blk.shape == (Mr, P.shape[1])
+        terms.append(bf16_bits_to_f64(blk))
+    out = round_f64_to_bf16(_exact_sum(terms))
+    return send, out
