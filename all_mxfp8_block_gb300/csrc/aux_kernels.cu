@@ -10,6 +10,8 @@
 // scale of row/column 32c + x%32.  The pages' scale operands are the E8M0
 // tensors scaleA / scaleB (all_to_all_matmul_impl.h, LayoutScaleA/B with byte
 // pairs SCALE_C0 = 2): the same bytes in the hardware's own order.
+#include <cuda_bf16.h>
+
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -34,7 +36,8 @@ __global__ void pack_sfb_kernel(const uint8_t* __restrict__ B_scale, int N, int 
 }
 
 // Unfused variant: A_packed[m][r*ka + k] = A_seg[r][m][k] (the segments
-// concatenated along K), and the A scales into atoms [K/128][Mg][512].
+// concatenated along K; for the all-gather the row blocks stacked along M),
+// and the A scales into atoms [K/128][Mg][512].
 __global__ void pack_a_kernel(const __grid_constant__ GemmParams p, uint8_t* __restrict__ a_packed) {
     const long long stride = (long long)gridDim.x * blockDim.x;
     const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
@@ -45,7 +48,8 @@ __global__ void pack_a_kernel(const __grid_constant__ GemmParams p, uint8_t* __r
         const int k = (int)(i - (long long)m * v_per_row) * 16;
         const int r = k / p.ka;
         const int kin = k - r * p.ka;
-        const uint4 v = ptx::ld_nc_v4(p.A_seg[r] + (size_t)m * p.ka + kin);
+        const SegRow src = seg_row(p, r, m);
+        const uint4 v = ptx::ld_nc_v4(p.A_seg[src.seg] + (size_t)src.row * seg_ld(p) + seg_col0(p, r) + kin);
         *reinterpret_cast<uint4*>(a_packed + (size_t)m * p.K + k) = v;
     }
     const int kbs = p.K / BK;
@@ -58,7 +62,9 @@ __global__ void pack_a_kernel(const __grid_constant__ GemmParams p, uint8_t* __r
         if (m < p.M) {
             const int r = kbg / p.kb_per_seg;
             const int kb = kbg - r * p.kb_per_seg;
-            v = ptx::ld_nc_u32(p.A_sf_seg[r] + (size_t)m * (p.ka / 32) + (size_t)kb * 4);
+            const SegRow src = seg_row(p, r, m);
+            v = ptx::ld_nc_u32(p.A_sf_seg[src.seg] + (size_t)src.row * (seg_ld(p) / 32) + seg_col0(p, r) / 32 +
+                               (size_t)kb * 4);
         }
         sfa[atom_word(kbg, p.Mg, m)] = v;
     }
@@ -93,6 +99,51 @@ cudaError_t launch_pack_sfb(const uint8_t* B_scale, int N, int K, int Ng2, uint8
 cudaError_t launch_pack_a(const GemmParams& p, uint8_t* a_packed, int grid, cudaStream_t stream) {
     const long long work = (long long)p.M * p.K / 16;
     pack_a_kernel<<<grid > 0 ? grid : grid_for(work, 256), 256, 0, stream>>>(p, a_packed);
+    return cudaGetLastError();
+}
+
+// The collective step of the unfused GEMM + ReduceScatter: one thread per 8
+// columns (16 bytes) of a row of P.  Same arithmetic as the fused epilogue:
+// fp32 adds of the BF16 partials in rank order from 0, one rounding to BF16.
+__global__ void rs_reduce_kernel(const __grid_constant__ RsArgs a) {
+    const int vpr = a.N / 8;
+    const long long total = (long long)a.R * a.rows * vpr;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int v = (int)(i % vpr);
+        const long long row = i / vpr;
+        const int j = (int)(row / a.rows);
+        const size_t off = (size_t)(row - (long long)j * a.rows) * a.N + (size_t)v * 8;
+        const uint16_t* own = a.P + (size_t)row * a.N + (size_t)v * 8;
+        if (j != a.rank) {
+            *reinterpret_cast<uint4*>(a.send[j] + off) = ptx::ld_nc_v4(own);
+            continue;
+        }
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+        for (int q = 0; q < a.R; ++q) {
+            const uint4 t = ptx::ld_nc_v4(q == a.rank ? own : a.recv[q] + off);
+            const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc[2 * e] += __uint_as_float(w[e] << 16);
+                acc[2 * e + 1] += __uint_as_float(w[e] & 0xffff0000u);
+            }
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+            o[e] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+        *reinterpret_cast<uint4*>(a.out + off) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+cudaError_t launch_rs_reduce(const RsArgs& a, cudaStream_t stream) {
+    const long long work = (long long)a.R * a.rows * (a.N / 8);
+    rs_reduce_kernel<<<grid_for(work, 256), 256, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -54,7 +54,7 @@ constexpr int kErrTimeout = 6;
 constexpr int kErrDeviceCheck = 8;
 
 // Role ids recorded with a device error.
-constexpr int kRoleCopy = 1, kRoleTma = 2, kRoleMma = 3, kRoleEpi = 4, kRoleExit = 5;
+constexpr int kRoleCopy = 1, kRoleTma = 2, kRoleMma = 3, kRoleEpi = 4, kRoleExit = 5, kRoleReduce = 6;
 
 struct DevStatus {
     unsigned long long key;   // (launch_id << 8) | code, first error of a launch wins
@@ -126,9 +126,42 @@ struct GemmParams {
     DevStatus* status;
     unsigned long long launch_id;
     long long timeout_ns;
+    // seg_rows: 0 for the all-to-all (A_seg[r] holds K slice r of all M rows,
+    // [M][ka]); > 0 for the all-gather (A_seg[j] holds rows j*seg_rows ..
+    // (j+1)*seg_rows-1 of A with all K = R*ka columns, [seg_rows][K]; the R
+    // K slices are then column ranges of every block)
+    int seg_rows;
     const uint8_t* A_seg[kMaxSegments];
     const uint8_t* A_sf_seg[kMaxSegments];
+    // GEMM + ReduceScatter (rs_rows > 0, S == 1, the kernel without staging):
+    // the output rows form rs_R blocks of rs_rows.  The epilogue stores block
+    // j != rs_rank, rounded to BF16, through send_maps[j] (bf16 [rs_rows][N],
+    // 64-byte aligned maps in global memory) and block rs_rank through tmap_c
+    // (C = out, [rs_rows][N]), then counts its warp in rs_cnt[tile]; the copy
+    // warps then sum each row of out with recv[j] (fp32, j in order) in place.
+    // The m-tiles are taken starting at block rs_rank's, so its sums overlap
+    // the other blocks' GEMM.
+    int rs_rows, rs_rank, rs_R;
+    const CUtensorMap* send_maps;
+    const uint16_t* recv[kMaxSegments];
+    unsigned long long* rs_cnt;   // [Mt * Nt], zero between launches
 };
+
+// Where row m of K slice r of the stacked A lives: its input buffer and the
+// row inside it; seg_ld is that buffer's row length in bytes (scales: /32)
+// and seg_col0 the column where slice r starts in it.
+struct SegRow {
+    int seg, row;
+};
+__host__ __device__ inline SegRow seg_row(const GemmParams& p, int r, int m) {
+    if (p.seg_rows > 0) {
+        const int j = m / p.seg_rows;
+        return {j, m - j * p.seg_rows};
+    }
+    return {r, m};
+}
+__host__ __device__ inline int seg_ld(const GemmParams& p) { return p.seg_rows > 0 ? p.K : p.ka; }
+__host__ __device__ inline int seg_col0(const GemmParams& p, int r) { return p.seg_rows > 0 ? r * p.ka : 0; }
 
 // Launchers (mxgemm.cu / aux_kernels.cu).  All return cudaError_t of the launch.
 // tmap_c: C as bf16 [M][N], box 32 rows x 32 columns, 64-byte swizzle (the epilogue's TMA stores)
@@ -139,5 +172,16 @@ int mxgemm_max_pairs(bool fused);
 cudaError_t launch_pack_a(const GemmParams& p, uint8_t* a_packed, int grid, cudaStream_t stream);
 cudaError_t launch_pack_sfb(const uint8_t* B_scale, int N, int K, int Ng2, uint8_t* sfb, cudaStream_t stream);
 cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t stream);
+// The reduce-scatter of the unfused GEMM + ReduceScatter: P bf16 [R*rows][N];
+// send[j] = block j of P (j != rank); out = bf16(sum over j in order of block
+// rank of P (j == rank) or recv[j]), fp32 adds.  Pointer arrays of R entries.
+struct RsArgs {
+    const uint16_t* P;
+    const uint16_t* recv[kMaxSegments];
+    uint16_t* send[kMaxSegments];
+    uint16_t* out;
+    int R, rank, rows, N;
+};
+cudaError_t launch_rs_reduce(const RsArgs& a, cudaStream_t stream);
 
 }  // namespace mxa2a

@@ -81,9 +81,12 @@ int tile_span(int64_t M, int64_t cm, int64_t rows = BM) {
 }  // namespace
 
 struct mxa2a_plan {
-    int R;
+    int R;                  // K slices of the GEMM's A (1 for the all-gather)
     int64_t M, ka, N, cm;
     int bn;
+    int kind = MXA2A_KIND_ALLTOALL;
+    int nseg = 0;           // input buffers of A: R (all-to-all) or the ranks (all-gather)
+    int64_t seg_rows = 0;   // all-gather: rows per input block; 0: all M rows
     int device = 0, sm_count = 0;
     // derived
     int64_t K = 0;
@@ -139,6 +142,17 @@ struct mxa2a_plan {
     // host-buffer path
     uint8_t* io = nullptr;
     size_t io_bytes = 0;
+    // GEMM + ReduceScatter: this rank, the ranks, rows per block
+    int rs_rank = 0, rs_R = 0;
+    int64_t rs_rows = 0;
+    uint16_t* rs_scratch = nullptr;         // the unfused path's partial P [M][N] (allocated on first use)
+    CUtensorMap* send_maps_dev = nullptr;   // workspace, after the segment maps
+    CUtensorMap send_maps_host[kMaxSegments];
+    const void* send_ptrs[kMaxSegments] = {};
+    CUtensorMap tmap_out;                   // out [rs_rows][N] of the last fused run
+    const void* tmap_out_ptr = nullptr;
+    unsigned long long* rs_cnt = nullptr;   // workspace: per-tile epilogue counts [Mt * 2 Nt]
+    size_t rs_cnt_bytes = 0;
 };
 
 namespace {
@@ -249,7 +263,7 @@ int check_device(mxa2a_plan* p) {
 int check_args(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, const void* B, const void* B_sf,
                const void* C) {
     if (!p || !A_seg || !A_sf || !B || !B_sf || !C) return MXA2A_ERR_NULL_PTR;
-    for (int r = 0; r < p->R; ++r) {
+    for (int r = 0; r < p->nseg; ++r) {
         if (!A_seg[r] || !A_sf[r]) return MXA2A_ERR_NULL_PTR;
         if (!aligned(A_seg[r], 16) || !aligned(A_sf[r], 4)) return MXA2A_ERR_MISALIGNED;
     }
@@ -305,7 +319,8 @@ void fill_params(mxa2a_plan* p, GemmParams& g, const void* const* A_seg, const v
     g.status = p->status;
     g.launch_id = ++p->launch_id;
     g.timeout_ns = p->timeout_ns;
-    for (int r = 0; r < p->R; ++r) {
+    g.seg_rows = (int)p->seg_rows;
+    for (int r = 0; r < p->nseg; ++r) {
         g.A_seg[r] = static_cast<const uint8_t*>(A_seg[r]);
         g.A_sf_seg[r] = static_cast<const uint8_t*>(A_sf[r]);
     }
@@ -354,14 +369,31 @@ int ensure_partials(mxa2a_plan* p) {
 
 enum RunMode { kRunFused, kRunUnfused, kRunDirect };
 
+// The reduce-scatter side of one GEMM + ReduceScatter run.
+struct RsRun {
+    bool fused;                 // the GEMM's epilogue routes and sums (else the reduce kernel after it)
+    const void* const* recv;
+    void* const* send;
+    void* out;
+};
+
 int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, const void* B, const void* B_sf,
-             void* C, void* stream_v, RunMode mode) {
+             void* C, void* stream_v, RunMode mode, const RsRun* rs = nullptr) {
     const bool fused = mode == kRunFused;
     int rc = check_args(p, A_seg, A_sf, B, B_sf, C);
     if (rc) return rc;
+    // a reduce-scatter plan runs through its own calls only, and they through this path with A read in place
+    if ((p->kind == MXA2A_KIND_REDUCE_SCATTER) != (rs != nullptr) || (rs && mode != kRunDirect))
+        return MXA2A_ERR_INVALID_OPTION;
     if ((rc = check_device(p))) return rc;
     if ((rc = refresh_b_map(p, B))) return rc;
-    if (p->tmap_c_ptr != C) {
+    const bool rs_fused = rs && rs->fused;
+    if (rs_fused) {
+        if (p->tmap_out_ptr != C) {
+            if (!encode_c(&p->tmap_out, C, (uint64_t)p->rs_rows, (uint64_t)p->N)) return MXA2A_ERR_CUDA;
+            p->tmap_out_ptr = C;
+        }
+    } else if (p->tmap_c_ptr != C) {
         if (!encode_c(&p->tmap_c, C, (uint64_t)p->M, (uint64_t)p->N)) return MXA2A_ERR_CUDA;
         p->tmap_c_ptr = C;
     }
@@ -373,20 +405,51 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
         // the single-CTA GEMM reading A in place: one tensor map per segment,
         // re-encoded and copied to the workspace when the segment pointers change
         if (g.pair) return MXA2A_ERR_INVALID_OPTION;
+        // all-gather: every 128-row tile must sit inside one input block
+        if (p->seg_rows % BM) return MXA2A_ERR_INVALID_OPTION;
+        const uint64_t rows = p->seg_rows ? (uint64_t)p->seg_rows : (uint64_t)p->M;
+        const uint64_t cols = p->seg_rows ? (uint64_t)p->K : (uint64_t)p->ka;   // an input buffer's row
         bool same = true;
-        for (int r = 0; r < p->R; ++r) same = same && p->seg_ptrs[r] == A_seg[r];
+        for (int r = 0; r < p->nseg; ++r) same = same && p->seg_ptrs[r] == A_seg[r];
         if (!same) {
-            for (int r = 0; r < p->R; ++r) {
-                if (!encode_2d(&p->seg_maps_host[r], A_seg[r], (uint64_t)p->ka, (uint64_t)p->M, BM))
+            for (int r = 0; r < p->nseg; ++r) {
+                if (!encode_2d(&p->seg_maps_host[r], A_seg[r], cols, rows, BM))
                     return MXA2A_ERR_CUDA;
                 p->seg_ptrs[r] = A_seg[r];
             }
-            if ((rc = cuda_rc(cudaMemcpyAsync(p->seg_maps_dev, p->seg_maps_host, sizeof(CUtensorMap) * p->R,
+            if ((rc = cuda_rc(cudaMemcpyAsync(p->seg_maps_dev, p->seg_maps_host, sizeof(CUtensorMap) * p->nseg,
                                               cudaMemcpyHostToDevice, stream))))
                 return rc;
         }
         g.direct = 1;
         g.seg_maps = p->seg_maps_dev;
+    }
+    if (rs_fused) {
+        // the epilogue stores the peers' blocks through one tensor map per send buffer
+        bool same = true;
+        for (int j = 0; j < p->rs_R; ++j) same = same && (j == p->rs_rank || p->send_ptrs[j] == rs->send[j]);
+        if (!same) {
+            for (int j = 0; j < p->rs_R; ++j) {
+                if (j == p->rs_rank) {
+                    std::memset(&p->send_maps_host[j], 0, sizeof(CUtensorMap));
+                    p->send_ptrs[j] = nullptr;
+                } else {
+                    if (!encode_c(&p->send_maps_host[j], rs->send[j], (uint64_t)p->rs_rows, (uint64_t)p->N))
+                        return MXA2A_ERR_CUDA;
+                    p->send_ptrs[j] = rs->send[j];
+                }
+            }
+            if ((rc = cuda_rc(cudaMemcpyAsync(p->send_maps_dev, p->send_maps_host, sizeof(CUtensorMap) * p->rs_R,
+                                              cudaMemcpyHostToDevice, stream))))
+                return rc;
+        }
+        g.rs_rows = (int)p->rs_rows;
+        g.rs_rank = p->rs_rank;
+        g.rs_R = p->rs_R;
+        g.send_maps = p->send_maps_dev;
+        g.rs_cnt = p->rs_cnt;
+        for (int j = 0; j < p->rs_R; ++j)
+            g.recv[j] = j == p->rs_rank ? nullptr : static_cast<const uint16_t*>(rs->recv[j]);
     }
     // Split partials are tagged with this run's launch index, which a graph
     // replays unchanged: a split plan must not be captured.
@@ -411,15 +474,124 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
     if (p->record_events && (rc = cuda_rc(cudaEventRecord(p->ev0[ev_slot], stream)))) return rc;
     rc = cuda_rc(launch_mxgemm(g, fused ? p->tmap_ring : p->tmap_apacked,
                                (g.pair || g.tile_n == BN_NARROW) ? p->tmap_b_half : p->tmap_b,
-                               p->tmap_c, fused ? p->grid_fused : p->grid_unfused, fused, stream));
+                               rs_fused ? p->tmap_out : p->tmap_c, fused ? p->grid_fused : p->grid_unfused, fused,
+                               stream));
     if (rc) return rc;
     ++launches;
     if (p->record_events) {
         if ((rc = cuda_rc(cudaEventRecord(p->ev1[ev_slot], stream)))) return rc;
         ++p->ev_recorded;
     }
+    if (rs && !rs->fused) {
+        // the collective step after the GEMM: P (in C) -> the send buffers and out
+        RsArgs ra;
+        std::memset(&ra, 0, sizeof ra);
+        ra.P = static_cast<const uint16_t*>(C);
+        for (int j = 0; j < p->rs_R; ++j) {
+            if (j == p->rs_rank) continue;
+            ra.recv[j] = static_cast<const uint16_t*>(rs->recv[j]);
+            ra.send[j] = static_cast<uint16_t*>(rs->send[j]);
+        }
+        ra.out = static_cast<uint16_t*>(rs->out);
+        ra.R = p->rs_R;
+        ra.rank = p->rs_rank;
+        ra.rows = (int)p->rs_rows;
+        ra.N = (int)p->N;
+        if ((rc = cuda_rc(launch_rs_reduce(ra, stream)))) return rc;
+        ++launches;
+    }
     p->last_launches = launches;
     return MXA2A_OK;
+}
+
+mxa2a_plan* create_impl(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t commMSize, int buffer_num,
+                        int kind, int nseg, int64_t seg_rows, bool staging = true) {
+    int dev = 0, major = 0, minor = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        g_last_error = MXA2A_ERR_CUDA;
+        return nullptr;
+    }
+    if (major != 10 || minor != 3) {
+        g_last_error = MXA2A_ERR_UNSUPPORTED_DEVICE;
+        return nullptr;
+    }
+    mxa2a_plan* p = new (std::nothrow) mxa2a_plan();
+    if (!p) {
+        g_last_error = MXA2A_ERR_CUDA;
+        return nullptr;
+    }
+    p->R = R;
+    p->kind = kind;
+    p->nseg = nseg;
+    p->seg_rows = seg_rows;
+    p->M = M;
+    p->ka = kPerRank;
+    p->N = N;
+    p->cm = commMSize;
+    p->bn = buffer_num;
+    p->device = dev;
+    p->sm_count = sms;
+    p->max_pairs_fused = mxgemm_max_pairs(true);
+    p->max_pairs_unfused = mxgemm_max_pairs(false);
+    derive(p);
+    // workspace: ring | sfa | sfb | packed A | flags | status (split-K partials separately)
+    // (a plan that reads A in place only has no ring and no packed A)
+    p->ring_bytes = staging ? (size_t)buffer_num * R * commMSize * kPerRank : 0;
+    p->sfa_bytes = (size_t)(p->K / BK) * p->Mg * kSfAtomBytes;
+    p->sfb_bytes = (size_t)(p->K / BK) * p->Ng2 * kSfAtomBytes;
+    p->apacked_bytes = staging ? (size_t)M * p->K : 0;
+    p->flags_bytes = FlagLayout::words(buffer_num, R) * sizeof(unsigned long long);
+    size_t off = 0;
+    const size_t o_ring = off; off = align_up(off + p->ring_bytes, 1024);
+    const size_t o_sfa = off; off = align_up(off + p->sfa_bytes, 1024);
+    const size_t o_sfb = off; off = align_up(off + p->sfb_bytes, 1024);
+    const size_t o_ap = off; off = align_up(off + p->apacked_bytes, 1024);
+    const size_t o_flags = off; off = align_up(off + p->flags_bytes, 1024);
+    const size_t o_status = off; off = align_up(off + sizeof(DevStatus), 1024);
+    const size_t o_maps = off; off = align_up(off + sizeof(CUtensorMap) * 2 * kMaxSegments, 1024);
+    // reduce-scatter tile counts, for either tile width (the narrow tile has 2 Nt columns of tiles)
+    p->rs_cnt_bytes = kind == MXA2A_KIND_REDUCE_SCATTER ? (size_t)p->Mt * 2 * p->Nt * sizeof(unsigned long long) : 0;
+    const size_t o_rs = off; off = align_up(off + p->rs_cnt_bytes, 1024);
+    p->ws_bytes = off;
+    if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        delete p;
+        g_last_error = MXA2A_ERR_CUDA;
+        return nullptr;
+    }
+    p->ring = p->ws + o_ring;
+    p->sfa = p->ws + o_sfa;
+    p->sfb = p->ws + o_sfb;
+    p->a_packed = p->ws + o_ap;
+    p->flags = reinterpret_cast<unsigned long long*>(p->ws + o_flags);
+    p->status = reinterpret_cast<DevStatus*>(p->ws + o_status);
+    p->seg_maps_dev = reinterpret_cast<CUtensorMap*>(p->ws + o_maps);
+    p->send_maps_dev = p->seg_maps_dev + kMaxSegments;
+    p->rs_cnt = p->rs_cnt_bytes ? reinterpret_cast<unsigned long long*>(p->ws + o_rs) : nullptr;
+    bool ok = cudaMemset(p->ws + o_sfa, 0, p->sfa_bytes) == cudaSuccess &&
+              cudaMemset(p->flags, 0, p->flags_bytes) == cudaSuccess &&
+              cudaMemset(p->status, 0, sizeof(DevStatus)) == cudaSuccess &&
+              (!p->rs_cnt_bytes || cudaMemset(p->rs_cnt, 0, p->rs_cnt_bytes) == cudaSuccess) &&
+              ensure_partials(p) == MXA2A_OK;
+    if (staging) {
+        ok = ok && encode_2d(&p->tmap_ring, p->ring, (uint64_t)kPerRank, (uint64_t)buffer_num * R * commMSize,
+                             (uint32_t)p->box_m);
+        ok = ok && encode_2d(&p->tmap_apacked, p->a_packed, (uint64_t)p->K, (uint64_t)M, BM);
+    } else {
+        std::memset(&p->tmap_ring, 0, sizeof(CUtensorMap));      // never used: A is read in place
+        std::memset(&p->tmap_apacked, 0, sizeof(CUtensorMap));
+    }
+    if (!ok || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        mxa2a_destroy(p);
+        g_last_error = MXA2A_ERR_CUDA;
+        return nullptr;
+    }
+    g_last_error = MXA2A_OK;
+    return p;
 }
 
 }  // namespace
@@ -440,82 +612,102 @@ int mxa2a_validate(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t commMS
 int mxa2a_last_error(void) { return g_last_error; }
 
 mxa2a_plan* mxa2a_create(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t commMSize, int buffer_num) {
-    int rc = mxa2a_validate(R, M, kPerRank, N, commMSize, buffer_num);
+    const int rc = mxa2a_validate(R, M, kPerRank, N, commMSize, buffer_num);
     if (rc) {
         g_last_error = rc;
         return nullptr;
     }
-    int dev = 0, major = 0, minor = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-        g_last_error = MXA2A_ERR_CUDA;
+    return create_impl(R, M, kPerRank, N, commMSize, buffer_num, MXA2A_KIND_ALLTOALL, R, 0);
+}
+
+int mxa2a_validate_allgather(int R, int64_t rowsPerRank, int64_t K, int64_t N, int64_t commMSize, int buffer_num) {
+    if (R < 1 || R > kMaxSegments || rowsPerRank < 1 || commMSize < 1) return MXA2A_ERR_INVALID_SHAPE;
+    if (rowsPerRank % commMSize || (int64_t)R * rowsPerRank > (int64_t(1) << 20)) return MXA2A_ERR_INVALID_SHAPE;
+    return mxa2a_validate(1, (int64_t)R * rowsPerRank, K, N, commMSize, buffer_num);
+}
+
+int mxa2a_validate_reduce_scatter(int R, int rank, int64_t M, int64_t K, int64_t N) {
+    if (R < 1 || R > kMaxSegments || rank < 0 || rank >= R) return MXA2A_ERR_INVALID_SHAPE;
+    if (M < 64 * (int64_t)R || M % (64 * (int64_t)R)) return MXA2A_ERR_INVALID_SHAPE;
+    return mxa2a_validate(1, M, K, N, 64, 2);
+}
+
+mxa2a_plan* mxa2a_create_reduce_scatter(int R, int rank, int64_t M, int64_t K, int64_t N) {
+    const int rc = mxa2a_validate_reduce_scatter(R, rank, M, K, N);
+    if (rc) {
+        g_last_error = rc;
         return nullptr;
     }
-    if (major != 10 || minor != 3) {
-        g_last_error = MXA2A_ERR_UNSUPPORTED_DEVICE;
-        return nullptr;
+    // one K slice, A read in place (no staging ring, no packed A)
+    mxa2a_plan* p = create_impl(1, M, K, N, 64, 2, MXA2A_KIND_REDUCE_SCATTER, 1, 0, false);
+    if (p) {
+        p->rs_rank = rank;
+        p->rs_R = R;
+        p->rs_rows = M / R;
     }
-    mxa2a_plan* p = new (std::nothrow) mxa2a_plan();
-    if (!p) {
-        g_last_error = MXA2A_ERR_CUDA;
-        return nullptr;
-    }
-    p->R = R;
-    p->M = M;
-    p->ka = kPerRank;
-    p->N = N;
-    p->cm = commMSize;
-    p->bn = buffer_num;
-    p->device = dev;
-    p->sm_count = sms;
-    p->max_pairs_fused = mxgemm_max_pairs(true);
-    p->max_pairs_unfused = mxgemm_max_pairs(false);
-    derive(p);
-    // workspace: ring | sfa | sfb | packed A | flags | status (split-K partials separately)
-    p->ring_bytes = (size_t)buffer_num * R * commMSize * kPerRank;
-    p->sfa_bytes = (size_t)(p->K / BK) * p->Mg * kSfAtomBytes;
-    p->sfb_bytes = (size_t)(p->K / BK) * p->Ng2 * kSfAtomBytes;
-    p->apacked_bytes = (size_t)M * p->K;
-    p->flags_bytes = FlagLayout::words(buffer_num, R) * sizeof(unsigned long long);
-    size_t off = 0;
-    const size_t o_ring = off; off = align_up(off + p->ring_bytes, 1024);
-    const size_t o_sfa = off; off = align_up(off + p->sfa_bytes, 1024);
-    const size_t o_sfb = off; off = align_up(off + p->sfb_bytes, 1024);
-    const size_t o_ap = off; off = align_up(off + p->apacked_bytes, 1024);
-    const size_t o_flags = off; off = align_up(off + p->flags_bytes, 1024);
-    const size_t o_status = off; off = align_up(off + sizeof(DevStatus), 1024);
-    const size_t o_maps = off; off = align_up(off + sizeof(CUtensorMap) * kMaxSegments, 1024);
-    p->ws_bytes = off;
-    if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
-        cudaGetLastError();
-        delete p;
-        g_last_error = MXA2A_ERR_CUDA;
-        return nullptr;
-    }
-    p->ring = p->ws + o_ring;
-    p->sfa = p->ws + o_sfa;
-    p->sfb = p->ws + o_sfb;
-    p->a_packed = p->ws + o_ap;
-    p->flags = reinterpret_cast<unsigned long long*>(p->ws + o_flags);
-    p->status = reinterpret_cast<DevStatus*>(p->ws + o_status);
-    p->seg_maps_dev = reinterpret_cast<CUtensorMap*>(p->ws + o_maps);
-    bool ok = cudaMemset(p->ws + o_sfa, 0, p->sfa_bytes) == cudaSuccess &&
-              cudaMemset(p->flags, 0, p->flags_bytes) == cudaSuccess &&
-              cudaMemset(p->status, 0, sizeof(DevStatus)) == cudaSuccess &&
-              ensure_partials(p) == MXA2A_OK;
-    ok = ok && encode_2d(&p->tmap_ring, p->ring, (uint64_t)kPerRank, (uint64_t)buffer_num * R * commMSize,
-                         (uint32_t)p->box_m);
-    ok = ok && encode_2d(&p->tmap_apacked, p->a_packed, (uint64_t)p->K, (uint64_t)M, BM);
-    if (!ok || cudaDeviceSynchronize() != cudaSuccess) {
-        cudaGetLastError();
-        mxa2a_destroy(p);
-        g_last_error = MXA2A_ERR_CUDA;
-        return nullptr;
-    }
-    g_last_error = MXA2A_OK;
     return p;
+}
+
+namespace {
+int run_rs(mxa2a_plan* p, const void* A, const void* A_sf, const void* B, const void* B_sf, const void* const* recv,
+           void* const* send, void* out, void* stream, bool fused) {
+    if (!p || !recv || !send || !out) return MXA2A_ERR_NULL_PTR;
+    if (p->kind != MXA2A_KIND_REDUCE_SCATTER) return MXA2A_ERR_INVALID_OPTION;
+    for (int j = 0; j < p->rs_R; ++j) {
+        if (j == p->rs_rank) continue;
+        if (!recv[j] || !send[j]) return MXA2A_ERR_NULL_PTR;
+        if (!aligned(recv[j], 16) || !aligned(send[j], 16)) return MXA2A_ERR_MISALIGNED;
+    }
+    if (!aligned(out, 16)) return MXA2A_ERR_MISALIGNED;
+    void* C = out;
+    if (!fused) {
+        int rc = check_device(p);
+        if (rc) return rc;
+        if (!p->rs_scratch) {
+            if (cudaMalloc(&p->rs_scratch, (size_t)p->M * p->N * 2) != cudaSuccess) {
+                cudaGetLastError();
+                p->rs_scratch = nullptr;
+                return MXA2A_ERR_CUDA;
+            }
+        }
+        C = p->rs_scratch;
+    }
+    const RsRun rs{fused, recv, send, out};
+    const void* a_seg[1] = {A};
+    const void* a_sf[1] = {A_sf};
+    return run_impl(p, a_seg, a_sf, B, B_sf, C, stream, kRunDirect, &rs);
+}
+}  // namespace
+
+int mxa2a_run_reduce_scatter(mxa2a_plan* p, const void* A, const void* A_sf, const void* B, const void* B_sf,
+                             const void* const* recv, void* const* send, void* out, void* stream) {
+    return run_rs(p, A, A_sf, B, B_sf, recv, send, out, stream, true);
+}
+
+int mxa2a_run_reduce_scatter_unfused(mxa2a_plan* p, const void* A, const void* A_sf, const void* B,
+                                     const void* B_sf, const void* const* recv, void* const* send, void* out,
+                                     void* stream) {
+    return run_rs(p, A, A_sf, B, B_sf, recv, send, out, stream, false);
+}
+
+mxa2a_plan* mxa2a_create_allgather(int R, int64_t rowsPerRank, int64_t K, int64_t N, int64_t commMSize,
+                                   int buffer_num) {
+    const int rc = mxa2a_validate_allgather(R, rowsPerRank, K, N, commMSize, buffer_num);
+    if (rc) {
+        g_last_error = rc;
+        return nullptr;
+    }
+    // The staging ring carries K slices of the gathered rows, as it carries the
+    // all-to-all's segments: credits per (slot, slice) let a slice of the next
+    // step land while other slices of the slot are still being read.  Slices
+    // of about 1024 columns (at least 8 K blocks each), at most 64.
+    const int64_t kb = K / BK;
+    int slices = 1;
+    for (int64_t d = 1; d <= std::min<int64_t>(kMaxSegments, kb / 8); ++d)
+        if (kb % d == 0) slices = (int)d;
+    // the copy role and the pack pick the input block by row and the columns by slice
+    return create_impl(slices, (int64_t)R * rowsPerRank, K / slices, N, commMSize, buffer_num,
+                       MXA2A_KIND_ALLGATHER, R, rowsPerRank);
 }
 
 int mxa2a_run(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, const void* B, const void* B_sf,
@@ -536,14 +728,16 @@ int mxa2a_run_direct(mxa2a_plan* p, const void* const* A_seg, const void* const*
 int mxa2a_run_host(mxa2a_plan* p, const void* const* A_seg_h, const void* const* A_sf_h, const void* B_h,
                    const void* B_sf_h, void* C_h, void* stream_v) {
     if (!p || !A_seg_h || !A_sf_h || !B_h || !B_sf_h || !C_h) return MXA2A_ERR_NULL_PTR;
-    for (int r = 0; r < p->R; ++r)
+    for (int r = 0; r < p->nseg; ++r)
         if (!A_seg_h[r] || !A_sf_h[r]) return MXA2A_ERR_NULL_PTR;
     int rc = check_device(p);
     if (rc) return rc;
-    const size_t a_b = (size_t)p->M * p->ka, asf_b = (size_t)p->M * (p->ka / 32);
+    const size_t seg_m = p->seg_rows ? (size_t)p->seg_rows : (size_t)p->M;
+    const size_t seg_k = p->seg_rows ? (size_t)p->K : (size_t)p->ka;
+    const size_t a_b = seg_m * seg_k, asf_b = seg_m * (seg_k / 32);
     const size_t b_b = (size_t)p->N * p->K, bsf_b = (size_t)p->N * (p->K / 32), c_b = (size_t)p->M * p->N * 2;
     const size_t a_s = align_up(a_b, 256), asf_s = align_up(asf_b, 256);
-    const size_t need = p->R * (a_s + asf_s) + align_up(b_b, 256) + align_up(bsf_b, 256) + align_up(c_b, 256);
+    const size_t need = p->nseg * (a_s + asf_s) + align_up(b_b, 256) + align_up(bsf_b, 256) + align_up(c_b, 256);
     if (p->io_bytes < need) {
         if (p->io) cudaFree(p->io);
         p->io = nullptr;
@@ -560,7 +754,7 @@ int mxa2a_run_host(mxa2a_plan* p, const void* const* A_seg_h, const void* const*
     const void* dA[kMaxSegments];
     const void* dS[kMaxSegments];
     uint8_t* cur = p->io;
-    for (int r = 0; r < p->R; ++r) {
+    for (int r = 0; r < p->nseg; ++r) {
         dA[r] = cur;
         if (cudaMemcpyAsync(cur, A_seg_h[r], a_b, cudaMemcpyHostToDevice, s) != cudaSuccess) return MXA2A_ERR_CUDA;
         cur += a_s;
@@ -722,6 +916,7 @@ int mxa2a_get_option(mxa2a_plan* p, int key, int64_t* v) {
         case MXA2A_INFO_NTILES: *v = p->Nt_fused; break;
         case MXA2A_INFO_TILE_N_FUSED: *v = p->tn_fused; break;
         case MXA2A_INFO_TILE_N_UNFUSED: *v = p->tn_unfused; break;
+        case MXA2A_INFO_KIND: *v = p->kind; break;
         case MXA2A_INFO_SPLITS: *v = p->S_fused; break;
         case MXA2A_INFO_ITEMS: *v = p->W_fused; break;
         case MXA2A_INFO_SPLITS_UNFUSED: *v = p->S_unfused; break;
@@ -795,6 +990,7 @@ void mxa2a_destroy(mxa2a_plan* p) {
     if (p->ws) cudaFree(p->ws);
     if (p->split_ws) cudaFree(p->split_ws);
     if (p->io) cudaFree(p->io);
+    if (p->rs_scratch) cudaFree(p->rs_scratch);
     for (int i = 0; i < p->ev_count; ++i) {
         cudaEventDestroy(p->ev0[i]);
         cudaEventDestroy(p->ev1[i]);

@@ -141,6 +141,8 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int w) {
     const int ntl = rem / (gm * p.S);
     const int rem2 = rem - ntl * (gm * p.S);
     it.mt = g * p.group_m + rem2 / p.S;
+    // GEMM + ReduceScatter: start at the m-tile of this rank's first row
+    if (p.rs_rows > 0 && !p.pair) it.mt = (it.mt + (p.rs_rank * p.rs_rows) / BM) % p.Mt;
     it.q = rem2 % p.S;
     it.nt = (p.zigzag && (g & 1)) ? (p.Nt - 1 - ntl) : ntl;
     it.seg_lo = it.q * p.R / p.S;
@@ -372,8 +374,10 @@ __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const
                         tma_load_2d_hint(a_dst + (size_t)b * p.box_m * BK, tma, bar, kx, ring_row, pol_stream);
                     }
                 } else if (p.direct) {
-                    // the A tile straight from segment r (no exchange, no pack)
-                    tma_load_2d_hint(a_dst, p.seg_maps + r, bar, kx, mt * BM, pol_stream);
+                    // the A tile straight from segment r (no exchange, no pack); all-gather:
+                    // from the input block holding the tile (seg_rows is a multiple of BM)
+                    const SegRow src = seg_row(p, r, mt * BM);
+                    tma_load_2d_hint(a_dst, p.seg_maps + src.seg, bar, seg_col0(p, r) + kx, src.row, pol_stream);
                 } else {
                     tma_load_2d_hint(a_dst, tma, bar, kg, mt * BM, pol_stream);
                 }
@@ -530,7 +534,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bi
 // written.  Lane 0 owns the bulk group: before the buffer is rewritten its
 // previous store must have finished reading it.
 __device__ __forceinline__ void store_c_chunk(const GemmParams& p, const CUtensorMap* tmc, uint8_t* buf, int lane,
-                                              const uint32_t* w, int x, int y) {
+                                              const uint32_t* w, int x, int y, int ylim) {
     if (lane == 0) bulk_wait_read_all();
     __syncwarp();
 #pragma unroll
@@ -540,9 +544,19 @@ __device__ __forceinline__ void store_c_chunk(const GemmParams& p, const CUtenso
     }
     fence_proxy_async_shared();   // the generic-proxy writes, before the TMA (async proxy) reads them
     __syncwarp();
-    if (lane == 0 && x < p.N && y < p.M) {
+    if (lane == 0 && x < p.N && y < ylim) {
         tma_store_2d_hint(tmc, buf, x, y, l2_policy_evict_first());   // C is written once: do not keep it in L2
         bulk_commit_group();
+    }
+}
+
+// fp32 sum of 8 BF16 values (one 16-byte vector, column order) into acc
+__device__ __forceinline__ void add_bf16x8(float* acc, const uint4& t) {
+    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        acc[2 * e] += __uint_as_float(w[e] << 16);
+        acc[2 * e + 1] += __uint_as_float(w[e] & 0xffff0000u);
     }
 }
 
@@ -552,7 +566,7 @@ __device__ __forceinline__ void wait_value_u64(const GemmParams& p, SmemCtl* ctl
     if (!wait_counter(p, ctl, ptr, want, kRoleEpi, -1, -1, -1)) *ok = false;
 }
 
-template <bool kPair, int kBN>
+template <bool kFused, bool kPair, int kBN>
 __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, int warp, int lane, uint32_t rank,
                               const CUtensorMap* tmc, uint8_t* sEpi) {
     using L = Lay<kPair, kBN>;
@@ -604,8 +618,32 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
             tc_fence_before();
             mbar_arrive(&ctl->acc_empty[buf]);   // this accumulator may now take a later item
             if (leader) TRACE(7, w, 0);
+            // C; or (GEMM + ReduceScatter) block j of the rows (rs_rows, a multiple of 64,
+            // so one block holds the warp's 32) to peer j's send buffer, this rank's
+            // block to out; rows past M are not stored
+            const CUtensorMap* dst = tmc;
+            int y = row_w, ylim = p.M;
+            const bool rs = !kFused && p.rs_rows > 0;   // (the staging kernel never reduce-scatters)
+            if (rs) {
+                const int blk = row_w < p.M ? row_w / p.rs_rows : -1;
+                dst = (blk >= 0 && blk != p.rs_rank) ? p.send_maps + blk : tmc;
+                y = blk >= 0 ? row_w - blk * p.rs_rows : 0;
+                ylim = blk >= 0 ? p.rs_rows : 0;
+            }
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) store_c_chunk(p, tmc, cbuf, lane, packed + c * 16, col0 + c * 32, row_w);
+            for (int c = 0; c < kChunks; ++c)
+                store_c_chunk(p, dst, cbuf, lane, packed + c * 16, col0 + c * 32, y, ylim);
+            if (rs && mt * BM < (p.rs_rank + 1) * p.rs_rows && (mt + 1) * BM > p.rs_rank * p.rs_rows) {
+                // a tile with rows of this rank's block: once this warp's stores have
+                // landed, count it for the copy warps that sum those rows
+                if (lane == 0) {
+                    bulk_wait_all();
+                    fence_proxy_async_global();
+                    fence_acq_rel_gpu();
+                    red_relaxed_add_u64(p.rs_cnt + (size_t)mt * p.Nt + item.nt, 1ull);
+                }
+                __syncwarp();
+            }
         } else {
             const size_t tile = (size_t)mt * p.Nt + item.nt;
             if (leader) ctl->ticket = (int)atomicAdd(&p.tile_cnt[tile], 1u);
@@ -679,7 +717,7 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
                             wds[j] = pack_bf16x2(__float_as_uint(acc[2 * j]), __float_as_uint(acc[2 * j + 1]));
-                        store_c_chunk(p, tmc, cbuf, lane, wds, col0 + c * 32, row_w);
+                        store_c_chunk(p, tmc, cbuf, lane, wds, col0 + c * 32, row_w, p.M);
                     }
                 }
                 tc_fence_before();
@@ -710,6 +748,107 @@ __device__ __forceinline__ void copy_bytes(const uint8_t* src, uint8_t* dst, lon
             const long long i = base + (long long)u * 32;
             if (i < n16) d[i] = v[u];
         }
+    }
+}
+
+// One warp copies nrows rows of row_bytes (a multiple of 16) from rows
+// src_ld bytes apart into consecutive rows: 8 loads of 16 bytes in flight
+// per lane, then the stores.
+__device__ __forceinline__ void copy_rows(const uint8_t* src, int src_ld, uint8_t* dst, int row_bytes, int nrows,
+                                          int lane) {
+    constexpr int U = 8;
+    const int vpr = row_bytes >> 4;
+    const int n16 = nrows * vpr;
+    uint4* d = reinterpret_cast<uint4*>(dst);
+    for (int base = lane; base < n16; base += 32 * U) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u * 32;
+            if (i < n16) {
+                const int row = i / vpr;
+                v[u] = ld_nc_v4(src + (size_t)row * src_ld + (size_t)(i - row * vpr) * 16);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u * 32;
+            if (i < n16) d[i] = v[u];
+        }
+    }
+}
+
+// GEMM + ReduceScatter, this rank's rows: the copy warps (idle otherwise in
+// the kernel without staging) claim tasks of 8 rows of out x one n-tile, wait
+// until the 8 epilogue warps of the tile that computed them have stored this
+// rank's BF16 partial there, and replace it by the sum over ranks j = 0..R-1
+// of block `rank` of rank j's partial (the stored value for j == rank,
+// recv[j] otherwise): fp32 adds in that order from 0, one rounding to BF16.
+__device__ void rs_reduce_role(const GemmParams& p, SmemCtl* ctl, int lane) {
+    constexpr int kRows = 8, U = 2, Q = 4;   // rows per task; rows and ranks loaded at once
+    const int n_tasks = (p.rs_rows / kRows) * p.Nt;
+    const int vpr = p.tile_n / 8;            // 16-byte vectors in a tile row: one per lane
+    unsigned long long* next = p.flags + FlagLayout::copy_next(p.bn, p.R);
+    uint16_t* out = p.C;
+    for (;;) {
+        int t = -1;
+        if (lane == 0 && !ctl->abort) {
+            t = (int)atomicAdd(next, 1ull);
+            if (t >= n_tasks) t = -1;
+        }
+        t = __shfl_sync(0xffffffffu, t, 0);
+        if (t < 0) return;   // uniform over the warp
+        const int g = t / p.Nt;
+        const int nt = t - g * p.Nt;
+        const int lr0 = g * kRows;                            // first row inside the block
+        const int mt = (p.rs_rank * p.rs_rows + lr0) / BM;    // the m-tile that computed them
+        int ok = 1;
+        if (lane == 0)
+            ok = wait_counter(p, ctl, p.rs_cnt + (size_t)mt * p.Nt + nt, (unsigned long long)kEpiWarps,
+                              kRoleReduce, mt, nt, -1) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) return;
+        const int col = nt * p.tile_n + lane * 8;
+        if (lane < vpr && col < p.N) {   // N % 8 == 0: a vector is all inside N or all past it
+#pragma unroll 1
+            for (int r0 = 0; r0 < kRows; r0 += U) {
+                float acc[U][8];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[u][e] = 0.0f;
+                for (int q0 = 0; q0 < p.rs_R; q0 += Q) {
+                    uint4 tv[U][Q];
+#pragma unroll
+                    for (int qq = 0; qq < Q; ++qq)
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            const int q = q0 + qq;
+                            const size_t off = (size_t)(lr0 + r0 + u) * p.N + col;
+                            tv[u][qq] = make_uint4(0u, 0u, 0u, 0u);
+                            if (q == p.rs_rank)
+                                tv[u][qq] = ld_cg_v4(out + off);
+                            else if (q < p.rs_R)
+                                tv[u][qq] = ld_nc_v4(p.recv[q] + off);
+                        }
+#pragma unroll
+                    for (int qq = 0; qq < Q; ++qq)
+#pragma unroll
+                        for (int u = 0; u < U; ++u)
+                            if (q0 + qq < p.rs_R) add_bf16x8(acc[u], tv[u][qq]);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        o[e] = pack_bf16x2(__float_as_uint(acc[u][2 * e]), __float_as_uint(acc[u][2 * e + 1]));
+                    *reinterpret_cast<uint4*>(out + (size_t)(lr0 + r0 + u) * p.N + col) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            }
+        }
+        __syncwarp();
     }
 }
 
@@ -758,7 +897,6 @@ __device__ __forceinline__ bool copy_task_ready(const GemmParams& p, int t, int 
 __device__ void copy_role(const GemmParams& p, SmemCtl* ctl, int lane) {
     const int per_step = p.R * p.chunks_per_seg;
     const long long chunk_bytes = (long long)p.rows_per_chunk * p.ka;
-    const int sf_cols = p.ka / 32;
     unsigned long long* next = p.flags + FlagLayout::copy_next(p.bn, p.R);
     for (;;) {
         int chosen = -1;
@@ -809,16 +947,21 @@ __device__ void copy_role(const GemmParams& p, SmemCtl* ctl, int lane) {
         const int c = rem - r * p.chunks_per_seg;
         const int slot = s % p.bn;
         const int row0 = s * p.cm + c * p.rows_per_chunk;
-        copy_bytes(p.A_seg[r] + (size_t)row0 * p.ka,
-                   p.ring + ((size_t)(slot * p.R + r) * p.cm + (size_t)c * p.rows_per_chunk) * p.ka, chunk_bytes,
-                   lane);
+        const SegRow src = seg_row(p, r, row0);   // a chunk never straddles two input blocks
+        const int ld = seg_ld(p), col0 = seg_col0(p, r);
+        uint8_t* dst = p.ring + ((size_t)(slot * p.R + r) * p.cm + (size_t)c * p.rows_per_chunk) * p.ka;
+        if (ld == p.ka)   // the rows of a segment are contiguous
+            copy_bytes(p.A_seg[src.seg] + (size_t)src.row * p.ka, dst, chunk_bytes, lane);
+        else              // all-gather: K slice r of full rows
+            copy_rows(p.A_seg[src.seg] + (size_t)src.row * ld + col0, ld, dst, p.ka, p.rows_per_chunk, lane);
         // scales of these rows: one u32 (4 E8M0 bytes = one 128-K block) per
         // (row, K block), placed at (row%32)*4 + (row%128)/32 of the block's atom
         const int nsf = p.rows_per_chunk * p.kb_per_seg;
         for (int i = lane; i < nsf; i += 32) {
             const int kb = i / p.rows_per_chunk;
             const int m = row0 + (i - kb * p.rows_per_chunk);
-            const uint32_t v = ld_nc_u32(p.A_sf_seg[r] + (size_t)m * sf_cols + kb * 4);
+            const uint32_t v = ld_nc_u32(p.A_sf_seg[src.seg] + (size_t)(src.row + (m - row0)) * (ld / 32) +
+                                         col0 / 32 + kb * 4);
             const int kbg = r * p.kb_per_seg + kb;
             uint32_t* atom = reinterpret_cast<uint32_t*>(p.sfa_stage + ((size_t)kbg * p.Mg + m / BM) * kSfAtomBytes);
             atom[(m & 31) * 4 + ((m & 127) >> 5)] = v;
@@ -868,7 +1011,12 @@ __device__ void pack_sfa_slice(const GemmParams& p) {
         const int kbg = (int)(i / rows);
         const int r = kbg / p.kb_per_seg;
         const int kb = kbg - r * p.kb_per_seg;
-        const uint32_t v = m < p.M ? ld_nc_u32(p.A_sf_seg[r] + (size_t)m * (p.ka / 32) + (size_t)kb * 4) : 0u;
+        uint32_t v = 0u;
+        if (m < p.M) {
+            const SegRow src = seg_row(p, r, m);
+            v = ld_nc_u32(p.A_sf_seg[src.seg] + (size_t)src.row * (seg_ld(p) / 32) + seg_col0(p, r) / 32 +
+                          (size_t)kb * 4);
+        }
         sfa[((size_t)kbg * p.Mg + (size_t)(m >> 7)) * (kSfAtomBytes / 4) + (size_t)((m & 31) * 4 + ((m & 127) >> 5))] = v;
     }
 }
@@ -955,11 +1103,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < kWarpCopy0) {
         if (!p.exchange_only) {
-            epilogue_role<kPair, kBN>(p, tmem, ctl, warp, lane, rank, &tmap_c, smem + L::Epi);
+            epilogue_role<kFused, kPair, kBN>(p, tmem, ctl, warp, lane, rank, &tmap_c, smem + L::Epi);
             if (lane == 0) bulk_wait_all();   // this warp's C stores are complete before the CTA ends
         }
     } else if (kFused && is_copy_warp(warp)) {
         copy_role(p, ctl, lane);
+    } else if (!kFused && p.rs_rows > 0 && is_copy_warp(warp)) {
+        rs_reduce_role(p, ctl, lane);
     }
     __syncwarp();
     __syncthreads();
@@ -1012,6 +1162,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (p.sfb_inline || p.direct) atomicExch(p.flags + FlagLayout::sfb_done(p.bn, p.R), 0ull);
+            if (!kFused && p.rs_rows > 0) {   // the reduce-scatter task counter and tile counts
+                atomicExch(p.flags + FlagLayout::copy_next(p.bn, p.R), 0ull);
+                for (int t = 0; t < p.Mt * p.Nt; ++t) p.rs_cnt[t] = 0ull;
+            }
             if (p.S > 1 && launch_failed(p))
                 for (int t = 0; t < p.Mt * p.Nt; ++t) atomicExch(&p.tile_cnt[t], 0u);
             atomicExch(done, 0ull);

@@ -174,6 +174,15 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
                  : "l"(p));
     return v;
 }
+// 16-byte load of data written earlier in this launch by another SM (at L2, not L1)
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
 __device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
     uint32_t v;
     asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));

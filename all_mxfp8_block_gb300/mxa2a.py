@@ -63,6 +63,11 @@ MXA2A_INFO_GROUP_FUSED = 115
 MXA2A_INFO_GROUP_UNFUSED = 116
 MXA2A_INFO_TILE_N_FUSED = 117
 MXA2A_INFO_TILE_N_UNFUSED = 118
+MXA2A_INFO_KIND = 119
+
+MXA2A_KIND_ALLTOALL = 0
+MXA2A_KIND_ALLGATHER = 1
+MXA2A_KIND_REDUCE_SCATTER = 2
 
 MXA2A_WS_RING = 1
 MXA2A_WS_SFA = 2
@@ -93,6 +98,12 @@ _SIGS = [
     ("mxa2a_validate", ctypes.c_int, [ctypes.c_int, _I64, _I64, _I64, _I64, ctypes.c_int]),
     ("mxa2a_create", _VP, [ctypes.c_int, _I64, _I64, _I64, _I64, ctypes.c_int]),
     ("mxa2a_last_error", ctypes.c_int, []),
+    ("mxa2a_validate_allgather", ctypes.c_int, [ctypes.c_int, _I64, _I64, _I64, _I64, ctypes.c_int]),
+    ("mxa2a_create_allgather", _VP, [ctypes.c_int, _I64, _I64, _I64, _I64, ctypes.c_int]),
+    ("mxa2a_validate_reduce_scatter", ctypes.c_int, [ctypes.c_int, ctypes.c_int, _I64, _I64, _I64]),
+    ("mxa2a_create_reduce_scatter", _VP, [ctypes.c_int, ctypes.c_int, _I64, _I64, _I64]),
+    ("mxa2a_run_reduce_scatter", ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _PP, _PP, _VP, _VP]),
+    ("mxa2a_run_reduce_scatter_unfused", ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _PP, _PP, _VP, _VP]),
     ("mxa2a_run", ctypes.c_int, [_VP, _PP, _PP, _VP, _VP, _VP, _VP]),
     ("mxa2a_run_unfused", ctypes.c_int, [_VP, _PP, _PP, _VP, _VP, _VP, _VP]),
     ("mxa2a_run_direct", ctypes.c_int, [_VP, _PP, _PP, _VP, _VP, _VP, _VP]),
@@ -180,6 +191,41 @@ def mxa2a_create(R, M, kPerRank, N, commMSize, buffer_num) -> int:
 
 def mxa2a_last_error() -> int:
     return load().mxa2a_last_error()
+
+
+def mxa2a_validate_allgather(R, rowsPerRank, K, N, commMSize, buffer_num) -> int:
+    return load().mxa2a_validate_allgather(R, rowsPerRank, K, N, commMSize, buffer_num)
+
+
+def mxa2a_create_allgather(R, rowsPerRank, K, N, commMSize, buffer_num) -> int:
+    h = load().mxa2a_create_allgather(R, rowsPerRank, K, N, commMSize, buffer_num)
+    if not h:
+        raise Mxa2aError(load().mxa2a_last_error(), "mxa2a_create_allgather")
+    return h
+
+
+def mxa2a_validate_reduce_scatter(R, rank, M, K, N) -> int:
+    return load().mxa2a_validate_reduce_scatter(R, rank, M, K, N)
+
+
+def mxa2a_create_reduce_scatter(R, rank, M, K, N) -> int:
+    h = load().mxa2a_create_reduce_scatter(R, rank, M, K, N)
+    if not h:
+        raise Mxa2aError(load().mxa2a_last_error(), "mxa2a_create_reduce_scatter")
+    return h
+
+
+def mxa2a_run_reduce_scatter(plan, A, A_scale, B, B_scale, recv, send, out, stream=None) -> None:
+    rv, sd = _ptr_array(recv), _ptr_array(send)
+    _check(load().mxa2a_run_reduce_scatter(plan, _ptr(A), _ptr(A_scale), _ptr(B), _ptr(B_scale), rv, sd,
+                                           _ptr(out), _stream(stream)), "mxa2a_run_reduce_scatter")
+
+
+def mxa2a_run_reduce_scatter_unfused(plan, A, A_scale, B, B_scale, recv, send, out, stream=None) -> None:
+    rv, sd = _ptr_array(recv), _ptr_array(send)
+    _check(load().mxa2a_run_reduce_scatter_unfused(plan, _ptr(A), _ptr(A_scale), _ptr(B), _ptr(B_scale), rv, sd,
+                                                   _ptr(out), _stream(stream)),
+           "mxa2a_run_reduce_scatter_unfused")
 
 
 def mxa2a_run(plan, A_seg, A_scale_seg, B, B_scale, C_bf16, stream=None) -> None:
@@ -316,3 +362,38 @@ class Plan:
             self.destroy()
         except Exception:
             pass
+
+
+class AllGatherPlan(Plan):
+    """AllGather + GEMM plan (``mxa2a_create_allgather``): the run methods take
+    the R row blocks ``A_blk`` / ``A_scale_blk`` in place of the segments."""
+
+    def __init__(self, R, rowsPerRank, K, N, commMSize, buffer_num):
+        self.shape = (R, rowsPerRank, K, N, commMSize, buffer_num)
+        self.R, self.M, self.K, self.N = R, R * rowsPerRank, K, N
+        self.handle = mxa2a_create_allgather(R, rowsPerRank, K, N, commMSize, buffer_num)
+
+
+class ReduceScatterPlan(Plan):
+    """GEMM + ReduceScatter plan (``mxa2a_create_reduce_scatter``) of rank
+    ``rank`` of ``R``: ``run`` / ``run_unfused`` take this rank's A, B (and
+    scales), the R received partial blocks ``recv`` and the R send buffers
+    ``send`` (entry ``rank`` of each unused) and the output block ``out``."""
+
+    def __init__(self, R, rank, M, K, N):
+        self.shape = (R, rank, M, K, N)
+        self.R, self.rank, self.M, self.K, self.N = R, rank, M, K, N
+        self.rows = M // R
+        self.handle = mxa2a_create_reduce_scatter(R, rank, M, K, N)
+
+    def run(self, A, A_scale, B, B_scale, recv, send, out, stream=None):
+        mxa2a_run_reduce_scatter(self.handle, A, A_scale, B, B_scale, recv, send, out, stream)
+
+    def run_unfused(self, A, A_scale, B, B_scale, recv, send, out, stream=None):
+        mxa2a_run_reduce_scatter_unfused(self.handle, A, A_scale, B, B_scale, recv, send, out, stream)
+
+    def run_direct(self, *a, **k):
+        raise Mxa2aError(MXA2A_ERR_INVALID_OPTION, "a reduce-scatter plan has run and run_unfused only")
+
+    def run_host(self, *a, **k):
+        raise Mxa2aError(MXA2A_ERR_INVALID_OPTION, "a reduce-scatter plan has run and run_unfused only")

@@ -271,6 +271,67 @@ def time_tiny_graph(dev, runs: int = 200):
     return out
 
 
+def time_siblings(dev, stream, flush, flush_bytes, steps, warmup):
+    """Mean ms per call of the sibling operators' fused and unfused paths on
+    their benchmark workloads (AllGather + GEMM: 4 blocks of 512 rows, K = N =
+    4096; GEMM + ReduceScatter: rank 1 of 4, 2048 x 4096 x 4096), each call
+    after an L2 flush, CUDA events around each call."""
+    import torch
+    from all_mxfp8_block_gb300 import inputs, mxa2a
+
+    def timed(call):
+        for _ in range(warmup):
+            mxa2a.mxa2a_l2_flush(flush, flush_bytes, stream)
+            call()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize(dev)
+        for i in range(steps):
+            mxa2a.mxa2a_l2_flush(flush, flush_bytes, stream)
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return sum(a.elapsed_time(b) for a, b in ev) / steps
+
+    bf16_tf, _, _ = measured_peaks()
+    peak = bf16_tf * FP8_OVER_BF16
+    out = {}
+    w = inputs.AG_WORKLOADS[1]
+    x = inputs.make_allgather_inputs(w)
+    A = [a.to(dev) for a in x["A_blk"]]
+    S = [s.to(dev) for s in x["A_scale_blk"]]
+    B, Bs = x["B"].to(dev), x["B_scale"].to(dev)
+    C = torch.empty((w.M, w.N), dtype=torch.int16, device=dev)
+    with mxa2a.AllGatherPlan(w.R, w.rowsPerRank, w.K, w.N, w.commMSize, w.buffer_num) as p:
+        res = {path + "_ms": timed(lambda fn=fn: fn(A, S, B, Bs, C, stream))
+               for path, fn in (("fused", p.run), ("unfused", p.run_unfused), ("direct", p.run_direct))}
+        st = p.status()
+        if st["code"] != 0:
+            raise RuntimeError(f"device status after the all-gather timing: {st}")
+    tf = w.flops / (res["fused_ms"] / 1e3) / 1e12
+    out["allgather_gemm"] = {"workload": w.name, "R": w.R, "rowsPerRank": w.rowsPerRank, "K": w.K, "N": w.N,
+                             "commMSize": w.commMSize, "buffer_num": w.buffer_num, **res, "value": tf,
+                             "unit": UNIT, "roofline_frac": tf / peak, "steps": steps}
+    del A, S, B, Bs, C
+    w = inputs.RS_WORKLOADS[1]
+    x = inputs.make_reduce_scatter_inputs(w)
+    A, S, B, Bs = (x[k].to(dev) for k in ("A", "A_scale", "B", "B_scale"))
+    recv = [None if r is None else r.to(dev) for r in x["recv"]]
+    send = [None if j == w.rank else torch.empty((w.rows, w.N), dtype=torch.int16, device=dev)
+            for j in range(w.R)]
+    o = torch.empty((w.rows, w.N), dtype=torch.int16, device=dev)
+    with mxa2a.ReduceScatterPlan(w.R, w.rank, w.M, w.K, w.N) as p:
+        res = {path + "_ms": timed(lambda fn=fn: fn(A, S, B, Bs, recv, send, o, stream))
+               for path, fn in (("fused", p.run), ("unfused", p.run_unfused))}
+        st = p.status()
+        if st["code"] != 0:
+            raise RuntimeError(f"device status after the reduce-scatter timing: {st}")
+    tf = w.flops / (res["fused_ms"] / 1e3) / 1e12
+    out["gemm_reduce_scatter"] = {"workload": w.name, "R": w.R, "rank": w.rank, "M": w.M, "K": w.K, "N": w.N,
+                                  **res, "value": tf, "unit": UNIT, "roofline_frac": tf / peak, "steps": steps}
+    return out
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -365,6 +426,11 @@ def run_ours(args, w):
         if st["code"] != 0:
             raise RuntimeError(f"device status after the credit ablation: {st}")
 
+    # the sibling fused operators at the headline's size, same caliber
+    siblings = None
+    if not args.no_siblings:
+        siblings = time_siblings(dev, stream, flush, flush_bytes, min(other_steps, 200), args.warmup)
+
     t_local = sum(step_ms) / 1e3
     t_max, flops_total = reduce_max_sum(t_local, float(w.flops) * args.steps, dev if ws > 1 else None)
     value = flops_total / t_max / 1e12
@@ -455,6 +521,7 @@ def run_ours(args, w):
             "value": w.flops / (sum(direct_ms) / len(direct_ms) / 1e3) / 1e12,
             "what": "A read in place from the segments (no staging ring, no pack): the exchange's cost"},
         "credit_ablation": credit_ablation,
+        "siblings": siblings,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": int(args.steps * (1 + launches_per_run)),
@@ -488,6 +555,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph timing of the smallest workload")
     ap.add_argument("--no-ablation", action="store_true", help="skip the staging-protocol ablation timings")
+    ap.add_argument("--no-siblings", action="store_true", help="skip the sibling operators' timings")
     ap.add_argument("--skew-ns", type=int, default=4000, help="copy delay of every 4th CTA in the ablation")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--split", type=int, default=0, help="force the K split of both paths (0 = automatic)")

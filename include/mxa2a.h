@@ -67,7 +67,8 @@ typedef struct mxa2a_plan mxa2a_plan;   /* opaque */
 /* Device-side status of the runs since the previous mxa2a_get_status call. */
 typedef struct mxa2a_status {
     int32_t code;       /* MXA2A_OK, or the first device error of the reported launch */
-    int32_t role;       /* 1 staging copy, 2 TMA producer, 3 MMA issuer, 4 epilogue, 5 exit */
+    int32_t role;       /* 1 staging copy, 2 TMA producer, 3 MMA issuer, 4 epilogue, 5 exit,
+                           6 reduce-scatter sum */
     int32_t block;      /* CTA that reported */
     int32_t step;       /* staging step waited on, -1 if none */
     int32_t segment;    /* segment waited on, -1 if none */
@@ -100,8 +101,90 @@ int mxa2a_validate(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t commMS
  */
 mxa2a_plan *mxa2a_create(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t commMSize, int buffer_num);
 
-/* Error code of the last failed mxa2a_create on this thread. */
+/* Error code of the last failed mxa2a_create* on this thread. */
 int mxa2a_last_error(void);
+
+/* What a plan computes (mxa2a_get_option(MXA2A_INFO_KIND)). */
+enum mxa2a_kind {
+    MXA2A_KIND_ALLTOALL = 0,       /* mxa2a_create: AllToAll + GEMM (above) */
+    MXA2A_KIND_ALLGATHER = 1,      /* mxa2a_create_allgather: AllGather + GEMM */
+    MXA2A_KIND_REDUCE_SCATTER = 2  /* mxa2a_create_reduce_scatter: GEMM + ReduceScatter */
+};
+
+/*
+ * AllGather + GEMM, the first fused-operator case of the performance
+ * optimisation guide (section 3.1, which gives the title only; this is the
+ * plain reading of the name).  R ranks each hold a block of rowsPerRank rows
+ * of A with all K columns; the all-gather stacks the blocks along M =
+ * R * rowsPerRank, and the rank multiplies the gathered A by its own B:
+ *
+ *   C[j*rowsPerRank + i][n] = bf16( sum_{k<K} e4m3(A_blk[j][i][k]) * 2^(A_scale_blk[j][i][k/32] - 127)
+ *                                            * e4m3(B[n][k])       * 2^(B_scale[n][k/32] - 127) )
+ *
+ * On one GPU the R blocks are R device buffers: A_blk[j] uint8 [rowsPerRank][K],
+ * A_scale_blk[j] uint8 [rowsPerRank][K/32].  The plan runs through the
+ * all-to-all plan's calls, which then take A_blk / A_scale_blk (R pointers
+ * each) in place of A_seg / A_scale_seg:
+ *   mxa2a_run          fused: the blocks travel commMSize rows at a time
+ *                      through the buffer_num-slot ring with the same credit
+ *                      protocol, and the GEMM consumes each step as it lands;
+ *   mxa2a_run_unfused  gather into one [M][K] operand, then the GEMM;
+ *   mxa2a_run_direct   the GEMM reads the blocks in place (rowsPerRank % 128
+ *                      == 0, else MXA2A_ERR_INVALID_OPTION);
+ *   mxa2a_run_host     the fused run from host buffers (R blocks).
+ * (mxa2a_run_noalloc computes the all-to-all only.)
+ * There is one K slice, so no K split.  B, B_scale, C, element formats,
+ * alignment, ownership, options and errors as for the all-to-all plan.
+ * Shape rules: 1 <= R <= 64, rowsPerRank % commMSize == 0, and the
+ * all-to-all rules for (R = 1, M = R * rowsPerRank, kPerRank = K, N,
+ * commMSize, buffer_num).  Returns MXA2A_OK or MXA2A_ERR_INVALID_SHAPE.
+ */
+int mxa2a_validate_allgather(int R, int64_t rowsPerRank, int64_t K, int64_t N, int64_t commMSize, int buffer_num);
+mxa2a_plan *mxa2a_create_allgather(int R, int64_t rowsPerRank, int64_t K, int64_t N, int64_t commMSize,
+                                   int buffer_num);
+
+/*
+ * GEMM + ReduceScatter, the second fused-operator case of the performance
+ * optimisation guide (section 3.2, title only; plain reading).  R ranks hold
+ * K-sharded operands; rank `rank` holds A uint8 [M][K] (+ A_scale [M][K/32])
+ * and B uint8 [N][K] (+ B_scale [N][K/32]), computes its partial
+ * P = bf16(A x B^T) ([M][N], the block-scaled product of the all-to-all plan
+ * with one segment) and reduce-scatters it: row block j (Mr = M / R rows) of
+ * every rank's partial goes to rank j, which sums them.  The partials travel
+ * as BF16 (the operation's output type) and are summed in fp32 in rank order
+ * and rounded once to BF16, the arithmetic of a BF16 GEMM followed by a BF16
+ * reduce-scatter.  From this rank's side, on one GPU:
+ *
+ *   send[j][i][n] = P[j*Mr + i][n]                             j != rank
+ *   out[i][n]     = bf16( sum_{j<R} v_j[i][n] )  (fp32, j = 0, 1, .., R-1)
+ *                   v_rank = P[rank*Mr + i][n],  v_j = recv[j][i][n] (j != rank)
+ *
+ * recv[j] is what peer j sent this rank and send[j] what this rank sends peer
+ * j: host arrays of R device pointers to uint16 BF16 [Mr][N] buffers (entry
+ * `rank` unused, may be NULL); out uint16 BF16 [Mr][N].  Alignment: A, B,
+ * out, recv[j], send[j] 16 bytes; scales 4.
+ *   mxa2a_run_reduce_scatter          fused: one persistent GEMM (A and B
+ *       read in place) whose epilogue routes every finished tile, a peer's
+ *       rows to its send buffer and this rank's to out; the kernel's spare
+ *       warps then sum out's rows with the received partials in place, while
+ *       the GEMM goes on with the peers' blocks (this rank's block is
+ *       computed first);
+ *   mxa2a_run_reduce_scatter_unfused  the GEMM writes P into a plan-owned
+ *       [M][N] buffer, then a reduce-scatter kernel copies the peers' blocks
+ *       and sums this rank's.
+ * Both give the same bits.  Shape rules: 1 <= R <= 64, 0 <= rank < R,
+ * M % (64 * R) == 0, K % 128 == 0, N % 16 == 0, M, N, K <= 2^20.  Options as
+ * for the other kinds (no K split).  Returns NULL on error
+ * (mxa2a_last_error).
+ */
+int mxa2a_validate_reduce_scatter(int R, int rank, int64_t M, int64_t K, int64_t N);
+mxa2a_plan *mxa2a_create_reduce_scatter(int R, int rank, int64_t M, int64_t K, int64_t N);
+int mxa2a_run_reduce_scatter(mxa2a_plan *plan, const void *A, const void *A_scale, const void *B,
+                             const void *B_scale, const void *const *recv, void *const *send, void *out_bf16,
+                             void *stream);
+int mxa2a_run_reduce_scatter_unfused(mxa2a_plan *plan, const void *A, const void *A_scale, const void *B,
+                                     const void *B_scale, const void *const *recv, void *const *send,
+                                     void *out_bf16, void *stream);
 
 /*
  * The fused path: one persistent cooperative kernel stages A_seg[r] rows
@@ -218,7 +301,8 @@ enum mxa2a_option {
     MXA2A_INFO_GROUP_FUSED = 115,  /* raster group of the fused path (m rows) */
     MXA2A_INFO_GROUP_UNFUSED = 116, /* raster group of the unfused path (m rows) */
     MXA2A_INFO_TILE_N_FUSED = 117,  /* tile width of the fused path (128 or 256) */
-    MXA2A_INFO_TILE_N_UNFUSED = 118 /* tile width of the unfused path (128 or 256) */
+    MXA2A_INFO_TILE_N_UNFUSED = 118, /* tile width of the unfused path (128 or 256) */
+    MXA2A_INFO_KIND = 119          /* enum mxa2a_kind */
 };
 
 int mxa2a_set_option(mxa2a_plan *plan, int key, int64_t value);

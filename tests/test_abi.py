@@ -91,3 +91,39 @@ def test_null_plan_calls_fail_cleanly(lib):
     assert mxa2a.load().mxa2a_set_option(None, mxa2a.MXA2A_OPT_ZIGZAG, 1) == mxa2a.MXA2A_ERR_NULL_PTR
     assert mxa2a.load().mxa2a_run(None, None, None, None, None, None, None) == mxa2a.MXA2A_ERR_NULL_PTR
     mxa2a.load().mxa2a_destroy(None)
+
+
+def test_validate_allgather_rules(lib):
+    v = mxa2a.mxa2a_validate_allgather
+    ok, bad = mxa2a.MXA2A_OK, mxa2a.MXA2A_ERR_INVALID_SHAPE
+    assert v(4, 512, 4096, 4096, 256, 2) == ok
+    assert v(1, 128, 256, 256, 64, 2) == ok
+    assert v(0, 512, 4096, 4096, 256, 2) == bad          # R >= 1
+    assert v(65, 64, 256, 256, 64, 2) == bad            # R <= 64
+    assert v(4, 320, 4096, 4096, 256, 2) == bad         # rowsPerRank % commMSize
+    assert v(4, 512, 4000, 4096, 256, 2) == bad         # K % 128
+    assert v(4, 512, 4096, 4096, 96, 2) == bad          # commMSize % 64
+    assert v(1 << 10, 1 << 11, 256, 256, 64, 2) == bad  # R > 64 (and M > 2^20)
+    assert v(64, 1 << 15, 256, 256, 64, 2) == bad       # M = R * rowsPerRank > 2^20
+
+
+def test_validate_reduce_scatter_rules(lib):
+    v = mxa2a.mxa2a_validate_reduce_scatter
+    ok, bad = mxa2a.MXA2A_OK, mxa2a.MXA2A_ERR_INVALID_SHAPE
+    assert v(4, 1, 2048, 4096, 4096) == ok
+    assert v(1, 0, 64, 128, 16) == ok
+    assert v(4, 4, 2048, 4096, 4096) == bad             # rank < R
+    assert v(4, -1, 2048, 4096, 4096) == bad            # rank >= 0
+    assert v(4, 0, 2048 + 64, 4096, 4096) == bad        # M % (64 R)
+    assert v(4, 0, 128, 4096, 4096) == bad              # M >= 64 R
+    assert v(4, 0, 2048, 4000, 4096) == bad             # K % 128
+    assert v(4, 0, 2048, 4096, 4008) == bad             # N % 16
+    assert v(65, 0, 65 * 64, 128, 16) == bad            # R <= 64
+
+
+def test_null_sibling_calls_fail_cleanly(lib):
+    L = mxa2a.load()
+    assert L.mxa2a_run_reduce_scatter(None, None, None, None, None, None, None, None, None) == \
+        mxa2a.MXA2A_ERR_NULL_PTR
+    assert L.mxa2a_run_reduce_scatter_unfused(None, None, None, None, None, None, None, None, None) == \
+        mxa2a.MXA2A_ERR_NULL_PTR
