@@ -647,13 +647,12 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
         } else {
             const size_t tile = (size_t)mt * p.Nt + item.nt;
             if (leader) ctl->ticket = (int)atomicAdd(&p.tile_cnt[tile], 1u);
-            named_barrier_sync(2, kEpiThreads);
-            const bool last = ctl->ticket == p.S - 1;
-            // partial tile layout [kBN/4][BM][4]: thread `lrow` of a warp stores the
-            // float4 of columns 4g..4g+3 at (g*BM + lrow)*4, so each warp store
-            // covers 512 contiguous bytes
+            // Every split first writes its fp32 partial and frees the accumulator, so the
+            // next item's MMAs overlap the reduction.  Partial tile layout [kBN/4][BM][4]:
+            // thread `lrow` of a warp stores the float4 of columns 4g..4g+3 at
+            // (g*BM + lrow)*4, so each warp store covers 512 contiguous bytes.
             float* part_tile = p.partial + tile * (size_t)p.S * (BM * kBN);
-            if (!last) {
+            {
                 float* dst = part_tile + (size_t)item.q * (BM * kBN) + ((size_t)(tcol / 4) * BM + lrow) * 4;
 #pragma unroll 1
                 for (int c = 0; c < kChunks; ++c) {
@@ -669,6 +668,10 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
                 }
                 tc_fence_before();
                 mbar_arrive(&ctl->acc_empty[buf]);
+            }
+            named_barrier_sync(2, kEpiThreads);   // (also makes the leader's ticket visible)
+            const bool last = ctl->ticket == p.S - 1;
+            if (!last) {
                 __threadfence();
                 named_barrier_sync(2, kEpiThreads);
                 if (leader)
@@ -685,32 +688,26 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
                 }
                 named_barrier_sync(2, kEpiThreads);
                 const bool ok = ctl->epi_ok != 0;   // uniform over the epilogue warps
+                // M is a multiple of 64, so a warp's 32 rows are all inside M or all past it
+                if (ok && row_w < p.M) {
 #pragma unroll 1
-                for (int c = 0; c < kChunks; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), v);
-                    tc_wait_ld();
-                    // M is a multiple of 64, so a warp's 32 rows are all inside M or all past it
-                    if (ok && row_w < p.M) {
+                    for (int c = 0; c < kChunks; ++c) {
                         // fixed order q = 0..S-1, whichever split finished last
                         float acc[32];
 #pragma unroll
                         for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
                         for (int q = 0; q < p.S; ++q) {
-                            if (q == item.q) {
+                            const float* src =
+                                part_tile + (size_t)q * (BM * kBN) + ((size_t)(tcol / 4 + c * 8) * BM + lrow) * 4;
+                            uint4 t[8];
 #pragma unroll
-                                for (int e = 0; e < 32; ++e) acc[e] += __uint_as_float(v[e]);
-                            } else {
-                                const float* src = part_tile + (size_t)q * (BM * kBN) +
-                                                   ((size_t)(tcol / 4 + c * 8) * BM + lrow) * 4;
+                            for (int j = 0; j < 8; ++j) t[j] = ld_cg_v4(src + (size_t)j * BM * 4);
 #pragma unroll
-                                for (int j = 0; j < 8; ++j) {
-                                    const float4 t = *reinterpret_cast<const float4*>(src + (size_t)j * BM * 4);
-                                    acc[4 * j] += t.x;
-                                    acc[4 * j + 1] += t.y;
-                                    acc[4 * j + 2] += t.z;
-                                    acc[4 * j + 3] += t.w;
-                                }
+                            for (int j = 0; j < 8; ++j) {
+                                acc[4 * j] += __uint_as_float(t[j].x);
+                                acc[4 * j + 1] += __uint_as_float(t[j].y);
+                                acc[4 * j + 2] += __uint_as_float(t[j].z);
+                                acc[4 * j + 3] += __uint_as_float(t[j].w);
                             }
                         }
                         uint32_t wds[16];
@@ -720,8 +717,6 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
                         store_c_chunk(p, tmc, cbuf, lane, wds, col0 + c * 32, row_w, p.M);
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(&ctl->acc_empty[buf]);
                 if (leader) p.tile_cnt[tile] = 0u;   // ready for the next launch
                 if (!ok) return;
             }
