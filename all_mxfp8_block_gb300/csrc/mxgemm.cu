@@ -436,7 +436,9 @@ __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_
             const int stage = it % L::kStg;
             const uint32_t ph = (uint32_t)(it / L::kStg) & 1u;
             if (!wait_mbar(p, ctl, &ctl->full[stage], ph, kRoleMma)) return;
+            TRACE(11, it, 0);
             if (kPair && !wait_mbar(p, ctl, &ctl->peer_full[stage], ph, kRoleMma)) return;
+            if (kPair) TRACE(12, it, 0);
             ctl->consumed = it + 1;
             if (j == 0) TRACE(2, w, 0);
             tc_fence_after();
@@ -514,6 +516,7 @@ __device__ void forwarder_role(const GemmParams& p, SmemCtl* ctl) {
             const int stage = it % L::kStg;
             const uint32_t ph = (uint32_t)(it / L::kStg) & 1u;
             if (!wait_mbar(p, ctl, &ctl->full[stage], ph, kRoleMma)) return;
+            TRACE(13, it, 0);
             ctl->consumed = it + 1;
             mbar_arrive_remote(leader_full + (uint32_t)(stage * sizeof(uint64_t)));
             ++it;
