@@ -332,6 +332,25 @@ def time_siblings(dev, stream, flush, flush_bytes, steps, warmup):
     return out
 
 
+def run_siblings_only(args):
+    """The sibling operators alone (for profiling them): each path `warmup`
+    calls, then `steps` timed calls, in the order AllGather + GEMM fused,
+    unfused, direct, then GEMM + ReduceScatter fused, unfused."""
+    import torch
+    from all_mxfp8_block_gb300 import build as mxbuild
+    from all_mxfp8_block_gb300 import mxa2a
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    mxbuild.build()
+    mxa2a.load()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_bytes = max(2 * l2, 64 << 20) // 16 * 16
+    flush = torch.zeros(flush_bytes // 4, dtype=torch.int32, device=dev)
+    res = time_siblings(dev, torch.cuda.current_stream(dev), flush, flush_bytes, args.steps, args.warmup)
+    print(json.dumps({"siblings": res, "steps": args.steps, "warmup": args.warmup}), flush=True)
+    return 0
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -556,6 +575,8 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph timing of the smallest workload")
     ap.add_argument("--no-ablation", action="store_true", help="skip the staging-protocol ablation timings")
     ap.add_argument("--no-siblings", action="store_true", help="skip the sibling operators' timings")
+    ap.add_argument("--only-siblings", action="store_true",
+                    help="time only the sibling operators (one JSON line of their timings, not the benchmark line)")
     ap.add_argument("--skew-ns", type=int, default=4000, help="copy delay of every 4th CTA in the ablation")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--split", type=int, default=0, help="force the K split of both paths (0 = automatic)")
@@ -568,6 +589,8 @@ def main(argv=None):
     w = inputs.workload(int(args.workload)) if args.workload.isdigit() else inputs.workload(args.workload)
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.only_siblings:
+        return run_siblings_only(args)
     return run_ours(args, w)
 
 
