@@ -101,6 +101,7 @@ struct mxa2a_plan {
     int pair_fused = 0, pair_unfused = 0;   // CTA-pair kernel in use, per path
     int group_fused = 1, group_unfused = 1; // raster group, in m rows (tiles or tile pairs)
     int group_cap = 16;                     // option: largest unfused raster group
+    int group_fused_opt = 0;                // option: fused raster group in m-tiles (0 = one)
     int allow_pair = 0;           // option: 1 allows the CTA-pair kernel
     int max_pairs_fused = 0, max_pairs_unfused = 0;
     int rows_per_chunk = 1, chunks_per_seg = 1, n_copy_tasks = 0;
@@ -218,6 +219,23 @@ void derive(mxa2a_plan* p) {
         const int rows_u = (int)((p->M + row_u - 1) / row_u);
         p->group_unfused = std::max(1, std::min(rows_u, p->group_cap));
         p->group_fused = 1;
+        // Option: a fused group of g m-tiles, which must keep the items' order
+        // monotone in staging steps at group granularity (the credit protocol's
+        // freedom from deadlock rests on it): g divides the m-tiles of a step, or
+        // is a multiple of them within the ring's rows.
+        const int g = p->group_fused_opt;
+        if (g > 1 && !p->pair_fused && p->cm % BM == 0) {
+            const int tps = (int)(p->cm / BM);                       // m-tiles per step
+            const int ring = (int)((int64_t)p->bn * p->cm / BM);     // m-tiles in the ring
+            int gg = 1;
+            if (g <= tps) {
+                for (int d = g; d >= 1; --d)
+                    if (tps % d == 0) { gg = d; break; }
+            } else {
+                gg = std::min(g / tps, ring / tps) * tps;
+            }
+            p->group_fused = std::max(1, std::min(gg, p->Mt));
+        }
     }
     // Staging copy chunk: the largest divisor of commMSize rows within the
     // chunk size.  Automatic: about two steps' tasks for all copy workers (a
@@ -882,6 +900,10 @@ int mxa2a_set_option(mxa2a_plan* p, int key, int64_t v) {
             if (v < 0 || v > 1000000) return MXA2A_ERR_INVALID_OPTION;
             p->copy_skew_ns = (int)v;
             break;
+        case MXA2A_OPT_GROUP_FUSED:
+            if (v < 0 || v > 1024) return MXA2A_ERR_INVALID_OPTION;
+            p->group_fused_opt = (int)v;
+            break;
         default:
             return MXA2A_ERR_INVALID_OPTION;
     }
@@ -907,6 +929,7 @@ int mxa2a_get_option(mxa2a_plan* p, int key, int64_t* v) {
         case MXA2A_OPT_ELEM_TYPES: *v = p->elem_types; break;
         case MXA2A_OPT_STEP_CREDITS: *v = p->step_credits; break;
         case MXA2A_OPT_COPY_SKEW_NS: *v = p->copy_skew_ns; break;
+        case MXA2A_OPT_GROUP_FUSED: *v = p->group_fused_opt; break;
         case MXA2A_INFO_GROUP_FUSED: *v = p->group_fused; break;
         case MXA2A_INFO_GROUP_UNFUSED: *v = p->group_unfused; break;
         case MXA2A_INFO_CTA_PAIR: *v = p->pair_fused; break;

@@ -43,6 +43,7 @@ MXA2A_OPT_TILE_N = 13
 MXA2A_OPT_ELEM_TYPES = 14
 MXA2A_OPT_STEP_CREDITS = 15
 MXA2A_OPT_COPY_SKEW_NS = 16
+MXA2A_OPT_GROUP_FUSED = 17
 ELEM_TYPES = {("e4m3", "e4m3"): 0, ("e5m2", "e5m2"): 1, ("e4m3", "e5m2"): 2, ("e5m2", "e4m3"): 3}
 MXA2A_INFO_STEPS = 100
 MXA2A_INFO_MTILES = 101

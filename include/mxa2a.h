@@ -282,6 +282,12 @@ enum mxa2a_option {
                                       the whole step); 0 (default): per-segment credits */
     MXA2A_OPT_COPY_SKEW_NS = 16,   /* test knob: the copy workers of every 4th CTA wait this many ns
                                       before each copy task (0 = off, at most 1e6) */
+    MXA2A_OPT_GROUP_FUSED = 17,    /* fused raster group in m-tiles, n-tile outer inside a group
+                                      (0 or 1, default: m-tile by m-tile).  Rounded to a divisor of a
+                                      staging step's m-tiles, or to a multiple of them within the
+                                      ring's rows (buffer_num * commMSize); ignored when commMSize is
+                                      not a multiple of 128 or with the CTA-pair kernel (the planner's
+                                      choice: MXA2A_INFO_GROUP_FUSED) */
     /* read-only plan facts (mxa2a_get_option only) */
     MXA2A_INFO_STEPS = 100,        /* M / commMSize */
     MXA2A_INFO_MTILES = 101,
