@@ -245,6 +245,36 @@ RS_WORKLOADS = [
 ]
 
 
+@dataclass(frozen=True)
+class AllReduceWorkload:
+    """One problem size of GEMM + AllReduce (one-shot), seen from rank
+    ``rank`` of ``R``: A [M][K], B [N][K]; every rank ends with the sum of
+    all ranks' [M][N] partials."""
+    name: str
+    R: int
+    rank: int
+    M: int
+    K: int
+    N: int
+    seed: int
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def bytes_alg(self) -> int:
+        """A, B and their scales once; R-1 peers' partials read; the published partial and out written (BF16)."""
+        M, K, N = self.M, self.K, self.N
+        return M * K + M * K // MX_BLOCK + N * K + N * K // MX_BLOCK + 2 * (self.R + 1) * M * N
+
+
+AR_WORKLOADS = [
+    AllReduceWorkload("ar_r3_m192_k384_n272", 3, 1, 192, 384, 272, 50),
+    AllReduceWorkload("ar_r4_m2048_k4096_n4096", 4, 1, 2048, 4096, 4096, 51),
+]
+
+
 def make_allgather_inputs(w: AllGatherWorkload) -> dict:
     """Draw and quantise AllGather + GEMM inputs (CPU tensors).  Draw order:
     ``A_j = randn(rowsPerRank, K)`` for j = 0..R-1, then ``B = randn(K, N) /
@@ -276,6 +306,26 @@ def make_reduce_scatter_inputs(w: ReduceScatterWorkload) -> dict:
             recv.append(None)
         else:
             r = torch.randn(w.rows, w.N, generator=g, dtype=torch.float32)
+            recv.append(r.to(torch.bfloat16).view(torch.int16).contiguous())
+    A_codes, A_sf = quantize_mx_rows(A)
+    B_codes, B_sf = quantize_mx_rows(B.t().contiguous())
+    return {"A": A_codes, "A_scale": A_sf, "B": B_codes, "B_scale": B_sf, "recv": recv, "workload": w}
+
+
+def make_allreduce_inputs(w: AllReduceWorkload) -> dict:
+    """Draw GEMM + AllReduce inputs (CPU tensors).  Draw order: ``A =
+    randn(M, K)``, ``B = randn(K, N) / sqrt(K)`` (quantised to MXFP8), then
+    for every peer j != rank in order its published partial ``randn(M, N)``
+    rounded to BF16, as int16 bit patterns; ``recv[rank]`` is None."""
+    g = torch.Generator().manual_seed(w.seed)
+    A = torch.randn(w.M, w.K, generator=g, dtype=torch.float32)
+    B = torch.randn(w.K, w.N, generator=g, dtype=torch.float32) / math.sqrt(w.K)
+    recv = []
+    for j in range(w.R):
+        if j == w.rank:
+            recv.append(None)
+        else:
+            r = torch.randn(w.M, w.N, generator=g, dtype=torch.float32)
             recv.append(r.to(torch.bfloat16).view(torch.int16).contiguous())
     A_codes, A_sf = quantize_mx_rows(A)
     B_codes, B_sf = quantize_mx_rows(B.t().contiguous())

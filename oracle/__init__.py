@@ -14,9 +14,9 @@ against things other than itself: torch's float8 decoders (exhaustive), exact
 rational brute force, float64 matmul of exactly representable cases, identity
 and one-hot operands, power-of-two scale invariance, segment-order
 permutation and hand-worked fixtures in ``tests/golden/``.  The two sibling
-fused operators (AllGather + GEMM, GEMM + ReduceScatter, the performance
-optimisation guide's section 3 cases) are compositions of :func:`gemm` with a
-row stack and with an exact sum rounded once; they are pinned in
+fused operators (AllGather + GEMM, GEMM + ReduceScatter, GEMM + AllReduce,
+the performance optimisation guide's section 3 cases) are compositions of
+:func:`gemm` with a row stack and with an exact sum rounded once; they are pinned in
 ``tests/test_oracle_siblings.py`` (identity operands with known blocks, exact
 rational sums, torch's BF16 rounding).
 """
@@ -230,3 +230,22 @@ def gemm_reduce_scatter(A, A_scale, B, B_scale, recv, R: int, rank: int, nthread
         terms.append(bf16_bits_to_f64(blk))
     out = round_f64_to_bf16(_exact_sum(terms))
     return send, out
+
+
+def gemm_allreduce(A, A_scale, B, B_scale, recv, R: int, rank: int, nthreads: int = 0,
+                   a_fmt: str = "e4m3", b_fmt: str = "e4m3"):
+    """GEMM + AllReduce, one-shot, from rank ``rank`` of ``R`` (performance
+    optimisation guide, section 3.3, which names the operator only).  This
+    rank's partial P = :func:`gemm` of its A [M][K] and B [N][K], as BF16, is
+    published; its output is the sum over ranks j of rank j's partial
+    (``recv[j]``, BF16 bits [M][N], for j != rank; P for j == rank), computed
+    exactly and rounded once to BF16.  Returns ``(pub, out)``, both BF16 bits
+    [M][N]."""
+    P = gemm([A], [A_scale], B, B_scale, nthreads=nthreads, a_fmt=a_fmt, b_fmt=b_fmt)
+    assert 0 <= rank < R and len(recv) == R
+    terms = []
+    for j in range(R):
+        blk = P if j == rank else np.asarray(recv[j]).view(np.uint16)
+        assert blk.shape == P.shape
+        terms.append(bf16_bits_to_f64(blk))
+    return P, round_f64_to_bf16(_exact_sum(terms))

@@ -127,3 +127,18 @@ def test_null_sibling_calls_fail_cleanly(lib):
         mxa2a.MXA2A_ERR_NULL_PTR
     assert L.mxa2a_run_reduce_scatter_unfused(None, None, None, None, None, None, None, None, None) == \
         mxa2a.MXA2A_ERR_NULL_PTR
+
+
+def test_validate_allreduce_rules(lib):
+    v = mxa2a.mxa2a_validate_allreduce
+    ok, bad = mxa2a.MXA2A_OK, mxa2a.MXA2A_ERR_INVALID_SHAPE
+    assert v(4, 1, 2048, 4096, 4096) == ok
+    assert v(1, 0, 64, 128, 16) == ok
+    assert v(3, 1, 192, 384, 272) == ok
+    assert v(4, 4, 2048, 4096, 4096) == bad             # rank < R
+    assert v(0, 0, 2048, 4096, 4096) == bad             # R >= 1
+    assert v(4, 0, 2048 + 32, 4096, 4096) == bad        # M % 64
+    assert v(4, 0, 2048, 4000, 4096) == bad             # K % 128
+    assert v(4, 0, 2048, 4096, 4008) == bad             # N % 16
+    L = mxa2a.load()
+    assert L.mxa2a_run_allreduce(None, None, None, None, None, None, None, None, None) == mxa2a.MXA2A_ERR_NULL_PTR

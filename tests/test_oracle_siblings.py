@@ -1,5 +1,5 @@
 """Pins of the sibling-operator oracle functions (AllGather + GEMM, GEMM +
-ReduceScatter; the performance optimisation guide, section 3) and of its
+ReduceScatter, GEMM + AllReduce; the performance optimisation guide, section 3) and of its
 float64 -> BF16 rounding, against things other than the oracle itself:
 torch's BF16 conversion, the explicit BF16 grid of ``tests/_exact.py``, exact
 rational sums, and identity operands whose products are known block by block.
@@ -174,3 +174,47 @@ def test_reduce_scatter_cancellation_is_exact():
 def test_exact_sum_refuses_an_inexact_float64_sum():
     with pytest.raises(AssertionError):
         oracle._exact_sum([np.array([1.0]), np.array([2.0 ** -60])])
+
+
+# --- GEMM + AllReduce (one-shot) -----------------------------------------------------
+
+@pytest.mark.parametrize("R,rank", [(3, 0), (3, 2), (2, 1)])
+def test_allreduce_identity_B_publishes_and_sums_every_row(R, rank):
+    """B = I: the published partial is the decoded, scaled A; the output is,
+    for every row, the exact rational sum of that and the R-1 peers'
+    partials, rounded once to BF16 (grid search)."""
+    M, K = 64, 128
+    A = _finite_codes((M, K), 120 + R + rank)
+    S = inputs.random_scales((M, K // 32), 121, lo=117, hi=137).numpy()
+    B, Bs = _identity_b(K)
+    rng = np.random.default_rng(122 + rank)
+    recv = [None if j == rank else
+            _torch_bf16_bits(rng.standard_normal((M, K)).astype(np.float32) * 4) for j in range(R)]
+    pub, out = oracle.gemm_allreduce(A, S, B, Bs, recv, R, rank)
+    P = X.round_f64_to_bf16(X.e4m3_values(A) * np.repeat(X.e8m0_values(S), 32, axis=1))
+    assert np.array_equal(pub, P)
+    vals = [(p.astype(np.uint32) << 16).view(np.float32) for p in (P if j == rank else recv[j] for j in range(R))]
+    want = np.zeros((M, K), dtype=np.uint16)
+    for i in range(M):
+        for n in range(K):
+            want[i, n] = X.round_fraction_to_bf16(sum(Fraction(float(v[i, n])) for v in vals))
+    assert np.array_equal(out, want)
+
+
+def test_allreduce_is_the_reduce_scatter_of_one_block():
+    """Every rank's all-reduce output equals the reduce-scatter's output
+    blocks stacked: block j of the all-reduce is what rank j's reduce-scatter
+    computes from the same partials."""
+    R, M, K = 3, 192, 128
+    A = _finite_codes((M, K), 130)
+    S = inputs.random_scales((M, K // 32), 131, lo=120, hi=134).numpy()
+    B, Bs = _identity_b(K)
+    rng = np.random.default_rng(132)
+    rank = 1
+    recv = [None if j == rank else
+            _torch_bf16_bits(rng.standard_normal((M, K)).astype(np.float32)) for j in range(R)]
+    _, out = oracle.gemm_allreduce(A, S, B, Bs, recv, R, rank)
+    rows = M // R
+    _, rs_out = oracle.gemm_reduce_scatter(A, S, B, Bs, [None if r is None else r[rank * rows:(rank + 1) * rows]
+                                                        for r in recv], R, rank)
+    assert np.array_equal(out[rank * rows:(rank + 1) * rows], rs_out)
