@@ -107,7 +107,7 @@ cudaError_t launch_pack_a(const GemmParams& p, uint8_t* a_packed, int grid, cuda
 // fp32 adds of the BF16 partials in rank order from 0, one rounding to BF16.
 __global__ void rs_reduce_kernel(const __grid_constant__ RsArgs a) {
     const int vpr = a.N / 8;
-    const long long total = (long long)a.R * a.rows * vpr;
+    const long long total = (long long)a.nblk * a.rows * vpr;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
         const int v = (int)(i % vpr);
@@ -115,7 +115,7 @@ __global__ void rs_reduce_kernel(const __grid_constant__ RsArgs a) {
         const int j = (int)(row / a.rows);
         const size_t off = (size_t)(row - (long long)j * a.rows) * a.N + (size_t)v * 8;
         const uint16_t* own = a.P + (size_t)row * a.N + (size_t)v * 8;
-        if (j != a.rank) {
+        if (j != a.own) {
             *reinterpret_cast<uint4*>(a.send[j] + off) = ptx::ld_nc_v4(own);
             continue;
         }
@@ -142,7 +142,7 @@ __global__ void rs_reduce_kernel(const __grid_constant__ RsArgs a) {
 }
 
 cudaError_t launch_rs_reduce(const RsArgs& a, cudaStream_t stream) {
-    const long long work = (long long)a.R * a.rows * (a.N / 8);
+    const long long work = (long long)a.nblk * a.rows * (a.N / 8);
     rs_reduce_kernel<<<grid_for(work, 256), 256, 0, stream>>>(a);
     return cudaGetLastError();
 }

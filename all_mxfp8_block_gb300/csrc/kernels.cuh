@@ -141,9 +141,15 @@ struct GemmParams {
     // warps then sum each row of out with recv[j] (fp32, j in order) in place.
     // The m-tiles are taken starting at block rs_rank's, so its sums overlap
     // the other blocks' GEMM.
-    int rs_rows, rs_rank, rs_R;
+    // GEMM + AllReduce (one-shot) uses the same path with one block of all M
+    // rows (rs_own = 0) and rs_publish = 1: the block's partial goes to
+    // send_maps[0] (the buffer the peers read, rs_pub) and the sums read it
+    // there and write out.  rs_rank is the rank's place in the sum; rs_own the
+    // block summed here (RS: rs_rank).
+    int rs_rows, rs_rank, rs_R, rs_own, rs_publish;
     const CUtensorMap* send_maps;
     const uint16_t* recv[kMaxSegments];
+    const uint16_t* rs_pub;
     unsigned long long* rs_cnt;   // [Mt * Nt], zero between launches
 };
 
@@ -175,12 +181,14 @@ cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t stream);
 // The reduce-scatter of the unfused GEMM + ReduceScatter: P bf16 [R*rows][N];
 // send[j] = block j of P (j != rank); out = bf16(sum over j in order of block
 // rank of P (j == rank) or recv[j]), fp32 adds.  Pointer arrays of R entries.
+// With nblk blocks of rows (RS: nblk = R, own = rank; one-shot all-reduce:
+// nblk = 1, own = 0, P is the published partial).
 struct RsArgs {
     const uint16_t* P;
     const uint16_t* recv[kMaxSegments];
     uint16_t* send[kMaxSegments];
     uint16_t* out;
-    int R, rank, rows, N;
+    int R, rank, rows, N, nblk, own;
 };
 cudaError_t launch_rs_reduce(const RsArgs& a, cudaStream_t stream);
 

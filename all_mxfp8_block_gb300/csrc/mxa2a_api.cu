@@ -146,6 +146,9 @@ struct mxa2a_plan {
     // GEMM + ReduceScatter: this rank, the ranks, rows per block
     int rs_rank = 0, rs_R = 0;
     int64_t rs_rows = 0;
+    // blocks of rs_rows rows, the one summed here, and whether its partial is
+    // published (GEMM + AllReduce: one block of all rows, published)
+    int rs_nblk = 0, rs_own = 0, rs_publish = 0;
     uint16_t* rs_scratch = nullptr;         // the unfused path's partial P [M][N] (allocated on first use)
     CUtensorMap* send_maps_dev = nullptr;   // workspace, after the segment maps
     CUtensorMap send_maps_host[kMaxSegments];
@@ -387,13 +390,18 @@ int ensure_partials(mxa2a_plan* p) {
 
 enum RunMode { kRunFused, kRunUnfused, kRunDirect };
 
-// The reduce-scatter side of one GEMM + ReduceScatter run.
+// The collective side of one GEMM + ReduceScatter or GEMM + AllReduce run.
 struct RsRun {
     bool fused;                 // the GEMM's epilogue routes and sums (else the reduce kernel after it)
-    const void* const* recv;
-    void* const* send;
+    const void* const* recv;    // rs_R entries (entry rs_rank unused)
+    void* const* send;          // rs_nblk entries (entry rs_own unused); NULL for the all-reduce
+    void* pub;                  // the all-reduce's published partial, else NULL
     void* out;
 };
+
+bool is_rs_kind(const mxa2a_plan* p) {
+    return p->kind == MXA2A_KIND_REDUCE_SCATTER || p->kind == MXA2A_KIND_ALLREDUCE;
+}
 
 int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, const void* B, const void* B_sf,
              void* C, void* stream_v, RunMode mode, const RsRun* rs = nullptr) {
@@ -401,7 +409,7 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
     int rc = check_args(p, A_seg, A_sf, B, B_sf, C);
     if (rc) return rc;
     // a reduce-scatter plan runs through its own calls only, and they through this path with A read in place
-    if ((p->kind == MXA2A_KIND_REDUCE_SCATTER) != (rs != nullptr) || (rs && mode != kRunDirect))
+    if (is_rs_kind(p) != (rs != nullptr) || (rs && mode != kRunDirect))
         return MXA2A_ERR_INVALID_OPTION;
     if ((rc = check_device(p))) return rc;
     if ((rc = refresh_b_map(p, B))) return rc;
@@ -443,27 +451,34 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
         g.seg_maps = p->seg_maps_dev;
     }
     if (rs_fused) {
-        // the epilogue stores the peers' blocks through one tensor map per send buffer
+        // the epilogue stores the peers' blocks (and a published partial) through one
+        // tensor map per buffer
+        auto target = [&](int j) -> void* {
+            if (j == p->rs_own) return p->rs_publish ? rs->pub : nullptr;
+            return rs->send[j];
+        };
         bool same = true;
-        for (int j = 0; j < p->rs_R; ++j) same = same && (j == p->rs_rank || p->send_ptrs[j] == rs->send[j]);
+        for (int j = 0; j < p->rs_nblk; ++j) same = same && p->send_ptrs[j] == target(j);
         if (!same) {
-            for (int j = 0; j < p->rs_R; ++j) {
-                if (j == p->rs_rank) {
+            for (int j = 0; j < p->rs_nblk; ++j) {
+                void* t = target(j);
+                if (!t) {
                     std::memset(&p->send_maps_host[j], 0, sizeof(CUtensorMap));
-                    p->send_ptrs[j] = nullptr;
-                } else {
-                    if (!encode_c(&p->send_maps_host[j], rs->send[j], (uint64_t)p->rs_rows, (uint64_t)p->N))
-                        return MXA2A_ERR_CUDA;
-                    p->send_ptrs[j] = rs->send[j];
+                } else if (!encode_c(&p->send_maps_host[j], t, (uint64_t)p->rs_rows, (uint64_t)p->N)) {
+                    return MXA2A_ERR_CUDA;
                 }
+                p->send_ptrs[j] = t;
             }
-            if ((rc = cuda_rc(cudaMemcpyAsync(p->send_maps_dev, p->send_maps_host, sizeof(CUtensorMap) * p->rs_R,
-                                              cudaMemcpyHostToDevice, stream))))
+            if ((rc = cuda_rc(cudaMemcpyAsync(p->send_maps_dev, p->send_maps_host,
+                                              sizeof(CUtensorMap) * p->rs_nblk, cudaMemcpyHostToDevice, stream))))
                 return rc;
         }
         g.rs_rows = (int)p->rs_rows;
         g.rs_rank = p->rs_rank;
         g.rs_R = p->rs_R;
+        g.rs_own = p->rs_own;
+        g.rs_publish = p->rs_publish;
+        g.rs_pub = static_cast<const uint16_t*>(rs->pub);
         g.send_maps = p->send_maps_dev;
         g.rs_cnt = p->rs_cnt;
         for (int j = 0; j < p->rs_R; ++j)
@@ -505,16 +520,17 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
         RsArgs ra;
         std::memset(&ra, 0, sizeof ra);
         ra.P = static_cast<const uint16_t*>(C);
-        for (int j = 0; j < p->rs_R; ++j) {
-            if (j == p->rs_rank) continue;
-            ra.recv[j] = static_cast<const uint16_t*>(rs->recv[j]);
-            ra.send[j] = static_cast<uint16_t*>(rs->send[j]);
-        }
+        for (int j = 0; j < p->rs_R; ++j)
+            if (j != p->rs_rank) ra.recv[j] = static_cast<const uint16_t*>(rs->recv[j]);
+        for (int j = 0; j < p->rs_nblk; ++j)
+            if (j != p->rs_own) ra.send[j] = static_cast<uint16_t*>(rs->send[j]);
         ra.out = static_cast<uint16_t*>(rs->out);
         ra.R = p->rs_R;
         ra.rank = p->rs_rank;
         ra.rows = (int)p->rs_rows;
         ra.N = (int)p->N;
+        ra.nblk = p->rs_nblk;
+        ra.own = p->rs_own;
         if ((rc = cuda_rc(launch_rs_reduce(ra, stream)))) return rc;
         ++launches;
     }
@@ -571,7 +587,9 @@ mxa2a_plan* create_impl(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t c
     const size_t o_status = off; off = align_up(off + sizeof(DevStatus), 1024);
     const size_t o_maps = off; off = align_up(off + sizeof(CUtensorMap) * 2 * kMaxSegments, 1024);
     // reduce-scatter tile counts, for either tile width (the narrow tile has 2 Nt columns of tiles)
-    p->rs_cnt_bytes = kind == MXA2A_KIND_REDUCE_SCATTER ? (size_t)p->Mt * 2 * p->Nt * sizeof(unsigned long long) : 0;
+    p->rs_cnt_bytes = (kind == MXA2A_KIND_REDUCE_SCATTER || kind == MXA2A_KIND_ALLREDUCE)
+                          ? (size_t)p->Mt * 2 * p->Nt * sizeof(unsigned long long)
+                          : 0;
     const size_t o_rs = off; off = align_up(off + p->rs_cnt_bytes, 1024);
     p->ws_bytes = off;
     if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
@@ -662,6 +680,32 @@ mxa2a_plan* mxa2a_create_reduce_scatter(int R, int rank, int64_t M, int64_t K, i
         p->rs_rank = rank;
         p->rs_R = R;
         p->rs_rows = M / R;
+        p->rs_nblk = R;
+        p->rs_own = rank;
+        p->rs_publish = 0;
+    }
+    return p;
+}
+
+int mxa2a_validate_allreduce(int R, int rank, int64_t M, int64_t K, int64_t N) {
+    if (R < 1 || R > kMaxSegments || rank < 0 || rank >= R) return MXA2A_ERR_INVALID_SHAPE;
+    return mxa2a_validate(1, M, K, N, 64, 2);
+}
+
+mxa2a_plan* mxa2a_create_allreduce(int R, int rank, int64_t M, int64_t K, int64_t N) {
+    const int rc = mxa2a_validate_allreduce(R, rank, M, K, N);
+    if (rc) {
+        g_last_error = rc;
+        return nullptr;
+    }
+    mxa2a_plan* p = create_impl(1, M, K, N, 64, 2, MXA2A_KIND_ALLREDUCE, 1, 0, false);
+    if (p) {   // one block of all M rows, summed here and published
+        p->rs_rank = rank;
+        p->rs_R = R;
+        p->rs_rows = M;
+        p->rs_nblk = 1;
+        p->rs_own = 0;
+        p->rs_publish = 1;
     }
     return p;
 }
@@ -690,12 +734,40 @@ int run_rs(mxa2a_plan* p, const void* A, const void* A_sf, const void* B, const 
         }
         C = p->rs_scratch;
     }
-    const RsRun rs{fused, recv, send, out};
+    const RsRun rs{fused, recv, send, nullptr, out};
     const void* a_seg[1] = {A};
     const void* a_sf[1] = {A_sf};
     return run_impl(p, a_seg, a_sf, B, B_sf, C, stream, kRunDirect, &rs);
 }
+
+int run_ar(mxa2a_plan* p, const void* A, const void* A_sf, const void* B, const void* B_sf, const void* const* recv,
+           void* pub, void* out, void* stream, bool fused) {
+    if (!p || !recv || !pub || !out) return MXA2A_ERR_NULL_PTR;
+    if (p->kind != MXA2A_KIND_ALLREDUCE) return MXA2A_ERR_INVALID_OPTION;
+    for (int j = 0; j < p->rs_R; ++j) {
+        if (j == p->rs_rank) continue;
+        if (!recv[j]) return MXA2A_ERR_NULL_PTR;
+        if (!aligned(recv[j], 16)) return MXA2A_ERR_MISALIGNED;
+    }
+    if (!aligned(out, 16) || !aligned(pub, 16)) return MXA2A_ERR_MISALIGNED;
+    // fused: the GEMM's epilogue publishes the partial and the kernel sums into
+    // out; unfused: the GEMM writes the partial into pub, then the reduce kernel
+    const RsRun rs{fused, recv, nullptr, pub, out};
+    const void* a_seg[1] = {A};
+    const void* a_sf[1] = {A_sf};
+    return run_impl(p, a_seg, a_sf, B, B_sf, fused ? out : pub, stream, kRunDirect, &rs);
+}
 }  // namespace
+
+int mxa2a_run_allreduce(mxa2a_plan* p, const void* A, const void* A_sf, const void* B, const void* B_sf,
+                        const void* const* recv, void* pub, void* out, void* stream) {
+    return run_ar(p, A, A_sf, B, B_sf, recv, pub, out, stream, true);
+}
+
+int mxa2a_run_allreduce_unfused(mxa2a_plan* p, const void* A, const void* A_sf, const void* B, const void* B_sf,
+                                const void* const* recv, void* pub, void* out, void* stream) {
+    return run_ar(p, A, A_sf, B, B_sf, recv, pub, out, stream, false);
+}
 
 int mxa2a_run_reduce_scatter(mxa2a_plan* p, const void* A, const void* A_sf, const void* B, const void* B_sf,
                              const void* const* recv, void* const* send, void* out, void* stream) {

@@ -142,7 +142,7 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int w) {
     const int rem2 = rem - ntl * (gm * p.S);
     it.mt = g * p.group_m + rem2 / p.S;
     // GEMM + ReduceScatter: start at the m-tile of this rank's first row
-    if (p.rs_rows > 0 && !p.pair) it.mt = (it.mt + (p.rs_rank * p.rs_rows) / BM) % p.Mt;
+    if (p.rs_rows > 0 && !p.pair) it.mt = (it.mt + (p.rs_own * p.rs_rows) / BM) % p.Mt;
     it.q = rem2 % p.S;
     it.nt = (p.zigzag && (g & 1)) ? (p.Nt - 1 - ntl) : ntl;
     it.seg_lo = it.q * p.R / p.S;
@@ -629,14 +629,14 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
             const bool rs = !kFused && p.rs_rows > 0;   // (the staging kernel never reduce-scatters)
             if (rs) {
                 const int blk = row_w < p.M ? row_w / p.rs_rows : -1;
-                dst = (blk >= 0 && blk != p.rs_rank) ? p.send_maps + blk : tmc;
+                dst = (blk >= 0 && (blk != p.rs_own || p.rs_publish)) ? p.send_maps + blk : tmc;
                 y = blk >= 0 ? row_w - blk * p.rs_rows : 0;
                 ylim = blk >= 0 ? p.rs_rows : 0;
             }
 #pragma unroll
             for (int c = 0; c < kChunks; ++c)
                 store_c_chunk(p, dst, cbuf, lane, packed + c * 16, col0 + c * 32, y, ylim);
-            if (rs && mt * BM < (p.rs_rank + 1) * p.rs_rows && (mt + 1) * BM > p.rs_rank * p.rs_rows) {
+            if (rs && mt * BM < (p.rs_own + 1) * p.rs_rows && (mt + 1) * BM > p.rs_own * p.rs_rows) {
                 // a tile with rows of this rank's block: once this warp's stores have
                 // landed, count it for the copy warps that sum those rows
                 if (lane == 0) {
@@ -783,11 +783,12 @@ __device__ __forceinline__ void copy_rows(const uint8_t* src, int src_ld, uint8_
 // of block `rank` of rank j's partial (the stored value for j == rank,
 // recv[j] otherwise): fp32 adds in that order from 0, one rounding to BF16.
 __device__ void rs_reduce_role(const GemmParams& p, SmemCtl* ctl, int lane) {
-    constexpr int kRows = 8, U = 2, Q = 4;   // rows per task; rows and ranks loaded at once
+    constexpr int kRows = 8, U = 4, Q = 4;   // rows per task; rows and ranks loaded at once
     const int n_tasks = (p.rs_rows / kRows) * p.Nt;
     const int vpr = p.tile_n / 8;            // 16-byte vectors in a tile row: one per lane
     unsigned long long* next = p.flags + FlagLayout::copy_next(p.bn, p.R);
     uint16_t* out = p.C;
+    const uint16_t* own_src = p.rs_publish ? p.rs_pub : out;   // where this rank's partial was stored
     for (;;) {
         int t = -1;
         if (lane == 0 && !ctl->abort) {
@@ -799,7 +800,7 @@ __device__ void rs_reduce_role(const GemmParams& p, SmemCtl* ctl, int lane) {
         const int g = t / p.Nt;
         const int nt = t - g * p.Nt;
         const int lr0 = g * kRows;                            // first row inside the block
-        const int mt = (p.rs_rank * p.rs_rows + lr0) / BM;    // the m-tile that computed them
+        const int mt = (p.rs_own * p.rs_rows + lr0) / BM;     // the m-tile that computed them
         int ok = 1;
         if (lane == 0)
             ok = wait_counter(p, ctl, p.rs_cnt + (size_t)mt * p.Nt + nt, (unsigned long long)kEpiWarps,
@@ -825,7 +826,7 @@ __device__ void rs_reduce_role(const GemmParams& p, SmemCtl* ctl, int lane) {
                             const size_t off = (size_t)(lr0 + r0 + u) * p.N + col;
                             tv[u][qq] = make_uint4(0u, 0u, 0u, 0u);
                             if (q == p.rs_rank)
-                                tv[u][qq] = ld_cg_v4(out + off);
+                                tv[u][qq] = ld_cg_v4(own_src + off);
                             else if (q < p.rs_R)
                                 tv[u][qq] = ld_nc_v4(p.recv[q] + off);
                         }

@@ -69,6 +69,7 @@ MXA2A_INFO_KIND = 119
 MXA2A_KIND_ALLTOALL = 0
 MXA2A_KIND_ALLGATHER = 1
 MXA2A_KIND_REDUCE_SCATTER = 2
+MXA2A_KIND_ALLREDUCE = 3
 
 MXA2A_WS_RING = 1
 MXA2A_WS_SFA = 2
@@ -105,6 +106,10 @@ _SIGS = [
     ("mxa2a_create_reduce_scatter", _VP, [ctypes.c_int, ctypes.c_int, _I64, _I64, _I64]),
     ("mxa2a_run_reduce_scatter", ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _PP, _PP, _VP, _VP]),
     ("mxa2a_run_reduce_scatter_unfused", ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _PP, _PP, _VP, _VP]),
+    ("mxa2a_validate_allreduce", ctypes.c_int, [ctypes.c_int, ctypes.c_int, _I64, _I64, _I64]),
+    ("mxa2a_create_allreduce", _VP, [ctypes.c_int, ctypes.c_int, _I64, _I64, _I64]),
+    ("mxa2a_run_allreduce", ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _PP, _VP, _VP, _VP]),
+    ("mxa2a_run_allreduce_unfused", ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _PP, _VP, _VP, _VP]),
     ("mxa2a_run", ctypes.c_int, [_VP, _PP, _PP, _VP, _VP, _VP, _VP]),
     ("mxa2a_run_unfused", ctypes.c_int, [_VP, _PP, _PP, _VP, _VP, _VP, _VP]),
     ("mxa2a_run_direct", ctypes.c_int, [_VP, _PP, _PP, _VP, _VP, _VP, _VP]),
@@ -214,6 +219,28 @@ def mxa2a_create_reduce_scatter(R, rank, M, K, N) -> int:
     if not h:
         raise Mxa2aError(load().mxa2a_last_error(), "mxa2a_create_reduce_scatter")
     return h
+
+
+def mxa2a_validate_allreduce(R, rank, M, K, N) -> int:
+    return load().mxa2a_validate_allreduce(R, rank, M, K, N)
+
+
+def mxa2a_create_allreduce(R, rank, M, K, N) -> int:
+    h = load().mxa2a_create_allreduce(R, rank, M, K, N)
+    if not h:
+        raise Mxa2aError(load().mxa2a_last_error(), "mxa2a_create_allreduce")
+    return h
+
+
+def mxa2a_run_allreduce(plan, A, A_scale, B, B_scale, recv, pub, out, stream=None) -> None:
+    _check(load().mxa2a_run_allreduce(plan, _ptr(A), _ptr(A_scale), _ptr(B), _ptr(B_scale), _ptr_array(recv),
+                                      _ptr(pub), _ptr(out), _stream(stream)), "mxa2a_run_allreduce")
+
+
+def mxa2a_run_allreduce_unfused(plan, A, A_scale, B, B_scale, recv, pub, out, stream=None) -> None:
+    _check(load().mxa2a_run_allreduce_unfused(plan, _ptr(A), _ptr(A_scale), _ptr(B), _ptr(B_scale),
+                                              _ptr_array(recv), _ptr(pub), _ptr(out), _stream(stream)),
+           "mxa2a_run_allreduce_unfused")
 
 
 def mxa2a_run_reduce_scatter(plan, A, A_scale, B, B_scale, recv, send, out, stream=None) -> None:
@@ -398,3 +425,28 @@ class ReduceScatterPlan(Plan):
 
     def run_host(self, *a, **k):
         raise Mxa2aError(MXA2A_ERR_INVALID_OPTION, "a reduce-scatter plan has run and run_unfused only")
+
+
+class AllReducePlan(Plan):
+    """GEMM + AllReduce (one-shot) plan (``mxa2a_create_allreduce``) of rank
+    ``rank`` of ``R``: ``run`` / ``run_unfused`` take this rank's A, B (and
+    scales), the R peers' published partials ``recv`` (entry ``rank`` unused),
+    this rank's published partial ``pub`` and the output ``out`` (both
+    [M][N] BF16)."""
+
+    def __init__(self, R, rank, M, K, N):
+        self.shape = (R, rank, M, K, N)
+        self.R, self.rank, self.M, self.K, self.N = R, rank, M, K, N
+        self.handle = mxa2a_create_allreduce(R, rank, M, K, N)
+
+    def run(self, A, A_scale, B, B_scale, recv, pub, out, stream=None):
+        mxa2a_run_allreduce(self.handle, A, A_scale, B, B_scale, recv, pub, out, stream)
+
+    def run_unfused(self, A, A_scale, B, B_scale, recv, pub, out, stream=None):
+        mxa2a_run_allreduce_unfused(self.handle, A, A_scale, B, B_scale, recv, pub, out, stream)
+
+    def run_direct(self, *a, **k):
+        raise Mxa2aError(MXA2A_ERR_INVALID_OPTION, "an all-reduce plan has run and run_unfused only")
+
+    def run_host(self, *a, **k):
+        raise Mxa2aError(MXA2A_ERR_INVALID_OPTION, "an all-reduce plan has run and run_unfused only")

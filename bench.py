@@ -274,8 +274,8 @@ def time_tiny_graph(dev, runs: int = 200):
 def time_siblings(dev, stream, flush, flush_bytes, steps, warmup):
     """Mean ms per call of the sibling operators' fused and unfused paths on
     their benchmark workloads (AllGather + GEMM: 4 blocks of 512 rows, K = N =
-    4096; GEMM + ReduceScatter: rank 1 of 4, 2048 x 4096 x 4096), each call
-    after an L2 flush, CUDA events around each call."""
+    4096; GEMM + ReduceScatter and GEMM + AllReduce: rank 1 of 4, 2048 x 4096
+    x 4096), each call after an L2 flush, CUDA events around each call."""
     import torch
     from all_mxfp8_block_gb300 import inputs, mxa2a
 
@@ -329,13 +329,30 @@ def time_siblings(dev, stream, flush, flush_bytes, steps, warmup):
     tf = w.flops / (res["fused_ms"] / 1e3) / 1e12
     out["gemm_reduce_scatter"] = {"workload": w.name, "R": w.R, "rank": w.rank, "M": w.M, "K": w.K, "N": w.N,
                                   **res, "value": tf, "unit": UNIT, "roofline_frac": tf / peak, "steps": steps}
+    del A, S, B, Bs, recv, send, o
+    w = inputs.AR_WORKLOADS[1]
+    x = inputs.make_allreduce_inputs(w)
+    A, S, B, Bs = (x[k].to(dev) for k in ("A", "A_scale", "B", "B_scale"))
+    recv = [None if r is None else r.to(dev) for r in x["recv"]]
+    pub = torch.empty((w.M, w.N), dtype=torch.int16, device=dev)
+    o = torch.empty((w.M, w.N), dtype=torch.int16, device=dev)
+    with mxa2a.AllReducePlan(w.R, w.rank, w.M, w.K, w.N) as p:
+        res = {path + "_ms": timed(lambda fn=fn: fn(A, S, B, Bs, recv, pub, o, stream))
+               for path, fn in (("fused", p.run), ("unfused", p.run_unfused))}
+        st = p.status()
+        if st["code"] != 0:
+            raise RuntimeError(f"device status after the all-reduce timing: {st}")
+    tf = w.flops / (res["fused_ms"] / 1e3) / 1e12
+    out["gemm_allreduce"] = {"workload": w.name, "R": w.R, "rank": w.rank, "M": w.M, "K": w.K, "N": w.N,
+                             **res, "value": tf, "unit": UNIT, "roofline_frac": tf / peak, "steps": steps}
     return out
 
 
 def run_siblings_only(args):
     """The sibling operators alone (for profiling them): each path `warmup`
     calls, then `steps` timed calls, in the order AllGather + GEMM fused,
-    unfused, direct, then GEMM + ReduceScatter fused, unfused."""
+    unfused, direct, GEMM + ReduceScatter fused, unfused, GEMM + AllReduce
+    fused, unfused."""
     import torch
     from all_mxfp8_block_gb300 import build as mxbuild
     from all_mxfp8_block_gb300 import mxa2a

@@ -108,7 +108,8 @@ int mxa2a_last_error(void);
 enum mxa2a_kind {
     MXA2A_KIND_ALLTOALL = 0,       /* mxa2a_create: AllToAll + GEMM (above) */
     MXA2A_KIND_ALLGATHER = 1,      /* mxa2a_create_allgather: AllGather + GEMM */
-    MXA2A_KIND_REDUCE_SCATTER = 2  /* mxa2a_create_reduce_scatter: GEMM + ReduceScatter */
+    MXA2A_KIND_REDUCE_SCATTER = 2, /* mxa2a_create_reduce_scatter: GEMM + ReduceScatter */
+    MXA2A_KIND_ALLREDUCE = 3       /* mxa2a_create_allreduce: GEMM + AllReduce (one-shot) */
 };
 
 /*
@@ -185,6 +186,39 @@ int mxa2a_run_reduce_scatter(mxa2a_plan *plan, const void *A, const void *A_scal
 int mxa2a_run_reduce_scatter_unfused(mxa2a_plan *plan, const void *A, const void *A_scale, const void *B,
                                      const void *B_scale, const void *const *recv, void *const *send,
                                      void *out_bf16, void *stream);
+
+/*
+ * GEMM + AllReduce, one-shot: the third fused-operator case of the
+ * performance optimisation guide (section 3.3, title only; plain reading).
+ * The operands are K-sharded as for the reduce-scatter, and every rank ends
+ * with the whole sum.  One-shot means that each rank publishes its partial
+ * and reads every peer's partial directly, with no ring of partial sums.
+ * From rank `rank`'s side, on one GPU, for all m < M, n < N:
+ *
+ *   pub[m][n] = P[m][n] = bf16(A x B^T)[m][n]        (this rank's published partial)
+ *   out[m][n] = bf16( sum_{j<R} v_j[m][n] )  (fp32, j = 0, 1, .., R-1)
+ *               v_rank = P[m][n],  v_j = recv[j][m][n] (j != rank)
+ *
+ * recv[j] is peer j's published partial: a host array of R device pointers
+ * to uint16 BF16 [M][N] (entry `rank` unused, may be NULL); pub and out are
+ * uint16 BF16 [M][N].  Alignment: A, B, pub, out, recv[j] 16 bytes; scales 4.
+ *   mxa2a_run_allreduce          fused: one persistent GEMM whose epilogue
+ *       publishes each finished tile to pub; the kernel's spare warps sum
+ *       each tile's rows with the peers' partials into out as soon as
+ *       it is published, while the GEMM goes on;
+ *   mxa2a_run_allreduce_unfused  the GEMM writes pub, then a reduce kernel
+ *       writes out.
+ * Both give the same bits.  Shape rules: 1 <= R <= 64, 0 <= rank < R,
+ * M % 64 == 0, K % 128 == 0, N % 16 == 0, M, N, K <= 2^20.  Returns NULL on
+ * error (mxa2a_last_error).
+ */
+int mxa2a_validate_allreduce(int R, int rank, int64_t M, int64_t K, int64_t N);
+mxa2a_plan *mxa2a_create_allreduce(int R, int rank, int64_t M, int64_t K, int64_t N);
+int mxa2a_run_allreduce(mxa2a_plan *plan, const void *A, const void *A_scale, const void *B, const void *B_scale,
+                        const void *const *recv, void *pub_bf16, void *out_bf16, void *stream);
+int mxa2a_run_allreduce_unfused(mxa2a_plan *plan, const void *A, const void *A_scale, const void *B,
+                                const void *B_scale, const void *const *recv, void *pub_bf16, void *out_bf16,
+                                void *stream);
 
 /*
  * The fused path: one persistent cooperative kernel stages A_seg[r] rows

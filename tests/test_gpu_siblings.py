@@ -1,10 +1,11 @@
 """GPU parity of the sibling fused operators through the C ABI: AllGather +
-GEMM and GEMM + ReduceScatter (the performance optimisation guide, sections
-3.1 and 3.2) against the CPU oracle.
+GEMM, GEMM + ReduceScatter and GEMM + AllReduce (one-shot) (the performance
+optimisation guide, sections 3.1 to 3.3) against the CPU oracle.
 
 Gates.  AllGather + GEMM, and the blocks GEMM + ReduceScatter sends, are GEMM
 outputs: per element |gpu - ref| <= 1e-2 + 1e-2*|ref|, as for the all-to-all.
-The reduced output adds one term: this rank's partial is rounded to BF16
+The reduced output (of the reduce-scatter and of the all-reduce) adds one
+term: this rank's partial is rounded to BF16
 before the sum (the operation's definition), and where the fp32 accumulation
 lands on the other side of a BF16 rounding midpoint than the exact product,
 the rounded partial differs by one BF16 spacing of |P| (2^(floor(log2|P|)-7)),
@@ -236,3 +237,64 @@ def test_reduce_scatter_argument_errors():
         _status_ok(p)
     with pytest.raises(mxa2a.Mxa2aError):
         mxa2a.ReduceScatterPlan(3, 3, 384, 384, 272)            # rank out of range
+
+
+# --- GEMM + AllReduce (one-shot) -----------------------------------------------------
+
+def _ar_run(p, dev, w, fused):
+    A, S, B, Bs, recv = dev
+    pub = torch.full((w.M, w.N), -1, dtype=torch.int16, device="cuda")
+    out = torch.full((w.M, w.N), -1, dtype=torch.int16, device="cuda")
+    (p.run if fused else p.run_unfused)(A, S, B, Bs, recv, pub, out)
+    torch.cuda.synchronize()
+    _status_ok(p)
+    return gu.host_bits(pub), gu.host_bits(out)
+
+
+def _ar_check(w):
+    x = inputs.make_allreduce_inputs(w)
+    dev = _rs_dev(x)
+    with mxa2a.AllReducePlan(w.R, w.rank, w.M, w.K, w.N) as p:
+        p.set_option(mxa2a.MXA2A_OPT_TIMEOUT_NS, 500_000_000)
+        assert p.get_option(mxa2a.MXA2A_INFO_KIND) == mxa2a.MXA2A_KIND_ALLREDUCE
+        pub_f, out_f = _ar_run(p, dev, w, True)
+        pub_u, out_u = _ar_run(p, dev, w, False)
+    pub_r, out_r = oracle.gemm_allreduce(x["A"], x["A_scale"], x["B"], x["B_scale"],
+                                         [None if r is None else r.numpy() for r in x["recv"]], w.R, w.rank)
+    gu.assert_parity(pub_f, pub_r, f"{w.name} pub")
+    _assert_out_parity(out_f, out_r, pub_r, f"{w.name} out")
+    assert np.array_equal(pub_f, pub_u), "pub fused != unfused"
+    assert np.array_equal(out_f, out_u), "out fused != unfused"
+
+
+@pytest.mark.parametrize("w", [inputs.AR_WORKLOADS[0],
+                               inputs.AllReduceWorkload("ar_r2_m320_k256_n528", 2, 0, 320, 256, 528, 52),
+                               inputs.AllReduceWorkload("ar_r5_m128_k128_n64", 5, 4, 128, 128, 64, 53),
+                               inputs.AllReduceWorkload("ar_r1_m64_k256_n256", 1, 0, 64, 256, 256, 54)],
+                         ids=lambda w: w.name)
+def test_allreduce_small_against_oracle(w):
+    _ar_check(w)
+
+
+def test_allreduce_full_size():
+    """The benchmark's all-reduce workload (rank 1 of 4, 2048 x 4096 x 4096) in full."""
+    _ar_check(inputs.AR_WORKLOADS[1])
+
+
+def test_allreduce_argument_errors():
+    w = inputs.AR_WORKLOADS[0]
+    x = inputs.make_allreduce_inputs(w)
+    A, S, B, Bs, recv = _rs_dev(x)
+    pub = torch.empty((w.M, w.N), dtype=torch.int16, device="cuda")
+    out = torch.empty((w.M, w.N), dtype=torch.int16, device="cuda")
+    with mxa2a.AllReducePlan(w.R, w.rank, w.M, w.K, w.N) as p:
+        bad = list(recv)
+        bad[(w.rank + 1) % w.R] = None
+        with pytest.raises(mxa2a.Mxa2aError) as e:
+            p.run(A, S, B, Bs, bad, pub, out)
+        assert e.value.code == mxa2a.MXA2A_ERR_NULL_PTR
+        with pytest.raises(mxa2a.Mxa2aError) as e:      # the reduce-scatter call on this kind
+            mxa2a.mxa2a_run_reduce_scatter(p.handle, A, S, B, Bs, recv, [None] * w.R, out)
+        assert e.value.code in (mxa2a.MXA2A_ERR_INVALID_OPTION, mxa2a.MXA2A_ERR_NULL_PTR)
+        torch.cuda.synchronize()
+        _status_ok(p)
