@@ -984,12 +984,12 @@ __device__ void copy_role(const GemmParams& p, SmemCtl* ctl, int lane) {
 // word (kbg, n) of the atoms = the 4 E8M0 bytes of column n for 128-wide K
 // block kbg, at (n%32)*4 + (n%128)/32 of atom (kbg, n/128); columns past N
 // get 0.
-__device__ void pack_sfb_slice(const GemmParams& p) {
+__device__ void pack_sfb_slice(const GemmParams& p, int tid, int nthreads) {
     uint32_t* sfb = reinterpret_cast<uint32_t*>(const_cast<uint8_t*>(p.sfb));   // written only here
     const int cols = p.Ng2 * 128;
     const long long total = (long long)(p.K / BK) * cols;
-    const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += stride) {
+    const long long stride = (long long)gridDim.x * nthreads;
+    for (long long i = blockIdx.x * (long long)nthreads + tid; i < total; i += stride) {
         const int n = (int)(i % cols);
         const int kbg = (int)(i / cols);
         const uint32_t v = n < p.N ? ld_nc_u32(p.B_scale + (size_t)n * (p.K / 32) + (size_t)kbg * 4) : 0u;
@@ -1080,12 +1080,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every CTA packs its slice of the B scales (and, direct, of the A
         // scales); the producers wait for all of them before their first load
         // (the CTAs are co-resident)
-        if (p.sfb_inline) pack_sfb_slice(p);
-        if (!kFused && p.direct) pack_sfa_slice(p);
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            __threadfence();
-            red_release_add_u64(p.flags + FlagLayout::sfb_done(p.bn, p.R), 1ull);
+        if (kFused) {
+            // the copy warps start staging at once; the other 12 warps pack
+            constexpr int kPackThreads = kThreads - kCopyWarps * 32;
+            if (!is_copy_warp(warp)) {
+                const int pw = warp < 10 ? warp : warp - 2;   // warps 0..9, 12, 13 -> 0..11
+                if (p.sfb_inline) pack_sfb_slice(p, pw * 32 + lane, kPackThreads);
+                named_barrier_sync(3, kPackThreads);
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    red_release_add_u64(p.flags + FlagLayout::sfb_done(p.bn, p.R), 1ull);
+                }
+            }
+        } else {
+            if (p.sfb_inline) pack_sfb_slice(p, threadIdx.x, blockDim.x);
+            if (p.direct) pack_sfa_slice(p);
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                __threadfence();
+                red_release_add_u64(p.flags + FlagLayout::sfb_done(p.bn, p.R), 1ull);
+            }
         }
     }
 
