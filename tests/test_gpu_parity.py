@@ -583,3 +583,42 @@ def test_full_size_workloads_sampled(idx):
         assert np.array_equal(got_f, got_u), "fused and unfused differ"
     # every output written (no NaN left from the 0xFFFF fill), magnitudes sane
     assert not np.isnan(gu.bits_to_f64(got_f)).any()
+
+
+def _random_shapes(n, seed):
+    """Seeded legal shapes: R 1..6, kPerRank 128..512, commMSize 64..256 in
+    steps of 64, M 1..8 staging steps, N 16..592 in steps of 16, buffer_num
+    1..4 and at least the staging steps one 128-row tile spans (2 when
+    commMSize is not a multiple of 128).  The rules are restated here so the
+    shapes exist before the library is loaded."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        R = int(rng.integers(1, 7))
+        ka = 128 * int(rng.integers(1, 5))
+        cm = 64 * int(rng.integers(1, 5))
+        M = cm * int(rng.integers(1, 9))
+        N = 16 * int(rng.integers(1, 38))
+        bn = int(rng.integers(1, 5))
+        if bn < (1 if cm % 128 == 0 else 2):
+            continue
+        out.append((R, M, ka, N, cm, bn, int(rng.integers(0, 1 << 30))))
+    return out
+
+
+@pytest.mark.parametrize("shape", _random_shapes(16, 2026), ids=lambda s: "r{}_m{}_ka{}_n{}_cm{}_bn{}".format(*s[:6]))
+def test_random_shapes_all_paths(shape):
+    """A seeded sweep of legal shapes: fused, unfused and direct against the
+    oracle, and bitwise equal to each other at the same K split."""
+    R, M, ka, N, cm, bn, seed = shape
+    assert mxa2a.mxa2a_validate(R, M, ka, N, cm, bn) == mxa2a.MXA2A_OK
+    w = inputs.Workload("sweep", R, M, ka, N, cm, bn, seed)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w) as p:
+        p.set_option(mxa2a.MXA2A_OPT_SPLIT_K, p.get_option(mxa2a.MXA2A_INFO_SPLITS))   # one split for all paths
+        got = {f: gu.host_bits(gu.run_gpu(p, d, M, N, fused=f)) for f in (True, False, "direct")}
+        torch.cuda.synchronize()
+        _status_ok(p)
+    gu.assert_parity(got[True], gu.oracle_full(x), f"sweep {shape}")
+    assert np.array_equal(got[True], got[False]) and np.array_equal(got[True], got["direct"])

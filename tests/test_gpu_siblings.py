@@ -298,3 +298,29 @@ def test_allreduce_argument_errors():
         assert e.value.code in (mxa2a.MXA2A_ERR_INVALID_OPTION, mxa2a.MXA2A_ERR_NULL_PTR)
         torch.cuda.synchronize()
         _status_ok(p)
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_random_sibling_shapes(seed):
+    """Seeded shapes for the three sibling operators against their oracles."""
+    rng = np.random.default_rng(700 + seed)
+    R = int(rng.integers(1, 6))
+    rows = 64 * int(rng.integers(1, 5))
+    K = 128 * int(rng.integers(1, 5))
+    N = 16 * int(rng.integers(1, 40))
+    cm = 64 * int(rng.integers(1, 3))
+    if rows % cm:
+        cm = 64
+    bn = 2
+    ag = inputs.AllGatherWorkload("ag_sweep", R, rows, K, N, cm, bn, 710 + seed)
+    x = inputs.make_allgather_inputs(ag)
+    with _ag_plan(ag) as p:
+        got_f = _ag_run(p, _ag_dev(x), ag.M, ag.N, "fused")
+        got_u = _ag_run(p, _ag_dev(x), ag.M, ag.N, "unfused")
+    gu.assert_parity(got_f, oracle.gemm_allgather(x["A_blk"], x["A_scale_blk"], x["B"], x["B_scale"]), "ag sweep")
+    assert np.array_equal(got_f, got_u)
+    rank = int(rng.integers(0, R))
+    rs = inputs.ReduceScatterWorkload("rs_sweep", R, rank, R * rows, K, N, 720 + seed)
+    xr = inputs.make_reduce_scatter_inputs(rs)
+    _rs_check(rs, _rs_dev(xr), xr)
+    _ar_check(inputs.AllReduceWorkload("ar_sweep", R, rank, rows, K, N, 730 + seed))
