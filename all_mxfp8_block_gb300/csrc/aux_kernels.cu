@@ -147,6 +147,56 @@ cudaError_t launch_rs_reduce(const RsArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Several copies in one launch, by the SMs (blockIdx.y = the copy): each a
+// run of 16-byte vectors between memory the device can address (device
+// memory, or pinned host memory through its device address).
+struct CopyList {
+    static constexpr int kMax = 160;
+    int n;
+    const uint4* src[kMax];
+    uint4* dst[kMax];
+    long long n16[kMax];
+};
+
+__global__ void copy_list_kernel(const __grid_constant__ CopyList l) {
+    const int c = blockIdx.y;
+    const uint4* __restrict__ s = l.src[c];
+    uint4* __restrict__ d = l.dst[c];
+    const long long n = l.n16[c];
+    constexpr int U = 4;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += stride * U) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (i + u * stride < n) v[u] = s[i + u * stride];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (i + u * stride < n) d[i + u * stride] = v[u];
+    }
+}
+
+// n copies (n <= 160; addresses 16-byte aligned, sizes multiples of 16)
+cudaError_t launch_copy_list(int n, const void* const* src, void* const* dst, const size_t* bytes,
+                             cudaStream_t stream) {
+    CopyList l;
+    l.n = n;
+    long long biggest = 0;
+    for (int i = 0; i < n; ++i) {
+        l.src[i] = static_cast<const uint4*>(src[i]);
+        l.dst[i] = static_cast<uint4*>(dst[i]);
+        l.n16[i] = (long long)(bytes[i] / 16);
+        biggest = l.n16[i] > biggest ? l.n16[i] : biggest;
+    }
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long want = (biggest + 256 * 4 - 1) / (256 * 4);
+    const int gx = (int)(want < 1 ? 1 : (want > 8LL * sms ? 8LL * sms : want));
+    copy_list_kernel<<<dim3(gx, n), 256, 0, stream>>>(l);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_l2_flush(void* buf, size_t bytes, cudaStream_t stream) {
     const long long n16 = (long long)(bytes / 16);
     l2_flush_kernel<<<grid_for(n16, 256), 256, 0, stream>>>(reinterpret_cast<uint4*>(buf), n16);

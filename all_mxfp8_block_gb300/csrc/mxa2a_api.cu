@@ -159,6 +159,12 @@ struct mxa2a_plan {
     size_t rs_cnt_bytes = 0;
 };
 
+namespace mxa2a {
+// aux_kernels.cu: several copies by the SMs in one launch
+cudaError_t launch_copy_list(int n, const void* const* src, void* const* dst, const size_t* bytes,
+                             cudaStream_t stream);
+}  // namespace mxa2a
+
 namespace {
 
 void derive(mxa2a_plan* p) {
@@ -273,6 +279,17 @@ void derive(mxa2a_plan* p) {
 }
 
 bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+// The device address of pinned (page-locked) host memory, or NULL for any
+// other pointer (pageable host memory is left to the DMA copies).
+const void* host_device_view(const void* h) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
 
 int check_device(mxa2a_plan* p) {
     int dev = -1;
@@ -843,13 +860,17 @@ int mxa2a_run_host(mxa2a_plan* p, const void* const* A_seg_h, const void* const*
     cudaStream_t s = static_cast<cudaStream_t>(stream_v);
     const void* dA[kMaxSegments];
     const void* dS[kMaxSegments];
+    const void* src[2 * kMaxSegments + 2];
+    void* dst[2 * kMaxSegments + 2];
+    size_t len[2 * kMaxSegments + 2];
+    int n = 0;
     uint8_t* cur = p->io;
     for (int r = 0; r < p->nseg; ++r) {
         dA[r] = cur;
-        if (cudaMemcpyAsync(cur, A_seg_h[r], a_b, cudaMemcpyHostToDevice, s) != cudaSuccess) return MXA2A_ERR_CUDA;
+        src[n] = A_seg_h[r], dst[n] = cur, len[n++] = a_b;
         cur += a_s;
         dS[r] = cur;
-        if (cudaMemcpyAsync(cur, A_sf_h[r], asf_b, cudaMemcpyHostToDevice, s) != cudaSuccess) return MXA2A_ERR_CUDA;
+        src[n] = A_sf_h[r], dst[n] = cur, len[n++] = asf_b;
         cur += asf_s;
     }
     uint8_t* dB = cur;
@@ -857,12 +878,32 @@ int mxa2a_run_host(mxa2a_plan* p, const void* const* A_seg_h, const void* const*
     uint8_t* dBs = cur;
     cur += align_up(bsf_b, 256);
     uint8_t* dC = cur;
-    if (cudaMemcpyAsync(dB, B_h, b_b, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(dBs, B_sf_h, bsf_b, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return MXA2A_ERR_CUDA;
+    src[n] = B_h, dst[n] = dB, len[n++] = b_b;
+    src[n] = B_sf_h, dst[n] = dBs, len[n++] = bsf_b;
+    // Pinned host buffers are copied by the SMs in one launch (the device reads
+    // them through their device addresses); otherwise one DMA copy per buffer.
+    const void* view[2 * kMaxSegments + 2];
+    bool by_sms = true;
+    for (int i = 0; i < n && by_sms; ++i) {
+        view[i] = host_device_view(src[i]);
+        by_sms = view[i] && aligned(view[i], 16) && len[i] % 16 == 0;
+    }
+    if (by_sms) {
+        if ((rc = cuda_rc(launch_copy_list(n, view, dst, len, s)))) return rc;
+    } else {
+        for (int i = 0; i < n; ++i)
+            if (cudaMemcpyAsync(dst[i], src[i], len[i], cudaMemcpyHostToDevice, s) != cudaSuccess)
+                return MXA2A_ERR_CUDA;
+    }
     rc = run_impl(p, dA, dS, dB, dBs, dC, stream_v, kRunFused);
     if (rc) return rc;
-    if (cudaMemcpyAsync(C_h, dC, c_b, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MXA2A_ERR_CUDA;
+    void* c_view = const_cast<void*>(host_device_view(C_h));
+    if (c_view && aligned(c_view, 16)) {
+        const void* c_src = dC;
+        if ((rc = cuda_rc(launch_copy_list(1, &c_src, &c_view, &c_b, s)))) return rc;
+    } else if (cudaMemcpyAsync(C_h, dC, c_b, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+        return MXA2A_ERR_CUDA;
+    }
     return MXA2A_OK;
 }
 

@@ -269,9 +269,11 @@ int mxa2a_run_unfused(mxa2a_plan *plan, const void *const *A_seg, const void *co
 /*
  * End-to-end variant with HOST buffers (same layouts): copies the inputs to
  * plan-owned device buffers (allocated on the first call), runs the fused
- * path and copies C back, all asynchronously on stream.  Host buffers should
- * be pinned for the copies to overlap; the caller synchronises the stream
- * before reading C_bf16.
+ * path and copies C back, all asynchronously on stream; the caller
+ * synchronises the stream before reading C_bf16.  When every input buffer is
+ * pinned (page-locked, as cudaHostAlloc or cudaHostRegister give) the SMs
+ * copy them in one launch through their device addresses, and likewise C
+ * when it is pinned; pageable buffers go through one DMA copy each.
  */
 int mxa2a_run_host(mxa2a_plan *plan, const void *const *A_seg_host, const void *const *A_scale_seg_host,
                    const void *B_host, const void *B_scale_host, void *C_bf16_host, void *stream);

@@ -470,6 +470,30 @@ def test_non_default_stream_and_host_entry():
     gu.assert_parity(got, gu.oracle_full(x), "stream")
 
 
+def test_host_entry_pinned_and_pageable_same_bits():
+    """mxa2a_run_host with pinned host buffers (copied by the SMs) and with
+    pageable ones (DMA copies), and a mix: the same bits as the device entry."""
+    w = inputs.Workload("hostcopy", 3, 384, 256, 400, 128, 2, 97)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w) as p:
+        ref = gu.host_bits(gu.run_gpu(p, d, w.M, w.N))
+        outs = []
+        for pin_in, pin_out in ((True, True), (False, False), (True, False), (False, True)):
+            cv = (lambda t: t.pin_memory()) if pin_in else (lambda t: t.clone())
+            hA = [cv(a) for a in x["A_seg"]]
+            hS = [cv(s) for s in x["A_scale_seg"]]
+            hC = torch.full((w.M, w.N), -1, dtype=torch.int16)
+            if pin_out:
+                hC = hC.pin_memory()
+            p.run_host(hA, hS, cv(x["B"]), cv(x["B_scale"]), hC)
+            torch.cuda.synchronize()
+            _status_ok(p)
+            outs.append(hC.numpy().view(np.uint16).copy())
+    for o in outs:
+        assert np.array_equal(o, ref)
+
+
 def test_zero_A_gives_zero():
     w = inputs.Workload("zero", 2, 128, 128, 256, 64, 2, 0)
     x = inputs.make_inputs(w)
