@@ -865,12 +865,24 @@ int mxa2a_run_host(mxa2a_plan* p, const void* const* A_seg_h, const void* const*
     size_t len[2 * kMaxSegments + 2];
     int n = 0;
     uint8_t* cur = p->io;
+    // Pinned segments are read in place by the fused kernel's staging copies
+    // (the exchange then reads host memory through the device's link to it).
+    bool a_in_place = true;
+    for (int r = 0; r < p->nseg && a_in_place; ++r) {
+        dA[r] = host_device_view(A_seg_h[r]);
+        dS[r] = host_device_view(A_sf_h[r]);
+        a_in_place = dA[r] && dS[r] && aligned(dA[r], 16) && aligned(dS[r], 4);
+    }
     for (int r = 0; r < p->nseg; ++r) {
-        dA[r] = cur;
-        src[n] = A_seg_h[r], dst[n] = cur, len[n++] = a_b;
+        if (!a_in_place) {
+            dA[r] = cur;
+            src[n] = A_seg_h[r], dst[n] = cur, len[n++] = a_b;
+        }
         cur += a_s;
-        dS[r] = cur;
-        src[n] = A_sf_h[r], dst[n] = cur, len[n++] = asf_b;
+        if (!a_in_place) {
+            dS[r] = cur;
+            src[n] = A_sf_h[r], dst[n] = cur, len[n++] = asf_b;
+        }
         cur += asf_s;
     }
     uint8_t* dB = cur;

@@ -270,10 +270,14 @@ int mxa2a_run_unfused(mxa2a_plan *plan, const void *const *A_seg, const void *co
  * End-to-end variant with HOST buffers (same layouts): copies the inputs to
  * plan-owned device buffers (allocated on the first call), runs the fused
  * path and copies C back, all asynchronously on stream; the caller
- * synchronises the stream before reading C_bf16.  When every input buffer is
- * pinned (page-locked, as cudaHostAlloc or cudaHostRegister give) the SMs
- * copy them in one launch through their device addresses, and likewise C
- * when it is pinned; pageable buffers go through one DMA copy each.
+ * synchronises the stream before reading C_bf16.  Pinned host buffers
+ * (page-locked, as cudaHostAlloc or cudaHostRegister give) are used through
+ * their device addresses: pinned A segments and scales are read in place by
+ * the fused kernel's staging copies (the exchange then comes from host
+ * memory), pinned B and B_scale are copied by the SMs in one launch, and a
+ * pinned C is written back the same way; pageable buffers go through one DMA
+ * copy each.  The host buffers must stay unchanged until the stream has
+ * passed the run.
  */
 int mxa2a_run_host(mxa2a_plan *plan, const void *const *A_seg_host, const void *const *A_scale_seg_host,
                    const void *B_host, const void *B_scale_host, void *C_bf16_host, void *stream);
