@@ -30,7 +30,21 @@
 //            per CTA take copy tasks (step, segment, chunk) in step order,
 //            wait for the slot's credit, copy the rows of A_seg[r] and their
 //            scales, publish.  (Warp 13 idles: it would share an SM
-//            sub-partition with the MMA issuer.)
+//            sub-partition with the MMA issuer.)  In the kernel without
+//            staging these warps sum a GEMM + ReduceScatter's (or one-shot
+//            AllReduce's) own rows with the received partials once the
+//            epilogue has stored them.
+//
+// Prologue: every CTA packs a slice of the B scales into MMA atoms (and, for
+// the direct read, of the A scales) and counts itself on a grid counter that
+// the producers wait for (the launch is cooperative); in the fused kernel the
+// copy warps skip the pack and start staging at once.
+//
+// The same kernels serve the sibling operators: the all-gather stages row
+// blocks in K slices (the input buffer and column of a slice come from
+// seg_row / seg_ld / seg_col0), and the reduce-scatter and all-reduce route
+// each finished tile in the epilogue (peers' rows to their send buffers, the
+// own rows or the published partial through a tensor map each).
 //
 // Credits (the pages' per-slot signals with credit return, performance guide
 // 1.1/1.3, kept per segment as its fine-grained signals suggest) are
