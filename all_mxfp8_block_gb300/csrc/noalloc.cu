@@ -154,7 +154,8 @@ extern "C" int mxa2a_run_noalloc(int R, int64_t M, int64_t kPerRank, int64_t N, 
     if (scratch_address(dev, &scratch) != cudaSuccess) return MXA2A_ERR_CUDA;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
 
-    // plan: 128x256 tiles, no K split, the same staging chunking as a plan's
+    // plan: 128x256 tiles, no K split; staging chunks of about 8 KiB (a plan
+    // sizes them from the step and the SM count instead; same bits, other timing)
     const int64_t K = (int64_t)R * kPerRank;
     GemmParams g;
     std::memset(&g, 0, sizeof g);

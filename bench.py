@@ -38,7 +38,9 @@ if ROOT not in sys.path:
 
 METRIC = "fused MXFP8 a2a-GEMM TFLOP/s and % of roofline (1 GB300)"
 UNIT = "TFLOP/s"
-DEFAULT_WORKLOAD = 1          # the 4-segment 2048 x 4096 x 4096 problem
+DEFAULT_WORKLOAD = 3          # the largest problem: 8 segments, 8192 x 8192 x 8192
+CONFIG_WORKLOADS = (1, 2, 3, 4)   # the tensor-bound and the HBM-bound problems reported beside it
+ABLATION_WORKLOAD = 1         # the 2048 x 4096 x 4096 problem: the ring limits it the most
 FP8_OVER_BF16 = 2.0           # nominal dense fp8 : bf16 tensor rate (4.5 : 2.25 PFLOP/s)
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
@@ -271,11 +273,12 @@ def time_tiny_graph(dev, runs: int = 200):
     return out
 
 
-def time_siblings(dev, stream, flush, flush_bytes, steps, warmup):
+def time_siblings(dev, stream, flush, flush_bytes, steps, warmup, with_allreduce=True):
     """Mean ms per call of the sibling operators' fused and unfused paths on
     their benchmark workloads (AllGather + GEMM: 4 blocks of 512 rows, K = N =
-    4096; GEMM + ReduceScatter and GEMM + AllReduce: rank 1 of 4, 2048 x 4096
-    x 4096), each call after an L2 flush, CUDA events around each call."""
+    4096; GEMM + ReduceScatter and, with_allreduce, GEMM + AllReduce: rank 1 of
+    4, 2048 x 4096 x 4096), each call after an L2 flush, CUDA events around
+    each call."""
     import torch
     from all_mxfp8_block_gb300 import inputs, mxa2a
 
@@ -330,6 +333,8 @@ def time_siblings(dev, stream, flush, flush_bytes, steps, warmup):
     out["gemm_reduce_scatter"] = {"workload": w.name, "R": w.R, "rank": w.rank, "M": w.M, "K": w.K, "N": w.N,
                                   **res, "value": tf, "unit": UNIT, "roofline_frac": tf / peak, "steps": steps}
     del A, S, B, Bs, recv, send, o
+    if not with_allreduce:
+        return out
     w = inputs.AR_WORKLOADS[1]
     x = inputs.make_allreduce_inputs(w)
     A, S, B, Bs = (x[k].to(dev) for k in ("A", "A_scale", "B", "B_scale"))
@@ -368,6 +373,171 @@ def run_siblings_only(args):
     return 0
 
 
+def _device_inputs(x, dev):
+    return ([a.to(dev) for a in x["A_seg"]], [s.to(dev) for s in x["A_scale_seg"]],
+            x["B"].to(dev), x["B_scale"].to(dev))
+
+
+def make_timed_loop(dev, stream, flush, flush_bytes, ws):
+    """timed(fn, args, steps, warmup, sampler) -> per-step ms: every step after
+    an L2 flush (outside the events), CUDA events on the launch stream around
+    the library call; ranks barrier-aligned around the timed region."""
+    import torch
+    import torch.distributed as dist
+    from all_mxfp8_block_gb300 import mxa2a
+
+    def timed(fn, fargs, steps, warmup, sampler=None):
+        for _ in range(warmup):
+            mxa2a.mxa2a_l2_flush(flush, flush_bytes, stream)
+            fn(*fargs, stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        ctx = sampler if sampler is not None else _Null()
+        with ctx:
+            for i in range(steps):
+                mxa2a.mxa2a_l2_flush(flush, flush_bytes, stream)
+                ev[i][0].record(stream)
+                fn(*fargs, stream)
+                ev[i][1].record(stream)
+            torch.cuda.synchronize(dev)
+        if ws > 1:
+            dist.barrier()
+        return [a.elapsed_time(b) for a, b in ev]
+    return timed
+
+
+def roofline_of(w, step_s, kernel_s):
+    """t_roof = max(2MNK / MXFP8 peak, bytes_alg / HBM); the fraction of the
+    bound's peak the fused kernel reaches, and t_roof / t_step."""
+    bf16_tf, hbm, _ = measured_peaks()
+    p_fp8 = bf16_tf * FP8_OVER_BF16
+    t_roof, bound = roofline_terms(w, p_fp8, hbm)
+    if bound == "tensor":
+        achieved, peak, unit = w.flops / kernel_s / 1e12, p_fp8, "TFLOP/s"
+    else:
+        achieved, peak, unit = w.bytes_alg / kernel_s / 1e9, hbm, "GB/s"
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "t_roof_us": t_roof * 1e6, "roofline_pct": 100.0 * t_roof / step_s}
+
+
+def time_config(dev, timed, w, steps, warmup):
+    """One problem size: fused step, fused kernel (the library's events around
+    the GEMM launch), unfused step; the roofline fraction of the fused kernel."""
+    import torch
+    from all_mxfp8_block_gb300 import inputs, mxa2a
+    x = inputs.make_inputs(w)
+    dA, dS, dB, dBs = _device_inputs(x, dev)
+    C = torch.empty((w.M, w.N), dtype=torch.int16, device=dev)
+    with mxa2a.Plan(w.R, w.M, w.kPerRank, w.N, w.commMSize, w.buffer_num) as plan:
+        plan.set_option(mxa2a.MXA2A_OPT_RECORD_EVENTS, min(4096, steps))
+        fused = timed(plan.run, (dA, dS, dB, dBs, C), steps, warmup)
+        kern = plan.kernel_times(min(4096, steps))
+        plan.set_option(mxa2a.MXA2A_OPT_RECORD_EVENTS, 0)
+        unfused = timed(plan.run_unfused, (dA, dS, dB, dBs, C), steps, warmup)
+        st = plan.status()
+        if st["code"] != 0:
+            raise RuntimeError(f"device status after timing {w.name}: {st}")
+        info = {"splits": plan.get_option(mxa2a.MXA2A_INFO_SPLITS),
+                "cta_pair": plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR),
+                "cta_pair_unfused": plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED)}
+    return summarize_config(w, fused, kern, unfused, steps, info)
+
+
+def summarize_config(w, fused_ms, kern_ms, unfused_ms, steps, info):
+    f = statistics.mean(fused_ms) * 1e-3
+    k = statistics.mean(kern_ms) * 1e-3 if kern_ms else f
+    u = statistics.mean(unfused_ms) * 1e-3
+    rf = roofline_of(w, f, k)
+    return {"workload": w.name, "steps": steps, "fused_step_us": f * 1e6, "fused_kernel_us": k * 1e6,
+            "unfused_step_us": u * 1e6, "fused_faster": f < u, "fused_tflops": w.flops / f / 1e12,
+            "bound": rf["bound"], "frac": rf["frac"], "frac_unit": rf["unit"], "achieved": rf["achieved"],
+            "peak": rf["peak"], "roofline_pct": rf["roofline_pct"], "t_roof_us": rf["t_roof_us"], **info}
+
+
+def time_credit_ablation(dev, timed, steps, warmup, skew_ns):
+    """The staging-protocol ablation on the problem the ring limits most:
+    per-(slot, segment) credits against the whole-step protocol, each with and
+    without slowed copies on every 4th CTA."""
+    import torch
+    from all_mxfp8_block_gb300 import inputs, mxa2a
+    w = inputs.workload(ABLATION_WORKLOAD)
+    x = inputs.make_inputs(w)
+    dA, dS, dB, dBs = _device_inputs(x, dev)
+    C = torch.empty((w.M, w.N), dtype=torch.int16, device=dev)
+    out = {"workload": w.name, "skew_ns": skew_ns, "steps": steps,
+           "what": "fused ms per step; skew: the copy workers of every 4th CTA wait skew_ns before each copy task"}
+    with mxa2a.Plan(w.R, w.M, w.kPerRank, w.N, w.commMSize, w.buffer_num) as plan:
+        if plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR):
+            plan.set_option(mxa2a.MXA2A_OPT_CTA_PAIR, 0)   # the protocol options live in the single-CTA kernel
+        for sc, name in ((0, "per_segment"), (1, "whole_step")):
+            for skew in (0, skew_ns):
+                plan.set_option(mxa2a.MXA2A_OPT_STEP_CREDITS, sc)
+                plan.set_option(mxa2a.MXA2A_OPT_COPY_SKEW_NS, skew)
+                ms = timed(plan.run, (dA, dS, dB, dBs, C), steps, warmup)
+                out[name + ("_skew_ms" if skew else "_ms")] = statistics.mean(ms)
+        st = plan.status()
+        if st["code"] != 0:
+            raise RuntimeError(f"device status after the credit ablation: {st}")
+    return out
+
+
+def time_e2e(dev, stream, plan, x, w, steps, warmup, ws):
+    """End to end through mxa2a_run_host with pinned host buffers (host
+    wall clock per step: the copies in, the run, the copy of C out, the stream
+    sync), and beside it the host link alone: the same bytes moved by one
+    pinned cudaMemcpyAsync per buffer, timed the same way."""
+    import torch
+    import torch.distributed as dist
+    hA = [a.pin_memory() for a in x["A_seg"]]
+    hS = [s.pin_memory() for s in x["A_scale_seg"]]
+    hB, hBs = x["B"].pin_memory(), x["B_scale"].pin_memory()
+    hC = torch.empty((w.M, w.N), dtype=torch.int16).pin_memory()
+    for _ in range(warmup):
+        plan.run_host(hA, hS, hB, hBs, hC, stream)
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        plan.run_host(hA, hS, hB, hBs, hC, stream)
+        stream.synchronize()
+    t_e2e = time.perf_counter() - t0
+    if ws > 1:
+        dist.barrier()
+    t_e2e_max, fl = reduce_max_sum(t_e2e, float(w.flops) * steps, dev if ws > 1 else None)
+    h2d = sum(a.numel() for a in hA) + sum(s.numel() for s in hS) + hB.numel() + hBs.numel()
+    d2h = hC.numel() * 2
+    # the link alone: device buffers of the same sizes, one async copy per buffer
+    srcs = hA + hS + [hB, hBs]
+    dsts = [torch.empty_like(h, device=dev) for h in srcs]
+    dC = torch.empty((w.M, w.N), dtype=torch.int16, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            for d, h in zip(dsts, srcs):
+                d.copy_(h, non_blocking=True)
+            hC.copy_(dC, non_blocking=True)
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            for d, h in zip(dsts, srcs):
+                d.copy_(h, non_blocking=True)
+            hC.copy_(dC, non_blocking=True)
+            stream.synchronize()
+        t_link = time.perf_counter() - t0
+    t_link_max, _ = reduce_max_sum(t_link, 0.0, dev if ws > 1 else None)
+    link_gbs = (h2d + d2h) * steps / t_link_max / 1e9
+    return {"value": fl / t_e2e_max / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h),
+            "timer": "host wall clock per step (h2d copies + run + d2h copy + stream sync)", "steps": steps,
+            "us_per_step": t_e2e_max / steps * 1e6,
+            "link_us_per_step": t_link_max / steps * 1e6, "link_gbs": link_gbs,
+            "link_frac": t_link_max / t_e2e_max,
+            "link_what": "the same h2d + d2h bytes as one pinned cudaMemcpyAsync per buffer, nothing else; "
+                         "link_frac = link-only time / end-to-end time"}
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -386,14 +556,13 @@ def run_ours(args, w):
     mxa2a.load()
 
     x = inputs.make_inputs(w)
-    dA = [a.to(dev) for a in x["A_seg"]]
-    dS = [s.to(dev) for s in x["A_scale_seg"]]
-    dB, dBs = x["B"].to(dev), x["B_scale"].to(dev)
+    dA, dS, dB, dBs = _device_inputs(x, dev)
     C = torch.empty((w.M, w.N), dtype=torch.int16, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_bytes = max(2 * l2, 64 << 20) // 16 * 16
     flush = torch.zeros(flush_bytes // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    timed = make_timed_loop(dev, stream, flush, flush_bytes, ws)
 
     plan = mxa2a.Plan(w.R, w.M, w.kPerRank, w.N, w.commMSize, w.buffer_num)
     plan.set_option(mxa2a.MXA2A_OPT_RECORD_EVENTS, min(4096, max(1, args.steps)))
@@ -404,31 +573,13 @@ def run_ours(args, w):
     if args.group_m:
         plan.set_option(mxa2a.MXA2A_OPT_GROUP_M, args.group_m)
     run = plan.run if args.path == "fused" else plan.run_unfused
-
-    def timed_loop(fn, steps, warmup, sampler=None):
-        for _ in range(warmup):
-            mxa2a.mxa2a_l2_flush(flush, flush_bytes, stream)
-            fn(dA, dS, dB, dBs, C, stream)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        if ws > 1:
-            dist.barrier()
-        torch.cuda.synchronize(dev)
-        ctx = sampler if sampler is not None else _Null()
-        with ctx:
-            for i in range(steps):
-                mxa2a.mxa2a_l2_flush(flush, flush_bytes, stream)
-                ev[i][0].record(stream)
-                fn(dA, dS, dB, dBs, C, stream)
-                ev[i][1].record(stream)
-            torch.cuda.synchronize(dev)
-        if ws > 1:
-            dist.barrier()
-        return [a.elapsed_time(b) for a, b in ev]
+    fargs = (dA, dS, dB, dBs, C)
 
     sampler = ClockSampler(local)
-    step_ms = timed_loop(run, args.steps, args.warmup, sampler)
+    step_ms = timed(run, fargs, args.steps, args.warmup, sampler)
     launches_per_run = plan.get_option(mxa2a.MXA2A_INFO_LAUNCHES)
     kern_ms = plan.kernel_times(min(4096, args.steps))
+    plan.set_option(mxa2a.MXA2A_OPT_RECORD_EVENTS, 0)
     st = plan.status()
     if st["code"] != 0:
         raise RuntimeError(f"device status after the timed region: {st}")
@@ -436,68 +587,52 @@ def run_ours(args, w):
 
     # the other variant, same caliber, for the fused-vs-unfused comparison
     other = plan.run_unfused if args.path == "fused" else plan.run
-    other_steps = min(args.steps, 500)
-    other_ms = timed_loop(other, other_steps, args.warmup)
+    other_steps = min(args.steps, args.other_steps)
+    other_ms = timed(other, fargs, other_steps, args.warmup)
     # the direct-read ablation: A read in place, no exchange (same caliber)
-    direct_ms = None
-    if not plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED):
-        direct_ms = timed_loop(plan.run_direct, other_steps, args.warmup)
-
-    # the staging protocol ablation (fused): per-segment credits against the
-    # whole-step protocol, each with and without slowed copies on every 4th CTA
-    credit_ablation = None
-    if args.path == "fused" and not args.no_ablation and not plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR):
-        credit_ablation = {"skew_ns": args.skew_ns, "steps": min(other_steps, 200),
-                           "what": "fused ms per step; skew: the copy workers of every 4th CTA wait skew_ns "
-                                   "before each copy task"}
-        for sc, name in ((0, "per_segment"), (1, "whole_step")):
-            for skew in (0, args.skew_ns):
-                plan.set_option(mxa2a.MXA2A_OPT_STEP_CREDITS, sc)
-                plan.set_option(mxa2a.MXA2A_OPT_COPY_SKEW_NS, skew)
-                ms = timed_loop(plan.run, credit_ablation["steps"], args.warmup)
-                credit_ablation[name + ("_skew_ms" if skew else "_ms")] = sum(ms) / len(ms)
-        plan.set_option(mxa2a.MXA2A_OPT_STEP_CREDITS, 0)
-        plan.set_option(mxa2a.MXA2A_OPT_COPY_SKEW_NS, 0)
-        st = plan.status()
-        if st["code"] != 0:
-            raise RuntimeError(f"device status after the credit ablation: {st}")
-
-    # the sibling fused operators at the headline's size, same caliber
-    siblings = None
-    if not args.no_siblings:
-        siblings = time_siblings(dev, stream, flush, flush_bytes, min(other_steps, 200), args.warmup)
+    direct_ms = timed(plan.run_direct, fargs, other_steps, args.warmup)
+    st = plan.status()
+    if st["code"] != 0:
+        raise RuntimeError(f"device status after the comparison paths: {st}")
 
     t_local = sum(step_ms) / 1e3
     t_max, flops_total = reduce_max_sum(t_local, float(w.flops) * args.steps, dev if ws > 1 else None)
     value = flops_total / t_max / 1e12
     ms_per_step = t_max / args.steps * 1e3
 
-    # end to end through the C ABI with pinned host buffers (copies in the timed region)
+    # end to end through the C ABI with pinned host buffers (copies in the timed
+    # region), with the host link's own time for the same bytes beside it
     e2e = None
     if not args.no_e2e:
-        hA = [a.pin_memory() for a in x["A_seg"]]
-        hS = [s.pin_memory() for s in x["A_scale_seg"]]
-        hB, hBs = x["B"].pin_memory(), x["B_scale"].pin_memory()
-        hC = torch.empty((w.M, w.N), dtype=torch.int16).pin_memory()
-        e2e_steps = min(args.steps, 50)
-        for _ in range(max(3, args.warmup)):
-            plan.run_host(hA, hS, hB, hBs, hC, stream)
-        torch.cuda.synchronize(dev)
-        if ws > 1:
-            dist.barrier()
-        t0 = time.perf_counter()
-        for _ in range(e2e_steps):
-            plan.run_host(hA, hS, hB, hBs, hC, stream)
-            stream.synchronize()
-        t_e2e = time.perf_counter() - t0
-        if ws > 1:
-            dist.barrier()
-        t_e2e_max, fl = reduce_max_sum(t_e2e, float(w.flops) * e2e_steps, dev if ws > 1 else None)
-        h2d = (sum(a.numel() for a in hA) + sum(s.numel() for s in hS) + hB.numel() + hBs.numel())
-        e2e = {"value": fl / t_e2e_max / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(hC.numel() * 2),
-               "timer": "host wall clock per step (h2d copies + run + d2h copy + stream sync)",
-               "steps": e2e_steps}
+        e2e = time_e2e(dev, stream, plan, x, w, min(args.steps, 50), max(3, args.warmup), ws)
+
+    # every problem size, fused and unfused, same caliber (the headline's own numbers reused)
+    configs = None
+    if not args.no_configs:
+        configs = {}
+        fused_ms = step_ms if args.path == "fused" else other_ms
+        unfused_ms = other_ms if args.path == "fused" else step_ms
+        for idx in CONFIG_WORKLOADS:
+            wc = inputs.workload(idx)
+            if wc.name == w.name:
+                info = {"splits": plan.get_option(mxa2a.MXA2A_INFO_SPLITS),
+                        "cta_pair": plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR),
+                        "cta_pair_unfused": plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED)}
+                configs[wc.name] = summarize_config(wc, fused_ms, kern_ms if args.path == "fused" else [],
+                                                    unfused_ms, args.steps, info)
+            else:
+                configs[wc.name] = time_config(dev, timed, wc, min(args.steps, args.config_steps), args.warmup)
+
+    # the staging protocol ablation (fused) on the problem the ring limits most
+    credit_ablation = None
+    if args.path == "fused" and not args.no_ablation:
+        credit_ablation = time_credit_ablation(dev, timed, min(other_steps, 200), args.warmup, args.skew_ns)
+
+    # the sibling fused operators, same caliber
+    siblings = None
+    if not args.no_siblings:
+        siblings = time_siblings(dev, stream, flush, flush_bytes, min(other_steps, 200), args.warmup,
+                                 with_allreduce=args.with_allreduce)
 
     # the smallest workload, latency-bound: eager calls vs CUDA-graph replay
     tiny_graph = None
@@ -511,7 +646,14 @@ def run_ours(args, w):
     p_fp8 = bf16_tf * FP8_OVER_BF16
     t_roof, bound = roofline_terms(w, p_fp8, hbm)
     kern_avg_s = (sum(kern_ms) / len(kern_ms) / 1e3) if kern_ms else None
-    achieved = w.flops / kern_avg_s / 1e12 if kern_avg_s else None
+    if bound == "tensor":
+        achieved = w.flops / kern_avg_s / 1e12 if kern_avg_s else None
+        peak, r_unit = p_fp8, "TFLOP/s"
+        peak_note = f"{peak_src} bf16 {bf16_tf:.0f} TFLOP/s (burst) x nominal fp8:bf16 ratio 2"
+    else:
+        achieved = w.bytes_alg / kern_avg_s / 1e9 if kern_avg_s else None
+        peak, r_unit = hbm, "GB/s"
+        peak_note = f"{peak_src} HBM copy bandwidth"
 
     if rank != 0:
         if ws > 1:
@@ -519,7 +661,7 @@ def run_ours(args, w):
         return 0
 
     cpu = None
-    if not args.no_cpu_baseline and ws >= 1:
+    if not args.no_cpu_baseline:
         tf, rows, dt, cores = time_oracle(w, x, seconds=args.cpu_seconds)
         cpu = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"rows 0..{rows - 1} of C ({rows} x {w.N} outputs, full K={w.K}), one call, "
@@ -542,20 +684,20 @@ def run_ours(args, w):
                    "l2": f"flushed before every step ({flush_bytes >> 20} MiB write, 2x L2), outside the events",
                    "timer": "CUDA events on the launch stream around each library call"},
         "roofline_pct": 100.0 * t_roof / (ms_per_step / 1e3),
-        "roofline": {"bound": bound, "achieved": achieved, "peak": p_fp8, "unit": "TFLOP/s",
-                     "frac": (achieved / p_fp8) if achieved else None,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": r_unit,
+                     "frac": (achieved / peak) if achieved else None,
                      "traffic": profiled_traffic(w.name),
                      "kernel": "mxgemm_kernel<fused>" if args.path == "fused" else "mxgemm_kernel<unfused>",
                      "kernel_ms_avg": kern_avg_s * 1e3 if kern_avg_s else None,
-                     "peak_note": f"{peak_src} bf16 {bf16_tf:.0f} TFLOP/s (burst) x nominal fp8:bf16 ratio 2",
-                     "t_roof_us": t_roof * 1e6, "hbm_gbs": hbm},
+                     "peak_note": peak_note, "t_roof_us": t_roof * 1e6, "hbm_gbs": hbm},
         "unfused" if args.path == "fused" else "fused": {
             "ms_per_step": sum(other_ms) / len(other_ms), "steps": other_steps,
             "value": w.flops / (sum(other_ms) / len(other_ms) / 1e3) / 1e12},
-        "direct_read": None if direct_ms is None else {
+        "direct_read": {
             "ms_per_step": sum(direct_ms) / len(direct_ms), "steps": other_steps,
             "value": w.flops / (sum(direct_ms) / len(direct_ms) / 1e3) / 1e12,
             "what": "A read in place from the segments (no staging ring, no pack): the exchange's cost"},
+        "configs": configs,
         "credit_ablation": credit_ablation,
         "siblings": siblings,
         "cpu_baseline": cpu,
@@ -592,6 +734,12 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph timing of the smallest workload")
     ap.add_argument("--no-ablation", action="store_true", help="skip the staging-protocol ablation timings")
     ap.add_argument("--no-siblings", action="store_true", help="skip the sibling operators' timings")
+    ap.add_argument("--with-allreduce", action="store_true",
+                    help="also time GEMM + AllReduce (one-shot) among the sibling operators")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other problem sizes' timings")
+    ap.add_argument("--config-steps", type=int, default=200, help="timed steps per other problem size")
+    ap.add_argument("--other-steps", type=int, default=500,
+                    help="timed steps of the unfused and direct-read comparison paths")
     ap.add_argument("--only-siblings", action="store_true",
                     help="time only the sibling operators (one JSON line of their timings, not the benchmark line)")
     ap.add_argument("--skew-ns", type=int, default=4000, help="copy delay of every 4th CTA in the ablation")

@@ -89,6 +89,9 @@ typedef struct mxa2a_status {
  *   (2 when commMSize is 64 or not a multiple of 128, else 1);
  *   M, N, K <= 2^20.
  * Returns MXA2A_OK or MXA2A_ERR_INVALID_SHAPE.  Pure host code.
+ * Passage: all_to_all_matmul.cpp (the launcher), its argument checks (m, k, n,
+ * rankNum positive; k divisible by rankNum; CeilDiv(Ka, 64) even) and the
+ * [MODIFY C2] note that headMSize must divide m or the tail block is lost.
  */
 int mxa2a_validate(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t commMSize, int buffer_num);
 
@@ -97,11 +100,25 @@ int mxa2a_validate(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t commMS
  * the shape, derives the tiling (128x256 output tiles, 128-wide K blocks,
  * split-K over segments when there are too few tiles to fill the GPU),
  * allocates the workspace and encodes the TMA descriptors of the ring.
- * Returns NULL on error; mxa2a_last_error() then gives the code.
+ * Arguments: R segments ("ranks"), M rows of A and C, kPerRank = K extent of
+ * one segment, N columns of C, commMSize rows per staging step, buffer_num
+ * ring slots.  The plan (and its device workspace) belongs to the caller
+ * until mxa2a_destroy.  Returns NULL on error; mxa2a_last_error() then gives
+ * the code (MXA2A_ERR_INVALID_SHAPE, MXA2A_ERR_UNSUPPORTED_DEVICE, or
+ * MXA2A_ERR_CUDA when an allocation or a descriptor encoding failed).
+ * Passage: all_to_all_matmul.cpp (the launcher), runAllToAllMatmul: the
+ * tiling it fills before the launch (commTilingData.tileCnt from headMSize,
+ * [MODIFY C2]; bufferSize, [MODIFY C1]; the tile GEMM tiling for headMSize x
+ * n x Ka) and the communication space it reserves (rankSize * bufferSize *
+ * bufferBlockSize + scales); here the plan holds both.
  */
 mxa2a_plan *mxa2a_create(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t commMSize, int buffer_num);
 
-/* Error code of the last failed mxa2a_create* on this thread. */
+/* Error code of the last failed mxa2a_create* on this thread (MXA2A_OK after
+ * a successful one).  Thread-local; no side effects.
+ * Passage: all_to_all_matmul.cpp (the launcher), its ACL_CHECK wrapping of
+ * every runtime call: a failed call is reported, here as a code the caller
+ * reads instead of a message. */
 int mxa2a_last_error(void);
 
 /* What a plan computes (mxa2a_get_option(MXA2A_INFO_KIND)). */
@@ -236,6 +253,14 @@ int mxa2a_run_allreduce_unfused(mxa2a_plan *plan, const void *A, const void *A_s
  * does not change.  Replays share that index: a device time-out in one of
  * them stays reported (mxa2a_get_status) for the later ones, and
  * mxa2a_kernel_times does not see replays.
+ * Errors: MXA2A_ERR_NULL_PTR, MXA2A_ERR_MISALIGNED, MXA2A_ERR_WRONG_DEVICE,
+ * MXA2A_ERR_CAPTURE_SPLIT, MXA2A_ERR_CUDA (a launch failed); device
+ * time-outs later through mxa2a_get_status.
+ * Passage: all_to_all_matmul_impl.h, the kernel entry
+ * AllToAllQuantMatmulKernelE4M3E4M3(shmemSpace, aGM, scaleAGM, bGM, scaleBGM,
+ * cGM, tilingData), which runs Init and then Process: AllToAllProcess stages
+ * the segments through the ring, MatmulProcess runs the block-scaled GEMM on
+ * each staged slot.  The plan stands in for shmemSpace and tilingData.
  */
 int mxa2a_run(mxa2a_plan *plan, const void *const *A_seg, const void *const *A_scale_seg, const void *B,
               const void *B_scale, void *C_bf16, void *stream);
@@ -262,6 +287,12 @@ int mxa2a_run_direct(mxa2a_plan *plan, const void *const *A_seg, const void *con
  * the same result bits as mxa2a_run when both paths use the same K split
  * (MXA2A_OPT_SPLIT_K forces one; by default each path picks its own).
  * The CUDA-graph rules of mxa2a_run apply (MXA2A_INFO_SPLITS_UNFUSED).
+ * Errors as for mxa2a_run.
+ * Passage: all_to_all_matmul_impl.h, MatmulProcess (the QuantMatmulMxKernelSwat
+ * GEMM over the received A) run only after AllToAllProcess has finished every
+ * step (all_to_all_comm_udma.h, PutToAllRanks): the exchange and the GEMM in
+ * sequence instead of overlapped, the comparison the method's own pipeline
+ * is built to beat.
  */
 int mxa2a_run_unfused(mxa2a_plan *plan, const void *const *A_seg, const void *const *A_scale_seg, const void *B,
                       const void *B_scale, void *C_bf16, void *stream);
@@ -277,7 +308,10 @@ int mxa2a_run_unfused(mxa2a_plan *plan, const void *const *A_seg, const void *co
  * memory), pinned B and B_scale are copied by the SMs in one launch, and a
  * pinned C is written back the same way; pageable buffers go through one DMA
  * copy each.  The host buffers must stay unchanged until the stream has
- * passed the run.
+ * passed the run.  Errors as for mxa2a_run.
+ * Passage: all_to_all_matmul.cpp (the launcher), InitData and the
+ * aclrtMemcpy calls that move the inputs to the device before the launch and
+ * the output back after it.
  */
 int mxa2a_run_host(mxa2a_plan *plan, const void *const *A_seg_host, const void *const *A_scale_seg_host,
                    const void *B_host, const void *B_scale_host, void *C_bf16_host, void *stream);
@@ -285,7 +319,15 @@ int mxa2a_run_host(mxa2a_plan *plan, const void *const *A_seg_host, const void *
 /*
  * Copy the device status block to *out (synchronous; call after the runs'
  * stream is synchronised) and mark it read.  out->code is MXA2A_OK unless a
- * launch since the previous call reported a device error.
+ * launch since the previous call reported a device error.  Returns
+ * MXA2A_ERR_NULL_PTR, MXA2A_ERR_WRONG_DEVICE, MXA2A_ERR_CUDA (the copy
+ * failed) or MXA2A_OK.
+ * Passage: the performance optimisation guide, section 2.1 (deadlocks after
+ * moving from barrier_all to wait/notify): a wait that never ends is found by
+ * a watchdog time-out followed by a dump of where the signals stopped (a slot
+ * stuck at 1: the consumer never saw it; stuck at 0: the producer never
+ * notified).  Here every device wait is bounded, and the first one that runs
+ * out records its role, step, segment, slot and counter values.
  */
 int mxa2a_get_status(mxa2a_plan *plan, mxa2a_status *out);
 
@@ -351,11 +393,23 @@ enum mxa2a_option {
     MXA2A_INFO_KIND = 119          /* enum mxa2a_kind */
 };
 
+/* Set a tunable (MXA2A_OPT_*) or read it back, or read a plan fact
+ * (MXA2A_INFO_*, read-only).  Returns MXA2A_ERR_INVALID_OPTION for an unknown
+ * key, a value out of range, or a set of an MXA2A_INFO_* key; changing the
+ * tiling re-derives the plan (and may reallocate its split-K scratch:
+ * MXA2A_ERR_CUDA if that fails).
+ * Passage: all_to_all_matmul.cpp (the launcher), the knobs it marks for
+ * change, [MODIFY C1] bufferSize and [MODIFY C2] headMSize, and the
+ * performance optimisation guide, sections 1.2 to 1.4 (core flattening and
+ * split, signal granularity, swizzled tile order), whose choices the options
+ * expose. */
 int mxa2a_set_option(mxa2a_plan *plan, int key, int64_t value);
 int mxa2a_get_option(mxa2a_plan *plan, int key, int64_t *value);
 
 /* Duration of the main GEMM kernel of the last run, in ms (needs
- * MXA2A_OPT_RECORD_EVENTS >= 1; synchronises on that run's end event). */
+ * MXA2A_OPT_RECORD_EVENTS >= 1; synchronises on that run's end event).
+ * Passage: all_to_all_matmul.cpp (the launcher), perf mode: the main kernel
+ * timed alone, each round synchronised, after an L2 flush. */
 int mxa2a_last_kernel_ms(mxa2a_plan *plan, float *ms);
 
 /* Durations (ms) of the main GEMM kernel of the last min(max_count, recorded)
@@ -374,11 +428,16 @@ enum mxa2a_workspace {
 
 /* Synchronous copy of a workspace region to host memory (at most bytes);
  * *bytes_out receives the region's full size.  Synchronise the plan's
- * stream first. */
+ * stream first.
+ * Passage: all_to_all_matmul.cpp (the launcher), precision mode: the
+ * communication buffer's A and scales are copied back (shmem_A.bin,
+ * shmem_scale.bin) to check the exchange by itself. */
 int mxa2a_read_workspace(mxa2a_plan *plan, int which, void *host_dst, size_t bytes, size_t *bytes_out);
 
 /* Benchmark helper: add 1 to every 32-bit word of a device buffer (bytes %
- * 16 == 0), evicting other data from L2 when bytes exceeds its size. */
+ * 16 == 0), evicting other data from L2 when bytes exceeds its size.
+ * Passage: all_to_all_matmul.cpp (the launcher), perf mode: heavy_add_kernel
+ * over a cache-flush buffer larger than L2 before every timed round. */
 int mxa2a_l2_flush(void *device_buf, size_t bytes, void *stream);
 
 /*
@@ -389,8 +448,11 @@ int mxa2a_l2_flush(void *device_buf, size_t bytes, void *stream);
  * The pages have no counterpart of this entry point; it is a deployment
  * variant of mxa2a_run.
  *
- * Same shape rules, data layouts and result as mxa2a_run (no plan, no K
- * split).  It allocates nothing: the staging ring, scale tiles, credit
+ * Same shape rules, data layouts and result as mxa2a_run with E4M3 x E4M3
+ * operands (the element-type option of a plan does not exist here), run on
+ * the single-CTA kernel with no K split: the result bits equal those of
+ * mxa2a_run of a plan with MXA2A_OPT_SPLIT_K = 1 and MXA2A_OPT_CTA_PAIR = 0.
+ * It allocates nothing: the staging ring, scale tiles, credit
  * counters and status block live in one static device array of 16 MiB that
  * every GPU which loads this library holds until the process exits.  A shape
  * whose ring + scale tiles + counters exceed it returns
@@ -400,17 +462,24 @@ int mxa2a_l2_flush(void *device_buf, size_t bytes, void *stream);
  * stream capture begins.  Every call reuses the same array (the counters are
  * cleared on the stream at the start of each call), so calls that overlap on
  * the GPU — on two streams, or from two host threads — race.  Device-side
- * wait time-outs are not reported by this entry point.  Asynchronous on
+ * wait time-outs are not reported by this entry point: the kernel then stops
+ * early, C is left partly written (undefined), and the call has already
+ * returned MXA2A_OK.  Only a lost staging credit can cause one, i.e. a
+ * defect, not an input.  Asynchronous on
  * stream (a cudaStream_t, NULL = legacy default stream).
  */
 int mxa2a_run_noalloc(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t commMSize, int buffer_num,
                       const void *const *A_seg, const void *const *A_scale_seg, const void *B, const void *B_scale,
                       void *C_bf16, void *stream);
 
-/* Free the plan's workspace (synchronises the device first). NULL is a no-op. */
+/* Free the plan's workspace (synchronises the device first). NULL is a no-op.
+ * Passage: all_to_all_matmul.cpp (the launcher), the teardown after the
+ * runs (aclshmem_free of the communication space, aclrtFree of the buffers). */
 void mxa2a_destroy(mxa2a_plan *plan);
 
-/* Static string for an error code. */
+/* Static string for an error code (never NULL; unknown codes get a generic
+ * text).  Passage: all_to_all_matmul.cpp (the launcher), the messages its
+ * argument checks throw ("ERROR: k must be divisible by rankNum", ...). */
 const char *mxa2a_strerror(int code);
 
 #ifdef __cplusplus

@@ -48,7 +48,11 @@ def parity_stats(gpu_bits, ref_bits) -> dict:
     g = bits_to_f64(gpu_bits)
     r = bits_to_f64(ref_bits)
     nan_g, nan_r = np.isnan(g), np.isnan(r)
-    both = ~(nan_g | nan_r)
+    # an infinity matches the same infinity exactly (inf - inf would be NaN);
+    # an infinity against anything else fails the gate below
+    same_inf = np.isinf(g) & np.isinf(r) & (g == r)
+    inf_mismatch = (np.isinf(g) | np.isinf(r)) & ~same_inf & ~(nan_g | nan_r)
+    both = ~(nan_g | nan_r | same_inf | inf_mismatch)
     diff = g[both] - r[both]
     ad = np.abs(diff)
     rel = ad / np.maximum(np.abs(r[both]), 1e-8)
@@ -61,7 +65,9 @@ def parity_stats(gpu_bits, ref_bits) -> dict:
         "rmse": float(np.sqrt((diff ** 2).mean())) if ad.size else 0.0,
         "max_rel": float(rel.max()) if rel.size else 0.0,
         "over_1e-2": int((ad > 1e-2).sum()),
-        "fail": int((~gate).sum()) + int((nan_g != nan_r).sum()),
+        "fail": int((~gate).sum()) + int((nan_g != nan_r).sum()) + int(inf_mismatch.sum()),
+        "inf_matched": int(same_inf.sum()),
+        "inf_mismatch": int(inf_mismatch.sum()),
         "fail_pages_form": int((~gate_pages).sum()),
         "nan_mismatch": int((nan_g != nan_r).sum()),
     }

@@ -160,6 +160,44 @@ def test_scale_factors_per_block_and_column(M):
     assert np.array_equal(gu.bits_to_f64(got), gu.bits_to_f64(ref))
 
 
+@pytest.mark.parametrize("fused", [True, False])
+def test_e8m0_range_ends(fused):
+    """Scale bytes at both ends of the E8M0 range (254 = 2^127, 1 = 2^-126) in
+    the first 32-wide K block of some A rows and some B columns, all codes of
+    that block positive (so no infinities of both signs meet in one sum): the
+    products of two high scales overflow fp32 inside the tensor core (+inf),
+    two low scales underflow to zero, a high and a low scale give ordinary
+    values.  Compared with the oracle per element (matching infinities are
+    equal)."""
+    R, ka, M, N = 2, 128, 256, 256
+    K = R * ka
+    w = inputs.Workload("e8m0_ends", R, M, ka, N, 128, 2, 0)
+    x = inputs.make_inputs(inputs.Workload("e8m0_src", R, M, ka, N, 128, 2, 61))
+    A = torch.cat(x["A_seg"], dim=1).clone()
+    sA = torch.cat(x["A_scale_seg"], dim=1).clone()
+    B, sB = x["B"].clone(), x["B_scale"].clone()
+    A[:, :32] &= 0x7F                     # block 0 of every row and column: positive codes
+    B[:, :32] &= 0x7F
+    sA[0:64, 0] = 254
+    sA[64:128, 0] = 1
+    sA[128:160, 0] = 253
+    sB[0:64, 0] = 254
+    sB[64:128, 0] = 1
+    sB[128:160, 0] = 2
+    x = {"A_seg": [A[:, r * ka:(r + 1) * ka].contiguous() for r in range(R)],
+         "A_scale_seg": [sA[:, r * ka // 32:(r + 1) * ka // 32].contiguous() for r in range(R)],
+         "B": B.contiguous(), "B_scale": sB.contiguous()}
+    d = gu.to_device(x)
+    with _plan(w, split_k=1) as p:
+        C = gu.run_gpu(p, d, M, N, fused=fused)
+        torch.cuda.synchronize()
+        _status_ok(p)
+        got = gu.host_bits(C)
+    ref = gu.oracle_full(x)
+    st = gu.assert_parity(got, ref, f"e8m0 range ends fused={fused}")
+    assert st["inf_matched"] > 0      # the high x high cells did overflow on both sides
+
+
 # --- the smallest workload, and small shapes spanning tiles with ragged tails -------------
 
 @pytest.mark.parametrize("fused", [True, False])
