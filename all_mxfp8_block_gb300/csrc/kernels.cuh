@@ -171,8 +171,13 @@ __host__ __device__ inline int seg_col0(const GemmParams& p, int r) { return p.s
 
 // Launchers (mxgemm.cu / aux_kernels.cu).  All return cudaError_t of the launch.
 // tmap_c: C as bf16 [M][N], box 32 rows x 32 columns, 64-byte swizzle (the epilogue's TMA stores)
+// tmap_sf: the A and B scale atoms ([K/128][Mg][512] and [K/128][Ng2][512] u8)
+// as 2D u8 tensors of 256-byte rows, boxes of 2 and 4 rows (one atom, two
+// atoms); needed by the CTA-pair kernel, whose odd CTA's loads complete on the
+// even CTA's barrier (a form the plain bulk copy lacks), else may be NULL
 cudaError_t launch_mxgemm(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                          const CUtensorMap& tmap_c, int grid, bool fused, cudaStream_t stream);
+                          const CUtensorMap& tmap_c, int grid, bool fused, cudaStream_t stream,
+                          const CUtensorMap* tmap_sf = nullptr);
 // CTA pairs of the pair kernel that can be resident at once (0 if it cannot run)
 int mxgemm_max_pairs(bool fused);
 cudaError_t launch_pack_a(const GemmParams& p, uint8_t* a_packed, int grid, cudaStream_t stream);

@@ -65,6 +65,22 @@ bool encode_c(CUtensorMap* map, void* C, uint64_t M, uint64_t N) {
     return r == CUDA_SUCCESS;
 }
 
+// Scale atoms ([blocks][512] u8) as a 2D u8 tensor of 256-byte rows (2 per
+// atom), box box_rows x 256, no swizzle: the CTA-pair kernel's loads of one
+// A atom (2 rows) or a tile's two B atoms (4 rows).
+bool encode_atoms(CUtensorMap* map, const void* base, uint64_t atoms, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || atoms == 0) return false;
+    cuuint64_t dims[2] = {256, atoms * 2};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {256, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int tile_span(int64_t M, int64_t cm, int64_t rows = BM) {
@@ -125,6 +141,7 @@ struct mxa2a_plan {
     DevStatus* status = nullptr;
     size_t ring_bytes = 0, sfa_bytes = 0, sfb_bytes = 0, apacked_bytes = 0, partial_bytes = 0, flags_bytes = 0;
     CUtensorMap tmap_ring, tmap_apacked, tmap_b, tmap_b_half;
+    CUtensorMap tmap_sf[2];                 // the scale atoms in the workspace (CTA-pair kernel's loads)
     const void* tmap_b_ptr = nullptr;
     CUtensorMap tmap_c;                     // for the C pointer of the last run
     const void* tmap_c_ptr = nullptr;
@@ -525,7 +542,7 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
     rc = cuda_rc(launch_mxgemm(g, fused ? p->tmap_ring : p->tmap_apacked,
                                (g.pair || g.tile_n == BN_NARROW) ? p->tmap_b_half : p->tmap_b,
                                rs_fused ? p->tmap_out : p->tmap_c, fused ? p->grid_fused : p->grid_unfused, fused,
-                               stream));
+                               stream, p->tmap_sf));
     if (rc) return rc;
     ++launches;
     if (p->record_events) {
@@ -637,6 +654,8 @@ mxa2a_plan* create_impl(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t c
         std::memset(&p->tmap_ring, 0, sizeof(CUtensorMap));      // never used: A is read in place
         std::memset(&p->tmap_apacked, 0, sizeof(CUtensorMap));
     }
+    ok = ok && encode_atoms(&p->tmap_sf[0], p->sfa, (uint64_t)(p->K / BK) * p->Mg, 2) &&
+         encode_atoms(&p->tmap_sf[1], p->sfb, (uint64_t)(p->K / BK) * p->Ng2, 4);
     if (!ok || cudaDeviceSynchronize() != cudaSuccess) {
         cudaGetLastError();
         mxa2a_destroy(p);

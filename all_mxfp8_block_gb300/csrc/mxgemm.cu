@@ -59,6 +59,8 @@
 // status block instead of hanging.
 #include <cuda_bf16.h>
 
+#include <cstring>
+
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -86,13 +88,15 @@ __device__ __forceinline__ void trace_ev(unsigned kind, unsigned a, unsigned b) 
 #define TRACE(k, a, b) ((void)0)
 #endif
 
+// In the CTA-pair kernel the even CTA's full[] barriers cover both CTAs'
+// loads of a stage (each CTA's producer arms it for its own bytes and its TMA
+// loads complete on it), and its acc_empty[] barriers count the epilogue warps
+// of both CTAs; the odd CTA's copies of those barriers are unused.
 struct __align__(8) SmemCtl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
-    uint64_t peer_full[kMaxStages];   // pair kernel, even CTA: the odd CTA's stage landed
     uint64_t acc_full[kMaxAccBufs];    // per TMEM accumulator buffer
     uint64_t acc_empty[kMaxAccBufs];
-    uint64_t acc_empty_peer;          // pair kernel, even CTA: the odd CTA drained its TMEM
     uint64_t drain;
     uint32_t tmem_base;
     volatile int abort;
@@ -222,11 +226,17 @@ __device__ __forceinline__ bool launch_failed(const GemmParams& p) {
 }
 
 // Wait for an mbarrier phase; false on time-out or when the CTA is aborting.
-__device__ bool wait_mbar(const GemmParams& p, SmemCtl* ctl, uint64_t* bar, uint32_t parity, int role) {
-    if (mbar_try_wait(bar, parity)) return true;
+// cluster: the phase is completed by arrivals from the other CTA of a pair
+// (acquire at cluster scope).
+__device__ __forceinline__ bool try_wait_scoped(uint64_t* bar, uint32_t parity, bool cluster) {
+    return cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+}
+__device__ bool wait_mbar(const GemmParams& p, SmemCtl* ctl, uint64_t* bar, uint32_t parity, int role,
+                          bool cluster = false) {
+    if (try_wait_scoped(bar, parity, cluster)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (try_wait_scoped(bar, parity, cluster)) return true;
         if (ctl->abort) return false;
         if ((n & 63) == 0) {
             if (globaltimer() - t0 > (uint64_t)p.timeout_ns) {
@@ -244,15 +254,15 @@ __device__ bool wait_mbar(const GemmParams& p, SmemCtl* ctl, uint64_t* bar, uint
 
 // Whole-warp variant: every lane waits (each acquires), the outcome is uniform.
 __device__ __forceinline__ bool wait_mbar_warp(const GemmParams& p, SmemCtl* ctl, uint64_t* bar, uint32_t parity,
-                                               int role) {
-    const bool ok = wait_mbar(p, ctl, bar, parity, role);
+                                               int role, bool cluster = false) {
+    const bool ok = wait_mbar(p, ctl, bar, parity, role, cluster);
     return __all_sync(0xffffffffu, ok);
 }
 
 // Cleanup wait: only the time limit ends it (used after an abort).
-__device__ void wait_mbar_plain(const GemmParams& p, uint64_t* bar, uint32_t parity) {
+__device__ void wait_mbar_plain(const GemmParams& p, uint64_t* bar, uint32_t parity, bool cluster = false) {
     const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!try_wait_scoped(bar, parity, cluster)) {
         if (globaltimer() - t0 > (uint64_t)p.timeout_ns) {
             record_error(p, kErrTimeout, kRoleExit, -1, -1, -1, -1, (long long)parity);
             return;
@@ -294,9 +304,12 @@ __device__ __forceinline__ void named_barrier_sync(int id, int count) {
 // ------------------------------------------------------------------ roles
 template <bool kPair, int kBN>
 __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const CUtensorMap* tmb,
-                              uint8_t* sA, uint8_t* sB, uint8_t* sSfa, uint8_t* sSfb, SmemCtl* ctl,
-                              bool fused, uint32_t rank, int pid) {
+                              const CUtensorMap* tm_sfa, const CUtensorMap* tm_sfb, uint8_t* sA, uint8_t* sB,
+                              uint8_t* sSfa, uint8_t* sSfb, SmemCtl* ctl, bool fused, uint32_t rank, int pid) {
     using L = Lay<kPair, kBN>;
+    // CTA pair: every stage's loads of both CTAs complete on the even CTA's
+    // full barrier, which each producer arms for its own bytes
+    const uint32_t full0 = kPair ? mapa_shared(smem_u32(&ctl->full[0]), 0) : 0u;
     // B tiles are re-read by every m-tile: keep them in L2; A (ring or packed) is read by one
     // row of tiles at a time
     const uint64_t pol_keep = l2_policy_evict_last();
@@ -374,12 +387,40 @@ __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const
                 }
                 const int stage = it % L::kStg;
                 const uint32_t ph = (uint32_t)(it / L::kStg) & 1u;
-                if (!wait_mbar(p, ctl, &ctl->empty[stage], ph ^ 1u, kRoleTma)) return;
+                // (CTA pair: empty is completed by the even CTA's MMA commit)
+                if (!wait_mbar(p, ctl, &ctl->empty[stage], ph ^ 1u, kRoleTma, kPair)) return;
                 uint64_t* bar = &ctl->full[stage];
-                mbar_arrive_expect_tx(bar, bytes);
                 const int kx = kb * BK;
                 const int kg = r * p.ka + kx;
                 uint8_t* a_dst = sA + (size_t)stage * kAStageBytes;
+                if (kPair) {
+                    // A rows of this CTA's m-tile, its half of the tile's B rows,
+                    // its rows' A scale atom and the B scale atoms of all 256 columns
+                    const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
+                    if (rank == 0)
+                        mbar_arrive_expect_tx(bar, bytes);
+                    else
+                        mbar_arrive_expect_tx_remote(fb, bytes);
+                    if (fused) {
+                        for (int b = 0; b < nbox; ++b) {
+                            const int row0 = mt * BM + b * p.box_m;
+                            const int s = row0 / p.cm;
+                            const int ring_row = ((s % p.bn) * p.R + r) * p.cm + (row0 - s * p.cm);
+                            tma_load_2d_pair(a_dst + (size_t)b * p.box_m * BK, tma, fb, kx, ring_row, pol_stream);
+                        }
+                    } else {
+                        tma_load_2d_pair(a_dst, tma, fb, kg, mt * BM, pol_stream);
+                    }
+                    tma_load_2d_pair(sB + (size_t)stage * L::kBStage, tmb, fb, kg, b_row, pol_keep);
+                    const int kbg = kg / BK;
+                    tma_load_2d_pair(sSfa + (size_t)stage * kSfaStageBytes, tm_sfa, fb, 0,
+                                     2 * (kbg * p.Mg + mt), pol_stream);
+                    tma_load_2d_pair(sSfb + (size_t)stage * L::kSfbStage, tm_sfb, fb, 0,
+                                     2 * (kbg * p.Ng2 + item.nt * L::kSfbAtoms), pol_keep);
+                    ctl->issued[pid] = it + 1;
+                    continue;
+                }
+                mbar_arrive_expect_tx(bar, bytes);
                 if (fused) {
                     for (int b = 0; b < nbox; ++b) {
                         const int row0 = mt * BM + b * p.box_m;
@@ -441,18 +482,17 @@ __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_
         const int buf = n % L::kAccBufs;
         const uint32_t acc_ph = (uint32_t)(n / L::kAccBufs) & 1u;
         const uint32_t acc_col = tmem + kTmemAccCol + (uint32_t)(buf * kBN);
-        if (!wait_mbar(p, ctl, &ctl->acc_empty[buf], acc_ph ^ 1u, kRoleMma)) return;
-        if (kPair && !wait_mbar(p, ctl, &ctl->acc_empty_peer, acc_ph ^ 1u, kRoleMma)) return;
+        // (CTA pair: acc_empty counts the epilogue warps of both CTAs)
+        if (!wait_mbar(p, ctl, &ctl->acc_empty[buf], acc_ph ^ 1u, kRoleMma, kPair)) return;
         tc_fence_after();
         TRACE(1, w, 0);
         const int total = item.nseg * p.kb_per_seg;
         for (int j = 0; j < total; ++j) {
             const int stage = it % L::kStg;
             const uint32_t ph = (uint32_t)(it / L::kStg) & 1u;
-            if (!wait_mbar(p, ctl, &ctl->full[stage], ph, kRoleMma)) return;
+            // (CTA pair: full covers both CTAs' loads of the stage)
+            if (!wait_mbar(p, ctl, &ctl->full[stage], ph, kRoleMma, kPair)) return;
             TRACE(11, it, 0);
-            if (kPair && !wait_mbar(p, ctl, &ctl->peer_full[stage], ph, kRoleMma)) return;
-            if (kPair) TRACE(12, it, 0);
             ctl->consumed = it + 1;
             if (j == 0) TRACE(2, w, 0);
             tc_fence_after();
@@ -506,35 +546,23 @@ __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_
     }
 }
 
-// CTA-pair kernel, odd CTA: its MMAs are issued by the even CTA, which must
-// know when this CTA's stages have landed and when its TMEM share is drained.
-// Walks the same item and stage sequence and forwards every completed phase of
-// its local full[] and acc_empty barriers, one arrive each, to the even CTA's
-// peer_full[] and acc_empty_peer barriers.  Before item i (i >= 1) the even
-// CTA waits for phase i-1 of acc_empty_peer, i.e. the drain of item i-1.
-__device__ void forwarder_role(const GemmParams& p, SmemCtl* ctl) {
-    using L = Lay<true, BN>;   // one accumulator buffer
-    const uint32_t leader_full = mapa_shared(smem_u32(&ctl->peer_full[0]), 0);
-    const uint32_t leader_acc = mapa_shared(smem_u32(&ctl->acc_empty_peer), 0);
-    int it = 0;
-    int n_items = 0;
-    for (int w = first_item<true>(); w < p.W; w += item_stride<true>(), ++n_items) {
-        const Item item = decode_item(p, w);
-        if (n_items > 0) {
-            // this CTA's epilogue drained item n_items-1 (phase n_items-1 of acc_empty)
-            if (!wait_mbar(p, ctl, &ctl->acc_empty[0], (uint32_t)(n_items - 1) & 1u, kRoleMma)) return;
-            mbar_arrive_remote(leader_acc);
+// This thread has read its share of accumulator buffer `buf` (its tcgen05.ld
+// completed): release the buffer for a later item.  Single CTA: every
+// epilogue thread arrives (count kEpiThreads).  CTA pair: one arrival per
+// epilogue warp of either CTA, on the even CTA's barrier (count 2 * kEpiWarps).
+template <bool kPair>
+__device__ __forceinline__ void release_accumulator(SmemCtl* ctl, int buf, int lane, uint32_t rank) {
+    tc_fence_before();
+    if (kPair) {
+        __syncwarp();
+        if (lane == 0) {
+            if (rank == 0)
+                mbar_arrive(&ctl->acc_empty[buf]);
+            else
+                mbar_arrive_remote(mapa_shared(smem_u32(&ctl->acc_empty[buf]), 0));
         }
-        const int total = item.nseg * p.kb_per_seg;
-        for (int j = 0; j < total; ++j) {
-            const int stage = it % L::kStg;
-            const uint32_t ph = (uint32_t)(it / L::kStg) & 1u;
-            if (!wait_mbar(p, ctl, &ctl->full[stage], ph, kRoleMma)) return;
-            TRACE(13, it, 0);
-            ctl->consumed = it + 1;
-            mbar_arrive_remote(leader_full + (uint32_t)(stage * sizeof(uint64_t)));
-            ++it;
-        }
+    } else {
+        mbar_arrive(&ctl->acc_empty[buf]);
     }
 }
 
@@ -597,7 +625,7 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
         const int mt = cta_mtile<kPair>(item, rank);
         const int buf = n % L::kAccBufs;
         const uint32_t acc_ph = (uint32_t)(n / L::kAccBufs) & 1u;
-        const bool got = wait_mbar_warp(p, ctl, &ctl->acc_full[buf], acc_ph, kRoleEpi);
+        const bool got = wait_mbar_warp(p, ctl, &ctl->acc_full[buf], acc_ph, kRoleEpi, kPair);
         if (p.S > 1) {
             // the split path synchronises the 8 epilogue warps on a named barrier:
             // leave only all together
@@ -632,8 +660,7 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
 #pragma unroll
                 for (int j = 0; j < 16; ++j) packed[c * 16 + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
             }
-            tc_fence_before();
-            mbar_arrive(&ctl->acc_empty[buf]);   // this accumulator may now take a later item
+            release_accumulator<kPair>(ctl, buf, lane, rank);   // this accumulator may now take a later item
             if (leader) TRACE(7, w, 0);
             // C; or (GEMM + ReduceScatter) block j of the rows (rs_rows, a multiple of 64,
             // so one block holds the warp's 32) to peer j's send buffer, this rank's
@@ -683,8 +710,7 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
                                 make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(&ctl->acc_empty[buf]);
+                release_accumulator<kPair>(ctl, buf, lane, rank);
             }
             named_barrier_sync(2, kEpiThreads);   // (also makes the leader's ticket visible)
             const bool last = ctl->ticket == p.S - 1;
@@ -1038,7 +1064,8 @@ __device__ void pack_sfa_slice(const GemmParams& p) {
 template <bool kFused, bool kPair, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
     mxgemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_a,
-                  const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_c) {
+                  const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_c,
+                  const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb) {
     using L = Lay<kPair, kBN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1053,15 +1080,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < L::kStg; ++s) {
-            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->full[s], kPair ? 2 : 1);   // pair: each CTA's producer arms it
             mbar_init(&ctl->empty[s], 1);
-            mbar_init(&ctl->peer_full[s], 1);
         }
         for (int b = 0; b < L::kAccBufs; ++b) {
             mbar_init(&ctl->acc_full[b], 1);
-            mbar_init(&ctl->acc_empty[b], kEpiThreads);
+            mbar_init(&ctl->acc_empty[b], kPair ? 2 * kEpiWarps : kEpiThreads);
         }
-        mbar_init(&ctl->acc_empty_peer, 1);
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
         for (int i = 0; i < kProducers; ++i) ctl->issued[i] = 0;
@@ -1084,6 +1109,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tmap_a);
         prefetch_tensormap(&tmap_b);
         prefetch_tensormap(&tmap_c);
+        if (kPair) {
+            prefetch_tensormap(&tmap_sfa);
+            prefetch_tensormap(&tmap_sfb);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -1119,15 +1148,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kWarpTma || warp == kWarpTma1) {
         if (lane == 0 && !p.exchange_only)
-            producer_role<kPair, kBN>(p, &tmap_a, &tmap_b, sA, sB, sSfa, sSfb, ctl, kFused, rank,
-                                 warp == kWarpTma ? 0 : 1);
+            producer_role<kPair, kBN>(p, &tmap_a, &tmap_b, &tmap_sfa, &tmap_sfb, sA, sB, sSfa, sSfb, ctl, kFused,
+                                      rank, warp == kWarpTma ? 0 : 1);
     } else if (warp == kWarpMma) {
-        if (lane == 0 && !p.exchange_only) {
-            if (rank == 0)
-                mma_role<kPair, kBN>(p, tmem, sA, sB, sSfa, sSfb, ctl, kFused);
-            else
-                forwarder_role(p, ctl);
-        }
+        // (CTA pair: the even CTA issues the MMAs of both; the odd CTA's warp only owns its TMEM)
+        if (lane == 0 && !p.exchange_only && rank == 0)
+            mma_role<kPair, kBN>(p, tmem, sA, sB, sSfa, sSfb, ctl, kFused);
     } else if (warp < kWarpCopy0) {
         if (!p.exchange_only) {
             epilogue_role<kFused, kPair, kBN>(p, tmem, ctl, warp, lane, rank, &tmap_c, smem + L::Epi);
@@ -1143,10 +1169,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // After an abort, let every TMA load already issued land before the CTA exits
     // (each producer waits for its own stages beyond those the MMA side consumed).
-    if ((warp == kWarpTma || warp == kWarpTma1) && lane == 0 && ctl->abort) {
+    if (!kPair && (warp == kWarpTma || warp == kWarpTma1) && lane == 0 && ctl->abort) {
         const int pid = warp == kWarpTma ? 0 : 1;
         for (int i = ctl->consumed; i < ctl->issued[pid]; ++i)
             if (i % kProducers == pid) wait_mbar_plain(p, &ctl->full[i % L::kStg], (uint32_t)(i / L::kStg) & 1u);
+    }
+    if (kPair) {
+        // Both CTAs' producers have stopped.  Every stage past those the MMA
+        // thread consumed whose loads either CTA issued completes on the even
+        // CTA's full barrier: the even CTA arrives for whichever CTA did not arm
+        // it, then waits until the loads have landed (a normal run has none).
+        cluster_sync();
+        if (rank == 0 && threadIdx.x == 0) {
+            const uint32_t odd_issued = mapa_shared(smem_u32((const void*)&ctl->issued[0]), 1);
+            int iss_even[kProducers], iss_odd[kProducers], hi = 0;
+            for (int q = 0; q < kProducers; ++q) {
+                iss_even[q] = ctl->issued[q];
+                iss_odd[q] = (int)ld_shared_cluster_u32(odd_issued + 4u * (uint32_t)q);
+                hi = max(hi, max(iss_even[q], iss_odd[q]));
+            }
+            for (int i = ctl->consumed; i < hi; ++i) {
+                const int q = i % kProducers;
+                uint64_t* bar = &ctl->full[i % L::kStg];
+                if (i >= iss_even[q]) mbar_arrive(bar);
+                if (i >= iss_odd[q]) mbar_arrive(bar);
+                wait_mbar_plain(p, bar, (uint32_t)(i / L::kStg) & 1u, true);
+            }
+        }
     }
     // All MMAs complete before TMEM is released (in a pair, the even CTA's
     // commit arrives on both CTAs' drain barriers).
@@ -1156,7 +1205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
             tc_commit(&ctl->drain);
         }
-        wait_mbar_plain(p, &ctl->drain, 0);
+        wait_mbar_plain(p, &ctl->drain, 0, kPair);
     }
     __syncwarp();
     tc_fence_before();
@@ -1215,7 +1264,8 @@ cudaError_t prepare(int dev) {
 
 template <bool kFused, bool kPair, int kBN>
 cudaError_t launch_one(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                       const CUtensorMap& tmap_c, int grid, cudaStream_t stream) {
+                       const CUtensorMap& tmap_c, const CUtensorMap& tmap_sfa, const CUtensorMap& tmap_sfb, int grid,
+                       cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1243,7 +1293,7 @@ cudaError_t launch_one(const GemmParams& p, const CUtensorMap& tmap_a, const CUt
     }
     cfg.attrs = attr;
     cfg.numAttrs = (kPair || kFused || p.sfb_inline || p.direct) ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, &mxgemm_kernel<kFused, kPair, kBN>, p, tmap_a, tmap_b, tmap_c);
+    return cudaLaunchKernelEx(&cfg, &mxgemm_kernel<kFused, kPair, kBN>, p, tmap_a, tmap_b, tmap_c, tmap_sfa, tmap_sfb);
 }
 
 template <bool kFused>
@@ -1292,19 +1342,25 @@ extern "C" int mxa2a_trace_read(void* host, size_t bytes) {
 int mxgemm_max_pairs(bool fused) { return fused ? max_pairs_impl<true>() : max_pairs_impl<false>(); }
 
 cudaError_t launch_mxgemm(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                          const CUtensorMap& tmap_c, int grid, bool fused, cudaStream_t stream) {
+                          const CUtensorMap& tmap_c, int grid, bool fused, cudaStream_t stream,
+                          const CUtensorMap* tmap_sf) {
+    // the scale atoms' tensor maps (sfa, sfb) are read by the CTA-pair kernel only
+    CUtensorMap none;
+    std::memset(&none, 0, sizeof none);
+    const CUtensorMap& sfa = tmap_sf ? tmap_sf[0] : none;
+    const CUtensorMap& sfb = tmap_sf ? tmap_sf[1] : none;
     if (p.pair) {
-        if (p.tile_n != BN) return cudaErrorInvalidValue;
-        if (fused) return launch_one<true, true, BN>(p, tmap_a, tmap_b, tmap_c, grid, stream);
-        return launch_one<false, true, BN>(p, tmap_a, tmap_b, tmap_c, grid, stream);
+        if (p.tile_n != BN || !tmap_sf) return cudaErrorInvalidValue;
+        if (fused) return launch_one<true, true, BN>(p, tmap_a, tmap_b, tmap_c, sfa, sfb, grid, stream);
+        return launch_one<false, true, BN>(p, tmap_a, tmap_b, tmap_c, sfa, sfb, grid, stream);
     }
     if (p.tile_n == BN_NARROW) {
-        if (fused) return launch_one<true, false, BN_NARROW>(p, tmap_a, tmap_b, tmap_c, grid, stream);
-        return launch_one<false, false, BN_NARROW>(p, tmap_a, tmap_b, tmap_c, grid, stream);
+        if (fused) return launch_one<true, false, BN_NARROW>(p, tmap_a, tmap_b, tmap_c, sfa, sfb, grid, stream);
+        return launch_one<false, false, BN_NARROW>(p, tmap_a, tmap_b, tmap_c, sfa, sfb, grid, stream);
     }
     if (p.tile_n != BN) return cudaErrorInvalidValue;
-    if (fused) return launch_one<true, false, BN>(p, tmap_a, tmap_b, tmap_c, grid, stream);
-    return launch_one<false, false, BN>(p, tmap_a, tmap_b, tmap_c, grid, stream);
+    if (fused) return launch_one<true, false, BN>(p, tmap_a, tmap_b, tmap_c, sfa, sfb, grid, stream);
+    return launch_one<false, false, BN>(p, tmap_a, tmap_b, tmap_c, sfa, sfb, grid, stream);
 }
 
 }  // namespace mxa2a

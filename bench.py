@@ -570,6 +570,8 @@ def run_ours(args, w):
         plan.set_option(mxa2a.MXA2A_OPT_SPLIT_K, args.split)
     if args.single_cta:
         plan.set_option(mxa2a.MXA2A_OPT_CTA_PAIR, 0)
+    if args.cta_pair:
+        plan.set_option(mxa2a.MXA2A_OPT_CTA_PAIR, 1)
     if args.group_m:
         plan.set_option(mxa2a.MXA2A_OPT_GROUP_M, args.group_m)
     run = plan.run if args.path == "fused" else plan.run_unfused
@@ -590,7 +592,10 @@ def run_ours(args, w):
     other_steps = min(args.steps, args.other_steps)
     other_ms = timed(other, fargs, other_steps, args.warmup)
     # the direct-read ablation: A read in place, no exchange (same caliber)
-    direct_ms = timed(plan.run_direct, fargs, other_steps, args.warmup)
+    # (the direct read runs on the single-CTA kernel only)
+    direct_ms = None
+    if not plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED):
+        direct_ms = timed(plan.run_direct, fargs, other_steps, args.warmup)
     st = plan.status()
     if st["code"] != 0:
         raise RuntimeError(f"device status after the comparison paths: {st}")
@@ -693,7 +698,7 @@ def run_ours(args, w):
         "unfused" if args.path == "fused" else "fused": {
             "ms_per_step": sum(other_ms) / len(other_ms), "steps": other_steps,
             "value": w.flops / (sum(other_ms) / len(other_ms) / 1e3) / 1e12},
-        "direct_read": {
+        "direct_read": None if direct_ms is None else {
             "ms_per_step": sum(direct_ms) / len(direct_ms), "steps": other_steps,
             "value": w.flops / (sum(direct_ms) / len(direct_ms) / 1e3) / 1e12,
             "what": "A read in place from the segments (no staging ring, no pack): the exchange's cost"},
@@ -746,6 +751,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--split", type=int, default=0, help="force the K split of both paths (0 = automatic)")
     ap.add_argument("--single-cta", action="store_true", help="never use the CTA-pair kernel")
+    ap.add_argument("--cta-pair", action="store_true", help="use the CTA-pair kernel where the shape allows it")
     ap.add_argument("--group-m", type=int, default=0, help="largest unfused raster group in m-tiles (0 = library default)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
