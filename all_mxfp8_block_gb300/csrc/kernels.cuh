@@ -48,6 +48,8 @@ constexpr int kEpiBufBytes = 32 * 32 * 2;    // per epilogue warp: one 32x32 BF1
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemAccCol = 0;          // accumulators: 1 x 256 (wide) or 2 x 128 (narrow) fp32 columns
 constexpr uint32_t kTmemSfCol = 256;         // per stage: 4 SFA + 4 per 128 B columns
+constexpr int kWarpSf0 = 6;                  // single-CTA kernel: epilogue warps 6..9 (lane quarters 2, 3,
+constexpr int kSfWarps = 4;                  //   0, 1) also write each stage's scale factors into TMEM
 
 // Device error codes written to the status block (same numbers as the C ABI).
 constexpr int kErrTimeout = 6;

@@ -14,18 +14,22 @@
 //   warps 0, 12  TMA producers (even / odd stages): wait for a slot's segment
 //            to be published, then stream A (from the ring, or from the packed
 //            A when unfused), B and both scale tiles into a shared-memory ring
-//            of stages.  Two issuing warps: one thread's TMA loads overlap
+//            of stages (the scale tiles on their own barrier in the single-CTA
+//            kernel).  Two issuing warps: one thread's TMA loads overlap
 //            poorly, two reach about twice the per-SM load rate.
-//   warp 1   TMEM owner and MMA issuer: copies the stage's scale factors to
-//            TMEM (tcgen05.cp) and issues 4 tcgen05.mma kind::mxf8f6f4
+//   warp 1   TMEM owner and MMA issuer: 4 tcgen05.mma kind::mxf8f6f4
 //            block-scaled MMAs (128x256x32 each) per 128-wide K block.
 //            In the CTA-pair kernel the even CTA issues 256x256x32 MMAs for
-//            both CTAs (.cta_group::2) and the odd CTA's warp 1 forwards its
-//            stage-full and accumulator-empty signals to the even CTA.
+//            both CTAs (.cta_group::2), copying each stage's scale factors to
+//            TMEM first (tcgen05.cp); the odd CTA's loads complete on the even
+//            CTA's barriers and its epilogue warps release the accumulator
+//            there, so the odd CTA's warp 1 only owns its TMEM.
 //   warps 2-9 epilogue: TMEM -> registers -> BF16 -> shared staging -> TMA
 //            store, or, for split K, the in-kernel fixed-order reduction of
 //            the split partials.  Warp w drains TMEM lane quarter w%4, column
-//            half (w-2)/4.
+//            half (w-2)/4.  In the single-CTA kernel warps 6-9 (one per lane
+//            quarter) also write each stage's scale factors into TMEM
+//            (tcgen05.st) as soon as they land, ahead of the stage's A and B.
 //   warps 10, 11, 14, 15 staging copy (fused only): four independent workers
 //            per CTA take copy tasks (step, segment, chunk) in step order,
 //            wait for the slot's credit, copy the rows of A_seg[r] and their
@@ -89,18 +93,25 @@ __device__ __forceinline__ void trace_ev(unsigned kind, unsigned a, unsigned b) 
 #endif
 
 // In the CTA-pair kernel the even CTA's full[] barriers cover both CTAs'
-// loads of a stage (each CTA's producer arms it for its own bytes and its TMA
-// loads complete on it), and its acc_empty[] barriers count the epilogue warps
-// of both CTAs; the odd CTA's copies of those barriers are unused.
+// loads of a stage (its producer arms them for the bytes of both CTAs; every
+// TMA load of either CTA completes on them), and its acc_empty[] barriers
+// count the epilogue warps of both CTAs; the odd CTA's copies of those
+// barriers are unused.  tx_own[s]: the bytes this CTA's producer loaded into
+// stage s last; tx_odd[s] (even CTA): the odd CTA's bytes it armed stage s for.
+// (acc_empty: count 2 * kEpiWarps, one arrival per epilogue warp of each CTA.)
 struct __align__(8) SmemCtl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
     uint64_t acc_full[kMaxAccBufs];    // per TMEM accumulator buffer
     uint64_t acc_empty[kMaxAccBufs];
+    uint64_t sf_loaded[kMaxStages];    // single-CTA kernel: the stage's scale atoms have landed in smem
+    uint64_t sf_ready[kMaxStages];     // single-CTA kernel: the scale warps wrote them into TMEM
     uint64_t drain;
     uint32_t tmem_base;
     volatile int abort;
     volatile int issued[kProducers];   // per producer: 1 + index of its last issued stage
+    volatile uint32_t tx_own[kMaxStages];
+    volatile uint32_t tx_odd[kMaxStages];
     volatile int consumed;   // stages whose full barrier the MMA thread has passed
     volatile int ticket;     // split-K arrival order of the current tile (epilogue broadcast)
     volatile int epi_ok;     // epilogue broadcast: the other partials of the tile are ready
@@ -325,7 +336,11 @@ __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const
         const int mt = cta_mtile<kPair>(item, rank);
         const int nbox = fused ? num_boxes(p, mt) : 1;
         const uint32_t a_bytes = fused ? (uint32_t)(nbox * p.box_m * BK) : (uint32_t)kAStageBytes;
-        const uint32_t bytes = a_bytes + L::kBStage + kSfaStageBytes + L::kSfbStage;
+        // (CTA pair: A, B and both scale tiles on the full barrier; single CTA:
+        // the scale atoms on sf_loaded, for the scale warps)
+        const uint32_t ab_bytes = a_bytes + L::kBStage;
+        const uint32_t sf_bytes = kSfaStageBytes + L::kSfbStage;
+        const uint32_t bytes = kPair ? ab_bytes + sf_bytes : ab_bytes;
         const int b_row = item.nt * kBN + (kPair ? (int)rank * (kBN / 2) : 0);
         // One load per step first: when the copy role is ahead every segment
         // of the item's steps is already staged and the per-segment checks
@@ -395,12 +410,22 @@ __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const
                 uint8_t* a_dst = sA + (size_t)stage * kAStageBytes;
                 if (kPair) {
                     // A rows of this CTA's m-tile, its half of the tile's B rows,
-                    // its rows' A scale atom and the B scale atoms of all 256 columns
+                    // its rows' A scale atom and the B scale atoms of all 256
+                    // columns.  The even CTA arms the stage for both CTAs' bytes; the
+                    // odd CTA only issues (a remote arrive per stage would hold its
+                    // producer for a round trip).  Completions that land before the
+                    // arm leave the transaction count negative; the phase completes
+                    // only after the arrival.
                     const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
-                    if (rank == 0)
-                        mbar_arrive_expect_tx(bar, bytes);
-                    else
-                        mbar_arrive_expect_tx_remote(fb, bytes);
+                    ctl->tx_own[stage] = bytes;
+                    if (rank == 0) {
+                        const int mt_odd = cta_mtile<kPair>(item, 1);
+                        const uint32_t odd_a = fused ? (uint32_t)(num_boxes(p, mt_odd) * p.box_m * BK)
+                                                     : (uint32_t)kAStageBytes;
+                        const uint32_t odd = odd_a + L::kBStage + sf_bytes;
+                        ctl->tx_odd[stage] = odd;
+                        mbar_arrive_expect_tx(bar, bytes + odd);
+                    }
                     if (fused) {
                         for (int b = 0; b < nbox; ++b) {
                             const int row0 = mt * BM + b * p.box_m;
@@ -418,7 +443,21 @@ __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const
                     tma_load_2d_pair(sSfb + (size_t)stage * L::kSfbStage, tm_sfb, fb, 0,
                                      2 * (kbg * p.Ng2 + item.nt * L::kSfbAtoms), pol_keep);
                     ctl->issued[pid] = it + 1;
+                    TRACE(14, it, pid);
                     continue;
+                }
+                // the scale atoms first, on their own barrier: the scale warps put
+                // them into TMEM while A and B are still on their way
+                {
+                    uint64_t* sbar = &ctl->sf_loaded[stage];
+                    const int kbg = kg / BK;
+                    mbar_arrive_expect_tx(sbar, sf_bytes);
+                    bulk_load(sSfa + (size_t)stage * kSfaStageBytes, p.sfa + ((size_t)kbg * p.Mg + mt) * kSfAtomBytes,
+                              kSfaStageBytes, sbar);
+                    // the scales of all the tile's columns
+                    bulk_load(sSfb + (size_t)stage * L::kSfbStage,
+                              p.sfb + ((size_t)kbg * p.Ng2 + (size_t)item.nt * L::kSfbAtoms) * kSfAtomBytes,
+                              L::kSfbStage, sbar);
                 }
                 mbar_arrive_expect_tx(bar, bytes);
                 if (fused) {
@@ -437,14 +476,8 @@ __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const
                     tma_load_2d_hint(a_dst, tma, bar, kg, mt * BM, pol_stream);
                 }
                 tma_load_2d_hint(sB + (size_t)stage * L::kBStage, tmb, bar, kg, b_row, pol_keep);
-                const int kbg = kg / BK;
-                bulk_load(sSfa + (size_t)stage * kSfaStageBytes,
-                          p.sfa + ((size_t)kbg * p.Mg + mt) * kSfAtomBytes, kSfaStageBytes, bar);
-                // the scales of all the tile's columns: each CTA's MMA share needs them in its own TMEM
-                bulk_load(sSfb + (size_t)stage * L::kSfbStage,
-                          p.sfb + ((size_t)kbg * p.Ng2 + (size_t)item.nt * L::kSfbAtoms) * kSfAtomBytes, L::kSfbStage,
-                          bar);
                 ctl->issued[pid] = it + 1;
+                TRACE(14, it, pid);
             }
         }
     }
@@ -463,6 +496,14 @@ __device__ __forceinline__ void return_segment_credit(const GemmParams& p, int m
     }
 }
 
+// Scale factors to TMEM, per stage, into the stage's own TMEM scale columns.
+// CTA pair: the MMA thread copies them from the stage (tcgen05.cp
+// 32x128b.warpx4: a 512-byte atom lands in 4 TMEM columns, the same 32 x 16
+// bytes in every lane quarter; each CTA copies its own shared memory into its
+// own TMEM).  Single CTA: the scale warps write the same columns with
+// tcgen05.st from the stage as soon as its scale atoms have landed, ahead of
+// A and B (measured on GB300: the copies in the MMA issue stream cost about
+// a fifth of the MMA rate, the stores by other warps do not).
 template <bool kPair, int kBN>
 __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_t* sB, uint8_t* sSfa,
                          uint8_t* sSfb, SmemCtl* ctl, bool fused) {
@@ -490,18 +531,20 @@ __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_
         for (int j = 0; j < total; ++j) {
             const int stage = it % L::kStg;
             const uint32_t ph = (uint32_t)(it / L::kStg) & 1u;
-            // (CTA pair: full covers both CTAs' loads of the stage)
+            TRACE(15, it, 0);
+            // (CTA pair: full covers both CTAs' loads of the stage, scales included)
             if (!wait_mbar(p, ctl, &ctl->full[stage], ph, kRoleMma, kPair)) return;
             TRACE(11, it, 0);
             ctl->consumed = it + 1;
+            if (!kPair && !wait_mbar(p, ctl, &ctl->sf_ready[stage], ph, kRoleMma)) return;
             if (j == 0) TRACE(2, w, 0);
             tc_fence_after();
             const uint32_t sf_t = tmem + kTmemSfCol + (uint32_t)stage * L::kSfCols;
-            const uint32_t sfa_s = smem_u32(sSfa + (size_t)stage * kSfaStageBytes);
-            const uint32_t sfb_s = smem_u32(sSfb + (size_t)stage * L::kSfbStage);
             const uint64_t adesc = smem_desc(smem_u32(sA + (size_t)stage * kAStageBytes), 16, 1024, kLayoutSw128);
             const uint64_t bdesc = smem_desc(smem_u32(sB + (size_t)stage * L::kBStage), 16, 1024, kLayoutSw128);
             if (kPair) {
+                const uint32_t sfa_s = smem_u32(sSfa + (size_t)stage * kSfaStageBytes);
+                const uint32_t sfb_s = smem_u32(sSfb + (size_t)stage * L::kSfbStage);
                 tc_cp_32x128b_warpx4_pair(sf_t, smem_desc(sfa_s, 0, 128, kLayoutNone));
 #pragma unroll
                 for (int a = 0; a < L::kSfbAtoms; ++a)
@@ -513,10 +556,6 @@ __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_
                 }
                 tc_commit_pair_multicast(&ctl->empty[stage], 0x3);
             } else {
-                tc_cp_32x128b_warpx4(sf_t, smem_desc(sfa_s, 0, 128, kLayoutNone));
-#pragma unroll
-                for (int a = 0; a < L::kSfbAtoms; ++a)
-                    tc_cp_32x128b_warpx4(sf_t + 4 + 4 * a, smem_desc(sfb_s + a * kSfAtomBytes, 0, 128, kLayoutNone));
 #pragma unroll
                 for (int k = 0; k < BK / 32; ++k) {
                     const uint32_t idesc = idesc_base | ((uint32_t)k << 4) | ((uint32_t)k << 29);
@@ -525,6 +564,7 @@ __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_
                 }
                 tc_commit(&ctl->empty[stage]);
             }
+            TRACE(16, it, 0);
             ++it;
             if (fused && (j % p.kb_per_seg) == p.kb_per_seg - 1) {
                 // Every TMA read of this segment of the ring has landed in shared
@@ -546,10 +586,46 @@ __device__ void mma_role(const GemmParams& p, uint32_t tmem, uint8_t* sA, uint8_
     }
 }
 
+// The scale warps of the single-CTA kernel (epilogue warps 6..9, one per lane
+// quarter): for stages sf_it .. upto-1, as soon as a stage's scale atoms have
+// landed, this warp writes its 32 TMEM lanes of the stage's scale columns
+// with what the tcgen05.cp form would replicate there (lane l, column c of an
+// atom's 4 columns = the atom's 32-bit word l*4 + c), then arrives on
+// sf_ready[stage] (count 4).  A stage's columns are free again once its
+// scales landed anew: the producer reloads a stage only after the MMAs that
+// read it completed.
+template <bool kPair, int kBN>
+__device__ bool store_scales(const GemmParams& p, SmemCtl* ctl, uint32_t tmem, const uint8_t* sSfa,
+                             const uint8_t* sSfb, int& sf_it, int upto, int lane, int quarter) {
+    using L = Lay<kPair, kBN>;
+    for (; sf_it < upto; ++sf_it) {
+        const int stage = sf_it % L::kStg;
+        const uint32_t ph = (uint32_t)(sf_it / L::kStg) & 1u;
+        if (!wait_mbar_warp(p, ctl, &ctl->sf_loaded[stage], ph, kRoleEpi)) return false;
+        tc_fence_after();
+        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + kTmemSfCol + (uint32_t)stage * L::kSfCols;
+        const uint4 va = reinterpret_cast<const uint4*>(sSfa + (size_t)stage * kSfaStageBytes)[lane];
+        tmem_st_32x32b_x4(taddr, va);
+#pragma unroll
+        for (int a = 0; a < L::kSfbAtoms; ++a) {
+            const uint4 vb =
+                reinterpret_cast<const uint4*>(sSfb + (size_t)stage * L::kSfbStage + (size_t)a * kSfAtomBytes)[lane];
+            tmem_st_32x32b_x4(taddr + 4 + 4 * a, vb);
+        }
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->sf_ready[stage]);
+    }
+    return true;
+}
+
 // This thread has read its share of accumulator buffer `buf` (its tcgen05.ld
 // completed): release the buffer for a later item.  Single CTA: every
 // epilogue thread arrives (count kEpiThreads).  CTA pair: one arrival per
-// epilogue warp of either CTA, on the even CTA's barrier (count 2 * kEpiWarps).
+// epilogue warp of either CTA, on the even CTA's barrier (count 2 * kEpiWarps;
+// the warps arrive independently, so no warp of a CTA that gives up early can
+// hold the others).
 template <bool kPair>
 __device__ __forceinline__ void release_accumulator(SmemCtl* ctl, int buf, int lane, uint32_t rank) {
     tc_fence_before();
@@ -613,19 +689,40 @@ __device__ __forceinline__ void wait_value_u64(const GemmParams& p, SmemCtl* ctl
 
 template <bool kFused, bool kPair, int kBN>
 __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, int warp, int lane, uint32_t rank,
-                              const CUtensorMap* tmc, uint8_t* sEpi) {
+                              const CUtensorMap* tmc, uint8_t* sEpi, const uint8_t* sSfa, const uint8_t* sSfb) {
     using L = Lay<kPair, kBN>;
     const int ep = warp - kWarpEpi0;         // 0..7
     const int quarter = warp & 3;            // TMEM lanes this warp may access: 32*quarter .. +31
     const int half = ep >> 2;                // accumulator columns (kBN/2)*half .. +kBN/2-1
     const bool leader = (ep == 0 && lane == 0);
+    // Single-CTA kernel: warps 6..9 (one per lane quarter) are also the scale
+    // warps.  Before they drain item n's accumulator they write the scales of
+    // its stages and of the next item's first ones, up to kStg stages past
+    // item n (the producer can load those once item n's MMAs are done) and not
+    // past the next item (on the fused path a later item's rows may wait for
+    // staging credits that the next item returns).
+    const bool sf_warp = !kPair && warp >= kWarpSf0 && warp < kWarpSf0 + kSfWarps;
+    bool sf_ok = true;
+    int sf_it = 0;      // next stage whose scales this warp writes
+    int item_end = 0;   // stages of the items up to and including the current one
     int n = 0;   // items done; item n is in accumulator buffer n % kAccBufs
     for (int w = first_item<kPair>(); w < p.W; w += item_stride<kPair>(), ++n) {
         const Item item = decode_item(p, w);
         const int mt = cta_mtile<kPair>(item, rank);
         const int buf = n % L::kAccBufs;
         const uint32_t acc_ph = (uint32_t)(n / L::kAccBufs) & 1u;
-        const bool got = wait_mbar_warp(p, ctl, &ctl->acc_full[buf], acc_ph, kRoleEpi, kPair);
+        item_end += item.nseg * p.kb_per_seg;
+        if (sf_warp && sf_ok) {
+            int upto = item_end;
+            if (w + item_stride<kPair>() < p.W) {
+                const Item nx = decode_item(p, w + item_stride<kPair>());
+                upto = min(item_end + L::kStg, item_end + nx.nseg * p.kb_per_seg);
+            }
+            sf_ok = store_scales<kPair, kBN>(p, ctl, tmem, sSfa, sSfb, sf_it, upto, lane, quarter);
+        }
+        // (a warp whose scale stores gave up leaves through the same path as a
+        // warp whose wait ran out, so the split path's named barriers see it)
+        const bool got = sf_ok && wait_mbar_warp(p, ctl, &ctl->acc_full[buf], acc_ph, kRoleEpi, kPair);
         if (p.S > 1) {
             // the split path synchronises the 8 epilogue warps on a named barrier:
             // leave only all together
@@ -1080,8 +1177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < L::kStg; ++s) {
-            mbar_init(&ctl->full[s], kPair ? 2 : 1);   // pair: each CTA's producer arms it
+            mbar_init(&ctl->full[s], 1);   // (pair: the even CTA's producer arms it for both CTAs)
             mbar_init(&ctl->empty[s], 1);
+        }
+        for (int s = 0; s < L::kStg; ++s) {
+            mbar_init(&ctl->sf_loaded[s], 1);
+            mbar_init(&ctl->sf_ready[s], kSfWarps);
         }
         for (int b = 0; b < L::kAccBufs; ++b) {
             mbar_init(&ctl->acc_full[b], 1);
@@ -1156,7 +1257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_role<kPair, kBN>(p, tmem, sA, sB, sSfa, sSfb, ctl, kFused);
     } else if (warp < kWarpCopy0) {
         if (!p.exchange_only) {
-            epilogue_role<kFused, kPair, kBN>(p, tmem, ctl, warp, lane, rank, &tmap_c, smem + L::Epi);
+            epilogue_role<kFused, kPair, kBN>(p, tmem, ctl, warp, lane, rank, &tmap_c, smem + L::Epi, sSfa, sSfb);
             if (lane == 0) bulk_wait_all();   // this warp's C stores are complete before the CTA ends
         }
     } else if (kFused && is_copy_warp(warp)) {
@@ -1177,11 +1278,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kPair) {
         // Both CTAs' producers have stopped.  Every stage past those the MMA
         // thread consumed whose loads either CTA issued completes on the even
-        // CTA's full barrier: the even CTA arrives for whichever CTA did not arm
-        // it, then waits until the loads have landed (a normal run has none).
+        // CTA's full barrier.  Where the even CTA armed a stage the odd CTA never
+        // loaded, the odd CTA's bytes are completed by hand; where the odd CTA
+        // loaded a stage the even CTA never armed, it is armed for those bytes.
+        // Then the even CTA waits until the loads have landed (a normal run has
+        // no such stage).
         cluster_sync();
         if (rank == 0 && threadIdx.x == 0) {
             const uint32_t odd_issued = mapa_shared(smem_u32((const void*)&ctl->issued[0]), 1);
+            const uint32_t odd_tx = mapa_shared(smem_u32((const void*)&ctl->tx_own[0]), 1);
             int iss_even[kProducers], iss_odd[kProducers], hi = 0;
             for (int q = 0; q < kProducers; ++q) {
                 iss_even[q] = ctl->issued[q];
@@ -1189,10 +1294,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 hi = max(hi, max(iss_even[q], iss_odd[q]));
             }
             for (int i = ctl->consumed; i < hi; ++i) {
-                const int q = i % kProducers;
-                uint64_t* bar = &ctl->full[i % L::kStg];
-                if (i >= iss_even[q]) mbar_arrive(bar);
-                if (i >= iss_odd[q]) mbar_arrive(bar);
+                const int q = i % kProducers, stage = i % L::kStg;
+                const bool even = i < iss_even[q], odd = i < iss_odd[q];
+                if (!even && !odd) continue;   // nothing armed, nothing in flight
+                uint64_t* bar = &ctl->full[stage];
+                if (even && !odd) mbar_complete_tx(bar, ctl->tx_odd[stage]);
+                if (!even && odd)
+                    mbar_arrive_expect_tx(bar, ld_shared_cluster_u32(odd_tx + 4u * (uint32_t)stage));
                 wait_mbar_plain(p, bar, (uint32_t)(i / L::kStg) & 1u, true);
             }
         }
