@@ -33,9 +33,12 @@ constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kWarpCopy0 = 10;     // warps 10, 11, 14, 15: staging copy workers, one per warp
 constexpr int kCopyWarps = 4;      //   (fused kernel only; idle in the unfused kernel)
 constexpr int kWarpTma1 = 12;      // TMA producer 1 (one elected lane): odd stages
-// Warp 13 stays idle: it would share an SM sub-partition (warp % 4) with the
-// MMA-issuing warp 1, and a busy copy warp there slows the MMA issue.
+// Warp 13 is no copy worker: it would share an SM sub-partition (warp % 4)
+// with the MMA-issuing warp 1, and a busy copy warp there slows the MMA issue.
+// In the fused kernel one of its lanes returns the staging credits (mostly
+// asleep), so that the MMA thread issues no global atomics.
 __host__ __device__ constexpr bool is_copy_warp(int w) { return w == 10 || w == 11 || w >= 14; }
+constexpr int kWarpCredit = 13;
 // One thread's TMA loads overlap poorly (about one stage per 0.4 us per
 // thread on this GPU); two issuing warps double the per-SM load rate.
 constexpr int kProducers = 2;

@@ -249,7 +249,11 @@ void derive(mxa2a_plan* p) {
         // monotone in staging steps at group granularity (the credit protocol's
         // freedom from deadlock rests on it): g divides the m-tiles of a step, or
         // is a multiple of them within the ring's rows.
-        const int g = p->group_fused_opt;
+        // Default (option 0): half the ring's steps, so that the other half can be
+        // staged while a group is read (measured on the 8192^3 workload on GB300:
+        // DRAM reads 1.07 GB -> 0.39 GB per launch, 2-4 % faster).
+        int g = p->group_fused_opt;
+        if (g == 0 && p->cm % BM == 0) g = std::max(1, p->bn / 2) * (int)(p->cm / BM);
         if (g > 1 && !p->pair_fused && p->cm % BM == 0) {
             const int tps = (int)(p->cm / BM);                       // m-tiles per step
             const int ring = (int)((int64_t)p->bn * p->cm / BM);     // m-tiles in the ring

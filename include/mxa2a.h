@@ -365,7 +365,8 @@ enum mxa2a_option {
     MXA2A_OPT_COPY_SKEW_NS = 16,   /* test knob: the copy workers of every 4th CTA wait this many ns
                                       before each copy task (0 = off, at most 1e6) */
     MXA2A_OPT_GROUP_FUSED = 17,    /* fused raster group in m-tiles, n-tile outer inside a group
-                                      (0 or 1, default: m-tile by m-tile).  Rounded to a divisor of a
+                                      (0, default: the m-tiles of buffer_num / 2 staging steps, at least
+                                      one step; 1: m-tile by m-tile).  Rounded to a divisor of a
                                       staging step's m-tiles, or to a multiple of them within the
                                       ring's rows (buffer_num * commMSize); ignored when commMSize is
                                       not a multiple of 128 or with the CTA-pair kernel (the planner's

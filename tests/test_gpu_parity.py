@@ -316,18 +316,18 @@ def test_step_credits_and_copy_skew_same_bits(split):
         assert np.array_equal(v, outs[(0, 0)]), f"step_credits, skew = {k} differs"
 
 
-@pytest.mark.parametrize("group", [2, 3, 4, 8, 16])
+@pytest.mark.parametrize("group", [0, 1, 2, 3, 4, 8, 16])
 def test_fused_raster_groups_same_bits(group):
     """Fused raster groups (n-tile outer over whole staging steps within the
     ring) against the unfused path: the same bits, and the planner's rounding
-    of the requested group."""
+    of the requested group (0: the default, half the ring's steps)."""
     w = inputs.Workload("fgroup", 4, 2048, 256, 1040, 256, 4, 91)   # 2 m-tiles per step, 8 in the ring
     x = inputs.make_inputs(w)
     d = gu.to_device(x)
     with _plan(w, split_k=1) as p:
         ref = gu.host_bits(gu.run_gpu(p, d, w.M, w.N, fused=False))
         p.set_option(mxa2a.MXA2A_OPT_GROUP_FUSED, group)
-        want = {2: 2, 3: 2, 4: 4, 8: 8, 16: 8}[group]
+        want = {0: 4, 1: 1, 2: 2, 3: 2, 4: 4, 8: 8, 16: 8}[group]
         assert p.get_option(mxa2a.MXA2A_INFO_GROUP_FUSED) == want
         got = gu.host_bits(gu.run_gpu(p, d, w.M, w.N))
         torch.cuda.synchronize()
