@@ -12,26 +12,25 @@
 // pairs SCALE_C0 = 2): the same bytes in the hardware's own order.
 #include <cuda_bf16.h>
 
+#include "atoms.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
 
 namespace mxa2a {
 
-__device__ __forceinline__ size_t atom_word(int kbg, int groups, int x) {
-    return ((size_t)kbg * groups + (size_t)(x >> 7)) * (kSfAtomBytes / 4) + (size_t)((x & 31) * 4 + ((x & 127) >> 5));
-}
-
 // B_scale [N][K/32] -> atoms [K/128][Ng2][512]; columns N..Ng2*128 get 0.
+// One CTA per task of 128 columns x up to kTileKb K blocks, transposed in
+// shared memory (atoms.cuh).
 __global__ void pack_sfb_kernel(const uint8_t* __restrict__ B_scale, int N, int K, int Ng2, uint32_t* __restrict__ sfb) {
+    extern __shared__ uint32_t tile[];
     const int kbs = K / BK;
-    const long long total = (long long)kbs * Ng2 * 128;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int n = (int)(i % (Ng2 * 128));
-        const int kbg = (int)(i / (Ng2 * 128));
-        uint32_t v = 0;
-        if (n < N) v = ptx::ld_nc_u32(B_scale + (size_t)n * (K / 32) + (size_t)kbg * 4);
-        sfb[atom_word(kbg, Ng2, n)] = v;
+    const long long tasks = atom_tile_tasks(Ng2, kbs);
+    const size_t ld = (size_t)(K / 32);
+    auto load = [&](int kbg, int n) { return ptx::ld_nc_u32(B_scale + (size_t)n * ld + (size_t)kbg * 4); };
+    for (long long t = blockIdx.x; t < tasks; t += gridDim.x) {
+        const int g = (int)(t % Ng2), kb0 = (int)(t / Ng2) * kTileKb;
+        pack_atom_tile(sfb, Ng2, N, g, kb0, min(kTileKb, kbs - kb0), tile, threadIdx.x, blockDim.x, load,
+                       [] { __syncthreads(); });
     }
 }
 
@@ -52,22 +51,20 @@ __global__ void pack_a_kernel(const __grid_constant__ GemmParams p, uint8_t* __r
         const uint4 v = ptx::ld_nc_v4(p.A_seg[src.seg] + (size_t)src.row * seg_ld(p) + seg_col0(p, r) + kin);
         *reinterpret_cast<uint4*>(a_packed + (size_t)m * p.K + k) = v;
     }
+    // the scales: one warp per task of 128 rows x 4 K blocks (atoms.cuh)
     const int kbs = p.K / BK;
-    const long long nsf = (long long)kbs * p.Mg * 128;
+    const long long tasks = atom_tasks(p.Mg, kbs);
     uint32_t* sfa = reinterpret_cast<uint32_t*>(p.sfa_stage);
-    for (long long i = tid; i < nsf; i += stride) {
-        const int m = (int)(i % (p.Mg * 128));
-        const int kbg = (int)(i / (p.Mg * 128));
-        uint32_t v = 0;
-        if (m < p.M) {
-            const int r = kbg / p.kb_per_seg;
-            const int kb = kbg - r * p.kb_per_seg;
-            const SegRow src = seg_row(p, r, m);
-            v = ptx::ld_nc_u32(p.A_sf_seg[src.seg] + (size_t)src.row * (seg_ld(p) / 32) + seg_col0(p, r) / 32 +
-                               (size_t)kb * 4);
-        }
-        sfa[atom_word(kbg, p.Mg, m)] = v;
-    }
+    const int lane = threadIdx.x & 31;
+    auto load = [&](int kbg, int m) {
+        const int r = kbg / p.kb_per_seg;
+        const int kb = kbg - r * p.kb_per_seg;
+        const SegRow src = seg_row(p, r, m);
+        return ptx::ld_nc_u32(p.A_sf_seg[src.seg] + (size_t)src.row * (seg_ld(p) / 32) + seg_col0(p, r) / 32 +
+                              (size_t)kb * 4);
+    };
+    for (long long t = tid >> 5; t < tasks; t += stride >> 5)
+        pack_atom_task(sfa, p.Mg, kbs, p.M, (int)(t % p.Mg), (int)(t / p.Mg), lane, load);
 }
 
 __global__ void l2_flush_kernel(uint4* buf, long long n16) {
@@ -91,8 +88,11 @@ static int grid_for(long long work, int threads) {
 }
 
 cudaError_t launch_pack_sfb(const uint8_t* B_scale, int N, int K, int Ng2, uint8_t* sfb, cudaStream_t stream) {
-    const long long total = (long long)(K / BK) * Ng2 * 128;
-    pack_sfb_kernel<<<grid_for(total, 256), 256, 0, stream>>>(B_scale, N, K, Ng2, reinterpret_cast<uint32_t*>(sfb));
+    // one CTA per task (at most 8 per SM at a time)
+    const long long tasks = atom_tile_tasks(Ng2, K / BK);
+    const size_t smem = (size_t)kTileWords * 4;
+    pack_sfb_kernel<<<grid_for(tasks * 256, 256), 256, smem, stream>>>(B_scale, N, K, Ng2,
+                                                                      reinterpret_cast<uint32_t*>(sfb));
     return cudaGetLastError();
 }
 

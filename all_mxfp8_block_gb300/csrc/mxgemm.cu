@@ -65,6 +65,7 @@
 
 #include <cstring>
 
+#include "atoms.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -144,6 +145,7 @@ struct Lay {
     static_assert(kStg <= kMaxStages && kAccBufs <= kMaxAccBufs, "barrier arrays");
     static_assert(kAccBufs * kBN <= (int)kTmemSfCol && kTmemSfCol + kStg * kSfCols <= kTmemCols, "TMEM columns");
     static_assert(Epi % 1024 == 0, "C staging buffers need 512-byte alignment for the 64-byte swizzle");
+    static_assert((size_t)kStg * kAStageBytes >= (size_t)kTileWords * 4, "the prologue's pack tile fits the A stages");
 };
 
 // ------------------------------------------------------------------ work items
@@ -330,6 +332,7 @@ __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const
         if (!wait_counter(p, ctl, p.flags + FlagLayout::sfb_done(p.bn, p.R), gridDim.x, kRoleTma, -1, -1, -1))
             return;
         fence_proxy_async_global();   // the atoms were written through the generic proxy; TMA reads them
+        if (pid == 0) TRACE(23, 0, 0);
     }
     for (int w = first_item<kPair>(); w < p.W; w += item_stride<kPair>()) {
         const Item item = decode_item(p, w);
@@ -839,6 +842,7 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
                 release_accumulator<kPair>(ctl, buf, lane, rank);
             }
             named_barrier_sync(2, kEpiThreads);   // (also makes the leader's ticket visible)
+            if (leader) TRACE(30, w, ctl->ticket);
             const bool last = ctl->ticket == p.S - 1;
             if (!last) {
                 __threadfence();
@@ -856,21 +860,30 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
                     ctl->epi_ok = ok ? 1 : 0;
                 }
                 named_barrier_sync(2, kEpiThreads);
+                if (leader) TRACE(31, w, 0);
                 const bool ok = ctl->epi_ok != 0;   // uniform over the epilogue warps
-                // M is a multiple of 64, so a warp's 32 rows are all inside M or all past it
-                if (ok && row_w < p.M) {
+                // The reduction is spread over all 8 epilogue warps by units of 32
+                // rows x 32 columns inside M (M is a multiple of 64, so a 32-row
+                // group is all inside M or all past it); each unit sums the S
+                // partials in the fixed order q = 0..S-1 with the next split's
+                // loads in flight while the previous one is added.
+                if (ok) {
+                    const int rows_tile = min(BM, p.M - mt * BM);
+                    const int units = ((rows_tile + 31) / 32) * (kBN / 32);
 #pragma unroll 1
-                    for (int c = 0; c < kChunks; ++c) {
-                        // fixed order q = 0..S-1, whichever split finished last
+                    for (int u = ep; u < units; u += kEpiWarps) {
+                        const int rg = u / (kBN / 32), cc = u - rg * (kBN / 32);
+                        const float* base = part_tile + ((size_t)(cc * 8) * BM + (size_t)(rg * 32 + lane)) * 4;
                         float acc[32];
 #pragma unroll
                         for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
-                        for (int q = 0; q < p.S; ++q) {
-                            const float* src =
-                                part_tile + (size_t)q * (BM * kBN) + ((size_t)(tcol / 4 + c * 8) * BM + lrow) * 4;
-                            uint4 t[8];
+                        uint4 ta[8], tb[8];
+                        auto load = [&](uint4 (&t)[8], int q) {
+                            const float* src = base + (size_t)q * (BM * kBN);
 #pragma unroll
                             for (int j = 0; j < 8; ++j) t[j] = ld_cg_v4(src + (size_t)j * BM * 4);
+                        };
+                        auto add = [&](const uint4 (&t)[8]) {
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
                                 acc[4 * j] += __uint_as_float(t[j].x);
@@ -878,15 +891,26 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
                                 acc[4 * j + 2] += __uint_as_float(t[j].z);
                                 acc[4 * j + 3] += __uint_as_float(t[j].w);
                             }
+                        };
+                        load(ta, 0);
+#pragma unroll 1
+                        for (int q = 0; q < p.S; q += 2) {
+                            if (q + 1 < p.S) load(tb, q + 1);
+                            add(ta);
+                            if (q + 1 < p.S) {
+                                if (q + 2 < p.S) load(ta, q + 2);
+                                add(tb);
+                            }
                         }
                         uint32_t wds[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
                             wds[j] = pack_bf16x2(__float_as_uint(acc[2 * j]), __float_as_uint(acc[2 * j + 1]));
-                        store_c_chunk(p, tmc, cbuf, lane, wds, col0 + c * 32, row_w, p.M);
+                        store_c_chunk(p, tmc, cbuf, lane, wds, item.nt * kBN + cc * 32, mt * BM + rg * 32, p.M);
                     }
                 }
                 if (leader) p.tile_cnt[tile] = 0u;   // ready for the next launch
+                if (leader) TRACE(32, w, 0);
                 if (!ok) return;
             }
         }
@@ -1146,43 +1170,44 @@ __device__ void copy_role(const GemmParams& p, SmemCtl* ctl, int lane) {
     }
 }
 
-// A slice of the B scale pack (the same byte permutation as pack_sfb_kernel):
-// word (kbg, n) of the atoms = the 4 E8M0 bytes of column n for 128-wide K
-// block kbg, at (n%32)*4 + (n%128)/32 of atom (kbg, n/128); columns past N
-// get 0.
-__device__ void pack_sfb_slice(const GemmParams& p, int tid, int nthreads) {
+// This CTA's share of the B scale pack (the same byte permutation as
+// pack_sfb_kernel): word (kbg, n) of the atoms = the 4 E8M0 bytes of column n
+// for 128-wide K block kbg, at (n%32)*4 + (n%128)/32 of atom (kbg, n/128);
+// columns past N get 0.  Tasks of 128 columns x up to kTileKb K blocks go
+// round the CTAs; the nthreads threads taking part (tid, barrier sync) share
+// one transposing tile in shared memory (the pipeline stages, unused yet).
+template <typename Sync>
+__device__ void pack_sfb_cta(const GemmParams& p, uint32_t* tile, int tid, int nthreads, Sync sync) {
     uint32_t* sfb = reinterpret_cast<uint32_t*>(const_cast<uint8_t*>(p.sfb));   // written only here
-    const int cols = p.Ng2 * 128;
-    const long long total = (long long)(p.K / BK) * cols;
-    const long long stride = (long long)gridDim.x * nthreads;
-    for (long long i = blockIdx.x * (long long)nthreads + tid; i < total; i += stride) {
-        const int n = (int)(i % cols);
-        const int kbg = (int)(i / cols);
-        const uint32_t v = n < p.N ? ld_nc_u32(p.B_scale + (size_t)n * (p.K / 32) + (size_t)kbg * 4) : 0u;
-        sfb[((size_t)kbg * p.Ng2 + (size_t)(n >> 7)) * (kSfAtomBytes / 4) + (size_t)((n & 31) * 4 + ((n & 127) >> 5))] = v;
+    const int kbs = p.K / BK;
+    const long long tasks = atom_tile_tasks(p.Ng2, kbs);
+    const uint8_t* src = p.B_scale;
+    const size_t ld = (size_t)(p.K / 32);
+    auto load = [&](int kbg, int n) { return ld_nc_u32(src + (size_t)n * ld + (size_t)kbg * 4); };
+    for (long long t = blockIdx.x; t < tasks; t += gridDim.x) {
+        const int g = (int)(t % p.Ng2), kb0 = (int)(t / p.Ng2) * kTileKb;
+        pack_atom_tile(sfb, p.Ng2, p.N, g, kb0, min(kTileKb, kbs - kb0), tile, tid, nthreads, load, sync);
     }
 }
 
-// A slice of the A scale pack for the direct variant (the scale part of
-// pack_a_kernel): word (kbg, m) = the 4 E8M0 bytes of row m for 128-wide K
+// This CTA's share of the A scale pack for the direct variant (the scale part
+// of pack_a_kernel): word (kbg, m) = the 4 E8M0 bytes of row m for 128-wide K
 // block kbg, from segment kbg / kb_per_seg; rows past M get 0.
-__device__ void pack_sfa_slice(const GemmParams& p) {
+template <typename Sync>
+__device__ void pack_sfa_cta(const GemmParams& p, uint32_t* tile, int tid, int nthreads, Sync sync) {
     uint32_t* sfa = reinterpret_cast<uint32_t*>(p.sfa_stage);
-    const int rows = p.Mg * BM;
-    const long long total = (long long)(p.K / BK) * rows;
-    const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += stride) {
-        const int m = (int)(i % rows);
-        const int kbg = (int)(i / rows);
+    const int kbs = p.K / BK;
+    const long long tasks = atom_tile_tasks(p.Mg, kbs);
+    auto load = [&](int kbg, int m) {
         const int r = kbg / p.kb_per_seg;
         const int kb = kbg - r * p.kb_per_seg;
-        uint32_t v = 0u;
-        if (m < p.M) {
-            const SegRow src = seg_row(p, r, m);
-            v = ld_nc_u32(p.A_sf_seg[src.seg] + (size_t)src.row * (seg_ld(p) / 32) + seg_col0(p, r) / 32 +
-                          (size_t)kb * 4);
-        }
-        sfa[((size_t)kbg * p.Mg + (size_t)(m >> 7)) * (kSfAtomBytes / 4) + (size_t)((m & 31) * 4 + ((m & 127) >> 5))] = v;
+        const SegRow src = seg_row(p, r, m);
+        return ld_nc_u32(p.A_sf_seg[src.seg] + (size_t)src.row * (seg_ld(p) / 32) + seg_col0(p, r) / 32 +
+                         (size_t)kb * 4);
+    };
+    for (long long t = blockIdx.x; t < tasks; t += gridDim.x) {
+        const int g = (int)(t % p.Mg), kb0 = (int)(t / p.Mg) * kTileKb;
+        pack_atom_tile(sfa, p.Mg, p.M, g, kb0, min(kTileKb, kbs - kb0), tile, tid, nthreads, load, sync);
     }
 }
 
@@ -1225,6 +1250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_trace_n = 0;
 #endif
         fence_mbarrier_init();
+        TRACE(20, 0, 0);
     }
     if (warp == kWarpMma) {
         if (kPair) {
@@ -1249,6 +1275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kPair) cluster_sync();   // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
+    if (threadIdx.x == 0) TRACE(21, 0, 0);
     if (p.sfb_inline || p.direct) {
         // every CTA packs its slice of the B scales (and, direct, of the A
         // scales); the producers wait for all of them before their first load
@@ -1258,20 +1285,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr int kPackThreads = kThreads - kCopyWarps * 32;
             if (!is_copy_warp(warp)) {
                 const int pw = warp < 10 ? warp : warp - 2;   // warps 0..9, 12, 13 -> 0..11
-                if (p.sfb_inline) pack_sfb_slice(p, pw * 32 + lane, kPackThreads);
+                if (p.sfb_inline)
+                    pack_sfb_cta(p, reinterpret_cast<uint32_t*>(sA), pw * 32 + lane, kPackThreads,
+                                 [] { named_barrier_sync(3, kPackThreads); });
                 named_barrier_sync(3, kPackThreads);
                 if (threadIdx.x == 0) {
                     __threadfence();
                     red_release_add_u64(p.flags + FlagLayout::sfb_done(p.bn, p.R), 1ull);
+                    TRACE(22, 0, 0);
                 }
             }
         } else {
-            if (p.sfb_inline) pack_sfb_slice(p, threadIdx.x, blockDim.x);
-            if (p.direct) pack_sfa_slice(p);
+            auto sync = [] { __syncthreads(); };
+            if (p.sfb_inline) pack_sfb_cta(p, reinterpret_cast<uint32_t*>(sA), threadIdx.x, kThreads, sync);
+            if (p.direct) pack_sfa_cta(p, reinterpret_cast<uint32_t*>(sA), threadIdx.x, kThreads, sync);
             __syncthreads();
             if (threadIdx.x == 0) {
                 __threadfence();
                 red_release_add_u64(p.flags + FlagLayout::sfb_done(p.bn, p.R), 1ull);
+                TRACE(22, 0, 0);
             }
         }
     }
@@ -1297,8 +1329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (!kFused && p.rs_rows > 0 && is_copy_warp(warp)) {
         rs_reduce_role(p, ctl, lane);
     }
+    if (lane == 0) TRACE(27, warp, 0);
     __syncwarp();
     __syncthreads();
+    if (threadIdx.x == 0) TRACE(24, 0, 0);
 
     // After an abort, let every TMA load already issued land before the CTA exits
     // (each producer waits for its own stages beyond those the MMA side consumed).
@@ -1357,6 +1391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_dealloc_pair(tmem, kTmemCols);
         else
             tmem_dealloc(tmem, kTmemCols);
+        if (lane == 0) TRACE(25, 0, 0);
     }
     if ((kFused || p.S > 1 || p.sfb_inline || p.direct) && threadIdx.x == 0) {
         // The last CTA to finish zeroes the staging credits and the scale-pack
@@ -1366,25 +1401,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned long long* done = p.flags + FlagLayout::cta_done(p.bn, p.R);
         const unsigned long long prev = atomicAdd(done, 1ull);
         if (prev == (unsigned long long)gridDim.x - 1) {
+            // Every other CTA counted itself after its last access to these
+            // words, so plain stores do (serialised atomics cost several
+            // microseconds here with many segments).
             __threadfence();
+            auto zero = [](unsigned long long* w) { *reinterpret_cast<volatile unsigned long long*>(w) = 0ull; };
             if (kFused) {
-                atomicExch(p.flags + FlagLayout::copy_next(p.bn, p.R), 0ull);
+                zero(p.flags + FlagLayout::copy_next(p.bn, p.R));
                 for (int slot = 0; slot < p.bn; ++slot) {
-                    atomicExch(p.flags + FlagLayout::staged(slot, p.bn, p.R), 0ull);
+                    zero(p.flags + FlagLayout::staged(slot, p.bn, p.R));
                     for (int r = 0; r < p.R; ++r) {
-                        atomicExch(p.flags + FlagLayout::filled(slot, r, p.R), 0ull);
-                        atomicExch(p.flags + FlagLayout::drained(slot, r, p.bn, p.R), 0ull);
+                        zero(p.flags + FlagLayout::filled(slot, r, p.R));
+                        zero(p.flags + FlagLayout::drained(slot, r, p.bn, p.R));
                     }
                 }
             }
-            if (p.sfb_inline || p.direct) atomicExch(p.flags + FlagLayout::sfb_done(p.bn, p.R), 0ull);
+            if (p.sfb_inline || p.direct) zero(p.flags + FlagLayout::sfb_done(p.bn, p.R));
             if (!kFused && p.rs_rows > 0) {   // the reduce-scatter task counter and tile counts
-                atomicExch(p.flags + FlagLayout::copy_next(p.bn, p.R), 0ull);
+                zero(p.flags + FlagLayout::copy_next(p.bn, p.R));
                 for (int t = 0; t < p.Mt * p.Nt; ++t) p.rs_cnt[t] = 0ull;
             }
             if (p.S > 1 && launch_failed(p))
-                for (int t = 0; t < p.Mt * p.Nt; ++t) atomicExch(&p.tile_cnt[t], 0u);
-            atomicExch(done, 0ull);
+                for (int t = 0; t < p.Mt * p.Nt; ++t) reinterpret_cast<volatile unsigned*>(p.tile_cnt)[t] = 0u;
+            zero(done);
+            __threadfence();
+            TRACE(26, 0, 0);
             __threadfence();
         }
     }
