@@ -44,7 +44,7 @@ ABLATION_WORKLOAD = 1         # the 2048 x 4096 x 4096 problem: the ring limits 
 FP8_OVER_BF16 = 2.0           # nominal dense fp8 : bf16 tensor rate (4.5 : 2.25 PFLOP/s)
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["mxgemm.cu", "kernels.cuh", "ptx.cuh"]
+KERNEL_SOURCES = ["mxgemm.cu", "kernels.cuh", "ptx.cuh", "atoms.cuh"]
 
 
 # ----------------------------------------------------------------------------- helpers
