@@ -112,12 +112,11 @@ struct GemmParams {
     int direct;
     const CUtensorMap* seg_maps;
     uint16_t* C;                // bf16 [M][N]
-    // split-K (S > 1): items of one output tile finish in any order; all but the
-    // last write their fp32 tile to partial[tile][q] ([BM][BN]) and publish
-    // ready[tile][q] = launch_id; the last (ticket S-1 of tile_cnt[tile]) sums
-    // q = 0..S-1 in order, writes C and zeroes tile_cnt[tile]
+    // split-K (S > 1): every split writes its fp32 tile to partial[tile][q]
+    // ([BM][BN]) and publishes ready[tile][q] = launch_id; once all S have,
+    // split q sums its share of the tile's units, q = 0..S-1 in order, and
+    // writes C
     float* partial;             // fp32 [Mt*Nt][S][tile_n/4][BM][4] (4-column chunks, row-contiguous)
-    unsigned* tile_cnt;         // [Mt*Nt]
     unsigned long long* ready;  // [Mt*Nt][S]
     // fused staging
     int fused, exchange_only;

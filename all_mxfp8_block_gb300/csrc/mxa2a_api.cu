@@ -135,7 +135,6 @@ struct mxa2a_plan {
     // fp32 partial tiles [Mt*Nt][S][128][256] | tile counters u32 [Mt*Nt] | ready u64 [Mt*Nt][S]
     uint8_t* split_ws = nullptr;
     float* partial = nullptr;
-    unsigned* tile_cnt = nullptr;
     unsigned long long* ready = nullptr;
     unsigned long long* flags = nullptr;
     DevStatus* status = nullptr;
@@ -362,7 +361,6 @@ void fill_params(mxa2a_plan* p, GemmParams& g, const void* const* A_seg, const v
     g.sfb = p->sfb;
     g.C = static_cast<uint16_t*>(C);
     g.partial = p->partial;
-    g.tile_cnt = p->tile_cnt;
     g.ready = p->ready;
     g.fused = fused ? 1 : 0;
     g.exchange_only = fused ? p->exchange_only : 0;
@@ -404,24 +402,22 @@ int ensure_partials(mxa2a_plan* p) {
     // Nt * tile_n <= Ng2 * 128 for both tile widths
     const size_t tiles = (size_t)p->Mt * std::max(p->Nt_fused, p->Nt_unfused);
     const size_t part = (size_t)p->Mt * S * BM * ((size_t)p->Ng2 * 128) * sizeof(float);
-    const size_t cnt = align_up(tiles * sizeof(unsigned), 256);
     const size_t rdy = tiles * S * sizeof(unsigned long long);
-    const size_t need = part + cnt + rdy;
+    const size_t need = part + rdy;
     if (need <= p->partial_bytes) return MXA2A_OK;
     if (p->split_ws) cudaFree(p->split_ws);
     p->split_ws = nullptr;
     p->partial = nullptr;
     p->partial_bytes = 0;
     if (cudaMalloc(reinterpret_cast<void**>(&p->split_ws), need) != cudaSuccess ||
-        cudaMemset(p->split_ws + part, 0, cnt + rdy) != cudaSuccess) {
+        cudaMemset(p->split_ws + part, 0, rdy) != cudaSuccess) {
         cudaGetLastError();
         if (p->split_ws) cudaFree(p->split_ws);
         p->split_ws = nullptr;
         return MXA2A_ERR_CUDA;
     }
     p->partial = reinterpret_cast<float*>(p->split_ws);
-    p->tile_cnt = reinterpret_cast<unsigned*>(p->split_ws + part);
-    p->ready = reinterpret_cast<unsigned long long*>(p->split_ws + part + cnt);
+    p->ready = reinterpret_cast<unsigned long long*>(p->split_ws + part);
     p->partial_bytes = need;
     return MXA2A_OK;
 }

@@ -114,7 +114,6 @@ struct __align__(8) SmemCtl {
     volatile uint32_t tx_own[kMaxStages];
     volatile uint32_t tx_odd[kMaxStages];
     volatile int consumed;   // stages whose full barrier the MMA thread has passed
-    volatile int ticket;     // split-K arrival order of the current tile (epilogue broadcast)
     volatile int epi_ok;     // epilogue broadcast: the other partials of the tile are ready
     volatile int epi_warp_ok[kEpiWarps];
 };
@@ -719,6 +718,10 @@ __device__ __forceinline__ void wait_value_u64(const GemmParams& p, SmemCtl* ctl
     if (!wait_counter(p, ctl, ptr, want, kRoleEpi, -1, -1, -1)) *ok = false;
 }
 
+template <bool kPair, int kBN>
+__device__ void split_reduce(const GemmParams& p, SmemCtl* ctl, const CUtensorMap* tmc, uint8_t* cbuf, int ep,
+                             int lane, uint32_t rank);
+
 template <bool kFused, bool kPair, int kBN>
 __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, int warp, int lane, uint32_t rank,
                               const CUtensorMap* tmc, uint8_t* sEpi, const uint8_t* sSfa, const uint8_t* sSfb) {
@@ -818,102 +821,107 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
                 __syncwarp();
             }
         } else {
+            // Every split writes its fp32 partial, frees the accumulator (so the next
+            // item's MMAs overlap) and publishes ready[tile][q].  Partial tile layout
+            // [kBN/4][BM][4]: thread `lrow` of a warp stores the float4 of columns
+            // 4g..4g+3 at (g*BM + lrow)*4, so each warp store covers 512 contiguous bytes.
             const size_t tile = (size_t)mt * p.Nt + item.nt;
-            if (leader) ctl->ticket = (int)atomicAdd(&p.tile_cnt[tile], 1u);
-            // Every split first writes its fp32 partial and frees the accumulator, so the
-            // next item's MMAs overlap the reduction.  Partial tile layout [kBN/4][BM][4]:
-            // thread `lrow` of a warp stores the float4 of columns 4g..4g+3 at
-            // (g*BM + lrow)*4, so each warp store covers 512 contiguous bytes.
-            float* part_tile = p.partial + tile * (size_t)p.S * (BM * kBN);
-            {
-                float* dst = part_tile + (size_t)item.q * (BM * kBN) + ((size_t)(tcol / 4) * BM + lrow) * 4;
+            float* dst = p.partial + (tile * p.S + item.q) * (size_t)(BM * kBN) + ((size_t)(tcol / 4) * BM + lrow) * 4;
 #pragma unroll 1
-                for (int c = 0; c < kChunks; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), v);
-                    tc_wait_ld();
-                    if (row < p.M) {
+            for (int c = 0; c < kChunks; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), v);
+                tc_wait_ld();
+                if (row < p.M) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            *reinterpret_cast<uint4*>(dst + (size_t)(c * 8 + j) * BM * 4) =
-                                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                    }
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4*>(dst + (size_t)(c * 8 + j) * BM * 4) =
+                            make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                 }
-                release_accumulator<kPair>(ctl, buf, lane, rank);
             }
-            named_barrier_sync(2, kEpiThreads);   // (also makes the leader's ticket visible)
-            if (leader) TRACE(30, w, ctl->ticket);
-            const bool last = ctl->ticket == p.S - 1;
-            if (!last) {
-                __threadfence();
-                named_barrier_sync(2, kEpiThreads);
-                if (leader)
-                    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p.ready + tile * p.S + item.q),
-                                 "l"(p.launch_id)
-                                 : "memory");
-            } else {
-                // wait until every other split of this tile has published its partial
-                if (leader) {
-                    bool ok = true;
-                    for (int q = 0; q < p.S && ok; ++q)
-                        if (q != item.q) wait_value_u64(p, ctl, p.ready + tile * p.S + q, p.launch_id, &ok);
-                    ctl->epi_ok = ok ? 1 : 0;
-                }
-                named_barrier_sync(2, kEpiThreads);
-                if (leader) TRACE(31, w, 0);
-                const bool ok = ctl->epi_ok != 0;   // uniform over the epilogue warps
-                // The reduction is spread over all 8 epilogue warps by units of 32
-                // rows x 32 columns inside M (M is a multiple of 64, so a 32-row
-                // group is all inside M or all past it); each unit sums the S
-                // partials in the fixed order q = 0..S-1 with the next split's
-                // loads in flight while the previous one is added.
-                if (ok) {
-                    const int rows_tile = min(BM, p.M - mt * BM);
-                    const int units = ((rows_tile + 31) / 32) * (kBN / 32);
-#pragma unroll 1
-                    for (int u = ep; u < units; u += kEpiWarps) {
-                        const int rg = u / (kBN / 32), cc = u - rg * (kBN / 32);
-                        const float* base = part_tile + ((size_t)(cc * 8) * BM + (size_t)(rg * 32 + lane)) * 4;
-                        float acc[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
-                        uint4 ta[8], tb[8];
-                        auto load = [&](uint4 (&t)[8], int q) {
-                            const float* src = base + (size_t)q * (BM * kBN);
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) t[j] = ld_cg_v4(src + (size_t)j * BM * 4);
-                        };
-                        auto add = [&](const uint4 (&t)[8]) {
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                acc[4 * j] += __uint_as_float(t[j].x);
-                                acc[4 * j + 1] += __uint_as_float(t[j].y);
-                                acc[4 * j + 2] += __uint_as_float(t[j].z);
-                                acc[4 * j + 3] += __uint_as_float(t[j].w);
-                            }
-                        };
-                        load(ta, 0);
-#pragma unroll 1
-                        for (int q = 0; q < p.S; q += 2) {
-                            if (q + 1 < p.S) load(tb, q + 1);
-                            add(ta);
-                            if (q + 1 < p.S) {
-                                if (q + 2 < p.S) load(ta, q + 2);
-                                add(tb);
-                            }
-                        }
-                        uint32_t wds[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            wds[j] = pack_bf16x2(__float_as_uint(acc[2 * j]), __float_as_uint(acc[2 * j + 1]));
-                        store_c_chunk(p, tmc, cbuf, lane, wds, item.nt * kBN + cc * 32, mt * BM + rg * 32, p.M);
-                    }
-                }
-                if (leader) p.tile_cnt[tile] = 0u;   // ready for the next launch
-                if (leader) TRACE(32, w, 0);
-                if (!ok) return;
+            release_accumulator<kPair>(ctl, buf, lane, rank);
+            __threadfence();
+            named_barrier_sync(2, kEpiThreads);
+            if (leader) {
+                asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p.ready + tile * p.S + item.q),
+                             "l"(p.launch_id)
+                             : "memory");
+                TRACE(30, w, item.q);
             }
         }
+    }
+    if (p.S > 1) split_reduce<kPair, kBN>(p, ctl, tmc, sEpi + (size_t)ep * kEpiBufBytes, ep, lane, rank);
+}
+
+// The split-K sums, after this CTA has published the partials of all its
+// items (so no CTA waits for a partial before publishing its own: every wait
+// ends, as all CTAs are resident).  For each of its items (tile, q) it waits
+// until every split of the tile has published, then sums its share of the
+// tile: the units of 32 rows x 32 columns inside M numbered q, q + S, q + 2S,
+// ..., spread over the 8 epilogue warps (M is a multiple of 64, so a 32-row
+// group is all inside M or all past it).  Each unit sums the S partials in
+// the fixed order q = 0..S-1, the next split's loads in flight while the
+// previous one is added, and stores its BF16 32 x 32 box of C.
+template <bool kPair, int kBN>
+__device__ void split_reduce(const GemmParams& p, SmemCtl* ctl, const CUtensorMap* tmc, uint8_t* cbuf, int ep,
+                             int lane, uint32_t rank) {
+    const bool leader = (ep == 0 && lane == 0);
+    for (int w = first_item<kPair>(); w < p.W; w += item_stride<kPair>()) {
+        const Item item = decode_item(p, w);
+        const int mt = cta_mtile<kPair>(item, rank);
+        const size_t tile = (size_t)mt * p.Nt + item.nt;
+        if (leader) {
+            bool ok = true;
+            for (int q = 0; q < p.S && ok; ++q)
+                if (q != item.q) wait_value_u64(p, ctl, p.ready + tile * p.S + q, p.launch_id, &ok);
+            ctl->epi_ok = ok ? 1 : 0;
+            TRACE(31, w, 0);
+        }
+        named_barrier_sync(2, kEpiThreads);
+        const bool ok = ctl->epi_ok != 0;   // uniform over the epilogue warps
+        named_barrier_sync(2, kEpiThreads);   // (every warp has read it before the leader writes it again)
+        if (!ok) return;
+        const float* part_tile = p.partial + tile * (size_t)p.S * (BM * kBN);
+        const int rows_tile = min(BM, p.M - mt * BM);
+        const int units = ((rows_tile + 31) / 32) * (kBN / 32);
+#pragma unroll 1
+        for (int u = item.q + p.S * ep; u < units; u += p.S * kEpiWarps) {
+            const int rg = u / (kBN / 32), cc = u - rg * (kBN / 32);
+            const float* base = part_tile + ((size_t)(cc * 8) * BM + (size_t)(rg * 32 + lane)) * 4;
+            float acc[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
+            uint4 ta[8], tb[8];
+            auto load = [&](uint4 (&t)[8], int q) {
+                const float* src = base + (size_t)q * (BM * kBN);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) t[j] = ld_cg_v4(src + (size_t)j * BM * 4);
+            };
+            auto add = [&](const uint4 (&t)[8]) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    acc[4 * j] += __uint_as_float(t[j].x);
+                    acc[4 * j + 1] += __uint_as_float(t[j].y);
+                    acc[4 * j + 2] += __uint_as_float(t[j].z);
+                    acc[4 * j + 3] += __uint_as_float(t[j].w);
+                }
+            };
+            load(ta, 0);
+#pragma unroll 1
+            for (int q = 0; q < p.S; q += 2) {
+                if (q + 1 < p.S) load(tb, q + 1);
+                add(ta);
+                if (q + 1 < p.S) {
+                    if (q + 2 < p.S) load(ta, q + 2);
+                    add(tb);
+                }
+            }
+            uint32_t wds[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) wds[j] = pack_bf16x2(__float_as_uint(acc[2 * j]), __float_as_uint(acc[2 * j + 1]));
+            store_c_chunk(p, tmc, cbuf, lane, wds, item.nt * kBN + cc * 32, mt * BM + rg * 32, p.M);
+        }
+        if (leader) TRACE(32, w, 0);
     }
 }
 
@@ -1421,8 +1429,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 zero(p.flags + FlagLayout::copy_next(p.bn, p.R));
                 for (int t = 0; t < p.Mt * p.Nt; ++t) p.rs_cnt[t] = 0ull;
             }
-            if (p.S > 1 && launch_failed(p))
-                for (int t = 0; t < p.Mt * p.Nt; ++t) reinterpret_cast<volatile unsigned*>(p.tile_cnt)[t] = 0u;
             zero(done);
             __threadfence();
             TRACE(26, 0, 0);
