@@ -718,9 +718,9 @@ __device__ __forceinline__ void wait_value_u64(const GemmParams& p, SmemCtl* ctl
     if (!wait_counter(p, ctl, ptr, want, kRoleEpi, -1, -1, -1)) *ok = false;
 }
 
-template <bool kPair, int kBN>
-__device__ void split_reduce(const GemmParams& p, SmemCtl* ctl, const CUtensorMap* tmc, uint8_t* cbuf, int ep,
-                             int lane, uint32_t rank);
+template <int kBN>
+__device__ bool split_reduce(const GemmParams& p, SmemCtl* ctl, const CUtensorMap* tmc, uint8_t* cbuf, int ep,
+                             int lane, const Item& item, int mt, int w);
 
 template <bool kFused, bool kPair, int kBN>
 __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, int warp, int lane, uint32_t rank,
@@ -848,81 +848,82 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
                              : "memory");
                 TRACE(30, w, item.q);
             }
+            if (!split_reduce<kBN>(p, ctl, tmc, cbuf, ep, lane, item, mt, w)) return;
         }
     }
-    if (p.S > 1) split_reduce<kPair, kBN>(p, ctl, tmc, sEpi + (size_t)ep * kEpiBufBytes, ep, lane, rank);
 }
 
-// The split-K sums, after this CTA has published the partials of all its
-// items (so no CTA waits for a partial before publishing its own: every wait
-// ends, as all CTAs are resident).  For each of its items (tile, q) it waits
-// until every split of the tile has published, then sums its share of the
-// tile: the units of 32 rows x 32 columns inside M numbered q, q + S, q + 2S,
-// ..., spread over the 8 epilogue warps (M is a multiple of 64, so a 32-row
-// group is all inside M or all past it).  Each unit sums the S partials in
-// the fixed order q = 0..S-1, the next split's loads in flight while the
-// previous one is added, and stores its BF16 32 x 32 box of C.
-template <bool kPair, int kBN>
-__device__ void split_reduce(const GemmParams& p, SmemCtl* ctl, const CUtensorMap* tmc, uint8_t* cbuf, int ep,
-                             int lane, uint32_t rank) {
+// The split-K sums of item (tile, q), right after this split has published
+// its partial (the MMA thread meanwhile runs the next item): wait until every
+// split of the tile has published, then sum this split's share of the tile,
+// the units of 32 rows x 32 columns inside M numbered q, q + S, q + 2S, ...,
+// spread over the 8 epilogue warps (M is a multiple of 64, so a 32-row group
+// is all inside M or all past it).  Each unit sums the S partials in the
+// fixed order q = 0..S-1, the next split's loads in flight while the previous
+// one is added, and stores its BF16 32 x 32 box of C.  Every wait ends: the
+// K split is the innermost item index, so a tile's splits are consecutive
+// items, which the persistent grid runs in one round or two adjacent ones;
+// by induction over the rounds every CTA reaches and publishes each of its
+// items (all CTAs are resident).  False when the wait gave up.
+template <int kBN>
+__device__ bool split_reduce(const GemmParams& p, SmemCtl* ctl, const CUtensorMap* tmc, uint8_t* cbuf, int ep,
+                             int lane, const Item& item, int mt, int w) {
     const bool leader = (ep == 0 && lane == 0);
-    for (int w = first_item<kPair>(); w < p.W; w += item_stride<kPair>()) {
-        const Item item = decode_item(p, w);
-        const int mt = cta_mtile<kPair>(item, rank);
-        const size_t tile = (size_t)mt * p.Nt + item.nt;
-        if (leader) {
-            bool ok = true;
-            for (int q = 0; q < p.S && ok; ++q)
-                if (q != item.q) wait_value_u64(p, ctl, p.ready + tile * p.S + q, p.launch_id, &ok);
-            ctl->epi_ok = ok ? 1 : 0;
-            TRACE(31, w, 0);
-        }
-        named_barrier_sync(2, kEpiThreads);
-        const bool ok = ctl->epi_ok != 0;   // uniform over the epilogue warps
-        named_barrier_sync(2, kEpiThreads);   // (every warp has read it before the leader writes it again)
-        if (!ok) return;
-        const float* part_tile = p.partial + tile * (size_t)p.S * (BM * kBN);
-        const int rows_tile = min(BM, p.M - mt * BM);
-        const int units = ((rows_tile + 31) / 32) * (kBN / 32);
-#pragma unroll 1
-        for (int u = item.q + p.S * ep; u < units; u += p.S * kEpiWarps) {
-            const int rg = u / (kBN / 32), cc = u - rg * (kBN / 32);
-            const float* base = part_tile + ((size_t)(cc * 8) * BM + (size_t)(rg * 32 + lane)) * 4;
-            float acc[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
-            uint4 ta[8], tb[8];
-            auto load = [&](uint4 (&t)[8], int q) {
-                const float* src = base + (size_t)q * (BM * kBN);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) t[j] = ld_cg_v4(src + (size_t)j * BM * 4);
-            };
-            auto add = [&](const uint4 (&t)[8]) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    acc[4 * j] += __uint_as_float(t[j].x);
-                    acc[4 * j + 1] += __uint_as_float(t[j].y);
-                    acc[4 * j + 2] += __uint_as_float(t[j].z);
-                    acc[4 * j + 3] += __uint_as_float(t[j].w);
-                }
-            };
-            load(ta, 0);
-#pragma unroll 1
-            for (int q = 0; q < p.S; q += 2) {
-                if (q + 1 < p.S) load(tb, q + 1);
-                add(ta);
-                if (q + 1 < p.S) {
-                    if (q + 2 < p.S) load(ta, q + 2);
-                    add(tb);
-                }
-            }
-            uint32_t wds[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) wds[j] = pack_bf16x2(__float_as_uint(acc[2 * j]), __float_as_uint(acc[2 * j + 1]));
-            store_c_chunk(p, tmc, cbuf, lane, wds, item.nt * kBN + cc * 32, mt * BM + rg * 32, p.M);
-        }
-        if (leader) TRACE(32, w, 0);
+    const size_t tile = (size_t)mt * p.Nt + item.nt;
+    if (leader) {
+        bool ok = true;
+        for (int q = 0; q < p.S && ok; ++q)
+            if (q != item.q) wait_value_u64(p, ctl, p.ready + tile * p.S + q, p.launch_id, &ok);
+        ctl->epi_ok = ok ? 1 : 0;
+        TRACE(31, w, 0);
     }
+    named_barrier_sync(2, kEpiThreads);
+    const bool ok = ctl->epi_ok != 0;   // uniform over the epilogue warps
+    named_barrier_sync(2, kEpiThreads);   // (every warp has read it before the leader writes it again)
+    if (!ok) return false;
+    const float* part_tile = p.partial + tile * (size_t)p.S * (BM * kBN);
+    const int rows_tile = min(BM, p.M - mt * BM);
+    const int units = ((rows_tile + 31) / 32) * (kBN / 32);
+#pragma unroll 1
+    for (int u = item.q + p.S * ep; u < units; u += p.S * kEpiWarps) {
+        const int rg = u / (kBN / 32), cc = u - rg * (kBN / 32);
+        const float* base = part_tile + ((size_t)(cc * 8) * BM + (size_t)(rg * 32 + lane)) * 4;
+        float acc[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
+        uint4 ta[8], tb[8];
+        auto load = [&](uint4 (&t)[8], int q) {
+            const float* src = base + (size_t)q * (BM * kBN);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) t[j] = ld_cg_v4(src + (size_t)j * BM * 4);
+        };
+        auto add = [&](const uint4 (&t)[8]) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                acc[4 * j] += __uint_as_float(t[j].x);
+                acc[4 * j + 1] += __uint_as_float(t[j].y);
+                acc[4 * j + 2] += __uint_as_float(t[j].z);
+                acc[4 * j + 3] += __uint_as_float(t[j].w);
+            }
+        };
+        load(ta, 0);
+#pragma unroll 1
+        for (int q = 0; q < p.S; q += 2) {
+            if (q + 1 < p.S) load(tb, q + 1);
+            add(ta);
+            if (q + 1 < p.S) {
+                if (q + 2 < p.S) load(ta, q + 2);
+                add(tb);
+            }
+        }
+        uint32_t wds[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            wds[j] = pack_bf16x2(__float_as_uint(acc[2 * j]), __float_as_uint(acc[2 * j + 1]));
+        store_c_chunk(p, tmc, cbuf, lane, wds, item.nt * kBN + cc * 32, mt * BM + rg * 32, p.M);
+    }
+    if (leader) TRACE(32, w, 0);
+    return true;
 }
 
 // One warp copies `bytes` (a multiple of 16): 16 loads of 16 bytes in flight
