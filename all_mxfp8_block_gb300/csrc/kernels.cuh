@@ -112,6 +112,8 @@ struct GemmParams {
     int direct;
     const CUtensorMap* seg_maps;
     uint16_t* C;                // bf16 [M][N]
+    uint16_t* c_host;           // non-null: C goes to this host buffer (its device view) instead, by
+                                // generic stores from the epilogue (no reduce-scatter routing then)
     // split-K (S > 1): every split writes its fp32 tile to partial[tile][q]
     // ([BM][BN]) and publishes ready[tile][q] = launch_id; once all S have,
     // split q sums its share of the tile's units, q = 0..S-1 in order, and

@@ -110,6 +110,7 @@ struct mxa2a_plan {
     int tn_fused = BN, tn_unfused = BN;     // tile width per path (256, or 128 = the narrow tile)
     int Nt_fused = 0, Nt_unfused = 0;       // n-tiles per path
     int tile_opt = 0;                       // option: 0 automatic, 128 or 256 forced
+    void* c_host = nullptr;                 // during a host-buffer run: C's host buffer (device view)
     int elem_types = 0;                     // option: element-format pair (MXA2A_OPT_ELEM_TYPES)
     int step_credits = 0;                   // option: whole-step staging credits
     int copy_skew_ns = 0;                   // test knob: delay of every 4th CTA's copies
@@ -461,6 +462,7 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
     int launches = 0;
     GemmParams g;
     fill_params(p, g, A_seg, A_sf, C, fused);
+    g.c_host = rs ? nullptr : static_cast<uint16_t*>(p->c_host);
     if (mode == kRunDirect) {
         // the single-CTA GEMM reading A in place: one tensor map per segment,
         // re-encoded and copied to the workspace when the segment pointers change
@@ -926,15 +928,16 @@ int mxa2a_run_host(mxa2a_plan* p, const void* const* A_seg_h, const void* const*
             if (cudaMemcpyAsync(dst[i], src[i], len[i], cudaMemcpyHostToDevice, s) != cudaSuccess)
                 return MXA2A_ERR_CUDA;
     }
-    rc = run_impl(p, dA, dS, dB, dBs, dC, stream_v, kRunFused);
-    if (rc) return rc;
+    // A pinned C is written by the epilogue itself, tile by tile, through its
+    // device view: the host link carries C while the GEMM runs.  Otherwise
+    // one DMA copy after the run.
     void* c_view = const_cast<void*>(host_device_view(C_h));
-    if (c_view && aligned(c_view, 16)) {
-        const void* c_src = dC;
-        if ((rc = cuda_rc(launch_copy_list(1, &c_src, &c_view, &c_b, s)))) return rc;
-    } else if (cudaMemcpyAsync(C_h, dC, c_b, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
-        return MXA2A_ERR_CUDA;
-    }
+    const bool c_direct = c_view && aligned(c_view, 16);
+    p->c_host = c_direct ? c_view : nullptr;
+    rc = run_impl(p, dA, dS, dB, dBs, dC, stream_v, kRunFused);
+    p->c_host = nullptr;
+    if (rc) return rc;
+    if (!c_direct && cudaMemcpyAsync(C_h, dC, c_b, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MXA2A_ERR_CUDA;
     return MXA2A_OK;
 }
 

@@ -687,12 +687,29 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bi
 // previous store must have finished reading it.
 __device__ __forceinline__ void store_c_chunk(const GemmParams& p, const CUtensorMap* tmc, uint8_t* buf, int lane,
                                               const uint32_t* w, int x, int y, int ylim) {
-    if (lane == 0) bulk_wait_read_all();
+    if (lane == 0 && !p.c_host) bulk_wait_read_all();
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int pj = j ^ ((lane >> 1) & 3);
         *reinterpret_cast<uint4*>(buf + lane * 64 + pj * 16) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    }
+    if (p.c_host) {
+        // C in a host buffer: generic 16-byte stores from the staging buffer, four
+        // lanes per 64-byte row segment (8 rows per warp store); they stream over
+        // the host link while the next items run.  Units of 8 columns are all
+        // inside N or all past it (N % 16 == 0).
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int u = k * 32 + lane, r = u >> 2, c = u & 3;
+            const int gx = x + c * 8;
+            if (y + r < ylim && gx < p.N)
+                *reinterpret_cast<uint4*>(p.c_host + (size_t)(y + r) * p.N + gx) =
+                    *reinterpret_cast<const uint4*>(buf + r * 64 + ((c ^ ((r >> 1) & 3)) * 16));
+        }
+        __syncwarp();   // (read out before the next chunk rewrites the buffer)
+        return;
     }
     fence_proxy_async_shared();   // the generic-proxy writes, before the TMA (async proxy) reads them
     __syncwarp();

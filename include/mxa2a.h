@@ -306,8 +306,8 @@ int mxa2a_run_unfused(mxa2a_plan *plan, const void *const *A_seg, const void *co
  * their device addresses: pinned A segments and scales are read in place by
  * the fused kernel's staging copies (the exchange then comes from host
  * memory), pinned B and B_scale are copied by the SMs in one launch, and a
- * pinned C is written back the same way; pageable buffers go through one DMA
- * copy each.  The host buffers must stay unchanged until the stream has
+ * pinned C is written by the GEMM's epilogue itself, tile by tile, while the
+ * GEMM runs; pageable buffers go through one DMA copy each.  The host buffers must stay unchanged until the stream has
  * passed the run.  Errors as for mxa2a_run.
  * Passage: all_to_all_matmul.cpp (the launcher), InitData and the
  * aclrtMemcpy calls that move the inputs to the device before the launch and

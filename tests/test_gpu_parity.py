@@ -361,6 +361,18 @@ def test_forced_split_k(split):
     assert np.array_equal(got_f, got_u)
 
 
+@pytest.mark.parametrize("fused", [True, False])
+def test_split_k_tiles_straddling_grid_rounds(fused):
+    """K split 3 on a grid of 4 CTAs (27 items): the 3 splits of most tiles are
+    run by CTAs in two consecutive rounds of the persistent grid, and each split
+    waits for its siblings before it sums its share of the tile."""
+    w = inputs.Workload("straddle", 6, 384, 256, 640, 128, 2, 61)
+    with _plan(w, split_k=3, grid=4) as p:
+        key = mxa2a.MXA2A_INFO_GRID_FUSED if fused else mxa2a.MXA2A_INFO_GRID_UNFUSED
+        assert p.get_option(key) == 4
+    _check_full(w, fused=fused, split_k=3, grid=4)
+
+
 def test_split_k_deterministic_over_runs():
     """The split partials are summed in a fixed order whichever split finishes
     last, so repeated runs give identical bits."""
@@ -509,8 +521,10 @@ def test_non_default_stream_and_host_entry():
 
 
 def test_host_entry_pinned_and_pageable_same_bits():
-    """mxa2a_run_host with pinned host buffers (copied by the SMs) and with
-    pageable ones (DMA copies), and a mix: the same bits as the device entry."""
+    """mxa2a_run_host with pinned host buffers (inputs read or copied by the SMs,
+    a pinned C written by the epilogue itself) and with pageable ones (DMA
+    copies), and a mix: the same bits as the device entry.  N = 400 leaves a
+    ragged 16-column tail in the last 32-column chunk."""
     w = inputs.Workload("hostcopy", 3, 384, 256, 400, 128, 2, 97)
     x = inputs.make_inputs(w)
     d = gu.to_device(x)
@@ -530,6 +544,23 @@ def test_host_entry_pinned_and_pageable_same_bits():
             outs.append(hC.numpy().view(np.uint16).copy())
     for o in outs:
         assert np.array_equal(o, ref)
+
+
+def test_host_entry_pinned_output_with_split_k():
+    """The split-K sums also write a pinned C through its device view."""
+    w = inputs.Workload("hostsplit", 4, 256, 256, 528, 128, 2, 101)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w, split_k=3) as p:
+        ref = gu.host_bits(gu.run_gpu(p, d, w.M, w.N))
+        hA = [a.pin_memory() for a in x["A_seg"]]
+        hS = [a.pin_memory() for a in x["A_scale_seg"]]
+        hC = torch.full((w.M, w.N), -1, dtype=torch.int16).pin_memory()
+        p.run_host(hA, hS, x["B"].pin_memory(), x["B_scale"].pin_memory(), hC)
+        torch.cuda.synchronize()
+        _status_ok(p)
+    assert np.array_equal(hC.numpy().view(np.uint16), ref)
+    gu.assert_parity(ref, gu.oracle_full(x), "hostsplit")
 
 
 def test_zero_A_gives_zero():
