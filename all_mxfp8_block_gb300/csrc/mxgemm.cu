@@ -823,9 +823,44 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
                 y = blk >= 0 ? row_w - blk * p.rs_rows : 0;
                 ylim = blk >= 0 ? p.rs_rows : 0;
             }
+            if (p.c_host && !rs) {
+                // C in a host buffer: the warp's rows go through the staging buffer
+                // kHostRows at a time (a lane writes its row's kHostCols columns), so
+                // that every warp store writes whole row pieces of 2 * kHostCols bytes.
+                // Measured on GB300 over the host link (8192^3): 64-byte pieces
+                // 145 GB/s, 128 and 256 bytes 163 GB/s, a thread per row 3.5x slower.
+                constexpr int kHostCols = kBN / 2;                                 // columns per round
+                constexpr int kUnits = kHostCols / 8;                              // 16-byte units per row
+                constexpr int kHostRows = kEpiBufBytes / (2 * kHostCols);          // rows per round
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c)
-                store_c_chunk(p, dst, cbuf, lane, packed + c * 16, col0 + c * 32, y, ylim);
+                for (int c = 0; c < kBN / 2; c += kHostCols) {
+#pragma unroll
+                    for (int h = 0; h < 32 / kHostRows; ++h) {
+                        if (lane / kHostRows == h) {
+                            const int rr = lane % kHostRows;
+#pragma unroll
+                            for (int u = 0; u < kUnits; ++u)
+                                *reinterpret_cast<uint4*>(cbuf + rr * (kUnits * 16) + ((u ^ (rr & 7)) * 16)) =
+                                    make_uint4(packed[c / 2 + 4 * u], packed[c / 2 + 4 * u + 1],
+                                               packed[c / 2 + 4 * u + 2], packed[c / 2 + 4 * u + 3]);
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < kHostRows * kUnits / 32; ++k) {
+                            const int t = k * 32 + lane, rr = t / kUnits, u = t % kUnits;
+                            const int gy = row_w + h * kHostRows + rr, gx = col0 + c + u * 8;
+                            if (gy < p.M && gx < p.N)
+                                *reinterpret_cast<uint4*>(p.c_host + (size_t)gy * p.N + gx) =
+                                    *reinterpret_cast<const uint4*>(cbuf + rr * (kUnits * 16) + ((u ^ (rr & 7)) * 16));
+                        }
+                        __syncwarp();   // (read out before the next round rewrites the buffer)
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c)
+                    store_c_chunk(p, dst, cbuf, lane, packed + c * 16, col0 + c * 32, y, ylim);
+            }
             if (rs && mt * BM < (p.rs_own + 1) * p.rs_rows && (mt + 1) * BM > p.rs_own * p.rs_rows) {
                 // a tile with rows of this rank's block: once this warp's stores have
                 // landed, count it for the copy warps that sum those rows
