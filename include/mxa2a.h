@@ -349,8 +349,8 @@ enum mxa2a_option {
                                       fused path, buffer_num covers the steps of a 256-row tile;
                                       0 (default): the single-CTA kernel */
     MXA2A_OPT_GROUP_M = 11,        /* largest raster group of the unfused path, in m rows
-                                      (128-row tiles, or tile pairs), default 16; the fused path
-                                      always consumes the staging steps one m row at a time */
+                                      (128-row tiles, or tile pairs), default 16 (the fused path's
+                                      group: MXA2A_OPT_GROUP_FUSED) */
     MXA2A_OPT_TILE_N = 13,         /* GEMM tile width: 0 (default: 256) or 128 / 256.  128 doubles the
                                       tiles for the rows in flight and overlaps each tile's epilogue
                                       with the next tile (two TMEM accumulators) */
