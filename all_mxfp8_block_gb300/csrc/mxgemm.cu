@@ -198,6 +198,15 @@ __device__ __forceinline__ int item_stride() {
     return kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 }
 
+// With the rows in one m-tile (M <= 128) every B scale atom is read by exactly
+// one item (an item is an n-tile and a K range; a tile's K splits cover
+// disjoint ranges), so each CTA of the single-CTA kernel packs the atoms its
+// own items read, and its producers need no grid-wide count, only this CTA's
+// barrier.
+__device__ __forceinline__ bool own_sfb_pack(const GemmParams& p) {
+    return p.sfb_inline && !p.direct && p.Mt == 1;
+}
+
 __device__ __forceinline__ int num_boxes(const GemmParams& p, int mt) {
     const int rows = min(BM, p.M - mt * BM);
     return (rows + p.box_m - 1) / p.box_m;
@@ -328,7 +337,9 @@ __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const
     const uint64_t pol_stream = l2_policy_evict_first();
     int it = 0;   // global stage sequence number; this producer issues it % kProducers == pid
     if (p.sfb_inline || p.direct) {
-        if (!wait_counter(p, ctl, p.flags + FlagLayout::sfb_done(p.bn, p.R), gridDim.x, kRoleTma, -1, -1, -1))
+        // (all CTAs' atoms: the grid-wide count; only this CTA's own: its barrier, passed already)
+        if ((kPair || !own_sfb_pack(p)) &&
+            !wait_counter(p, ctl, p.flags + FlagLayout::sfb_done(p.bn, p.R), gridDim.x, kRoleTma, -1, -1, -1))
             return;
         fence_proxy_async_global();   // the atoms were written through the generic proxy; TMA reads them
         if (pid == 0) TRACE(23, 0, 0);
@@ -1251,6 +1262,22 @@ __device__ void pack_sfb_cta(const GemmParams& p, uint32_t* tile, int tid, int n
     }
 }
 
+// Each CTA packs the B scale atoms its own items read (see own_sfb_pack).
+template <int kBN, typename Sync>
+__device__ void pack_sfb_own(const GemmParams& p, uint32_t* tile, int tid, int nthreads, Sync sync) {
+    uint32_t* sfb = reinterpret_cast<uint32_t*>(const_cast<uint8_t*>(p.sfb));   // written only here
+    const uint8_t* src = p.B_scale;
+    const size_t ld = (size_t)(p.K / 32);
+    auto load = [&](int kbg, int n) { return ld_nc_u32(src + (size_t)n * ld + (size_t)kbg * 4); };
+    for (int w = first_item<false>(); w < p.W; w += item_stride<false>()) {
+        const Item item = decode_item(p, w);
+        const int kb_lo = item.seg_lo * p.kb_per_seg, kb_hi = (item.seg_lo + item.nseg) * p.kb_per_seg;
+        for (int g = item.nt * (kBN / 128); g < (item.nt + 1) * (kBN / 128); ++g)
+            for (int kb0 = kb_lo; kb0 < kb_hi; kb0 += kTileKb)
+                pack_atom_tile(sfb, p.Ng2, p.N, g, kb0, min(kTileKb, kb_hi - kb0), tile, tid, nthreads, load, sync);
+    }
+}
+
 // This CTA's share of the A scale pack for the direct variant (the scale part
 // of pack_a_kernel): word (kbg, m) = the 4 E8M0 bytes of row m for 128-wide K
 // block kbg, from segment kbg / kb_per_seg; rows past M get 0.
@@ -1346,11 +1373,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr int kPackThreads = kThreads - kCopyWarps * 32;
             if (!is_copy_warp(warp)) {
                 const int pw = warp < 10 ? warp : warp - 2;   // warps 0..9, 12, 13 -> 0..11
-                if (p.sfb_inline)
-                    pack_sfb_cta(p, reinterpret_cast<uint32_t*>(sA), pw * 32 + lane, kPackThreads,
-                                 [] { named_barrier_sync(3, kPackThreads); });
+                auto sync = [] { named_barrier_sync(3, kPackThreads); };
+                if (!kPair && own_sfb_pack(p))
+                    pack_sfb_own<kBN>(p, reinterpret_cast<uint32_t*>(sA), pw * 32 + lane, kPackThreads, sync);
+                else if (p.sfb_inline)
+                    pack_sfb_cta(p, reinterpret_cast<uint32_t*>(sA), pw * 32 + lane, kPackThreads, sync);
                 named_barrier_sync(3, kPackThreads);
-                if (threadIdx.x == 0) {
+                if (threadIdx.x == 0 && (kPair || !own_sfb_pack(p))) {
                     __threadfence();
                     red_release_add_u64(p.flags + FlagLayout::sfb_done(p.bn, p.R), 1ull);
                     TRACE(22, 0, 0);
@@ -1358,10 +1387,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else {
             auto sync = [] { __syncthreads(); };
-            if (p.sfb_inline) pack_sfb_cta(p, reinterpret_cast<uint32_t*>(sA), threadIdx.x, kThreads, sync);
+            if (!kPair && own_sfb_pack(p))
+                pack_sfb_own<kBN>(p, reinterpret_cast<uint32_t*>(sA), threadIdx.x, kThreads, sync);
+            else if (p.sfb_inline)
+                pack_sfb_cta(p, reinterpret_cast<uint32_t*>(sA), threadIdx.x, kThreads, sync);
             if (p.direct) pack_sfa_cta(p, reinterpret_cast<uint32_t*>(sA), threadIdx.x, kThreads, sync);
             __syncthreads();
-            if (threadIdx.x == 0) {
+            if (threadIdx.x == 0 && (kPair || !own_sfb_pack(p))) {
                 __threadfence();
                 red_release_add_u64(p.flags + FlagLayout::sfb_done(p.bn, p.R), 1ull);
                 TRACE(22, 0, 0);

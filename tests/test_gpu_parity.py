@@ -563,6 +563,29 @@ def test_host_entry_pinned_output_with_split_k():
     gu.assert_parity(ref, gu.oracle_full(x), "hostsplit")
 
 
+@pytest.mark.parametrize("split", [1, 4])
+def test_host_entry_pinned_output_rows_and_columns_past_the_ends(split):
+    """M = 64 (half a tile) and N = 400 (a ragged last tile): the epilogue's
+    stores to a pinned C skip the rows past M and the columns past N, with K
+    unsplit (whole 256-byte row pieces) and split 4 (the split sums' pieces)."""
+    w = inputs.Workload("hostm64", 4, 64, 256, 400, 64, 2, 103)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w, split_k=split) as p:
+        ref = gu.host_bits(gu.run_gpu(p, d, w.M, w.N))
+        hA = [a.pin_memory() for a in x["A_seg"]]
+        hS = [a.pin_memory() for a in x["A_scale_seg"]]
+        # one pinned buffer with a guard row after C: nothing may be written past M x N
+        guard = torch.full((w.M + 1, w.N), -1, dtype=torch.int16).pin_memory()
+        p.run_host(hA, hS, x["B"].pin_memory(), x["B_scale"].pin_memory(), guard[:w.M])
+        torch.cuda.synchronize()
+        _status_ok(p)
+    out = guard.numpy().view(np.uint16)
+    assert np.array_equal(out[:w.M], ref)
+    assert np.all(out[w.M] == 0xFFFF)
+    gu.assert_parity(ref, gu.oracle_full(x), f"hostm64 split {split}")
+
+
 def test_zero_A_gives_zero():
     w = inputs.Workload("zero", 2, 128, 128, 256, 64, 2, 0)
     x = inputs.make_inputs(w)
