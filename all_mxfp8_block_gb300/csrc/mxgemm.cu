@@ -1412,7 +1412,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp < kWarpCopy0) {
         if (!p.exchange_only) {
             epilogue_role<kFused, kPair, kBN>(p, tmem, ctl, warp, lane, rank, &tmap_c, smem + L::Epi, sSfa, sSfb);
-            if (lane == 0) bulk_wait_all();   // this warp's C stores are complete before the CTA ends
+            // this warp's C stores have read its staging buffer before the CTA ends
+            // (their writes are complete when the kernel is)
+            if (lane == 0) bulk_wait_read_all();
         }
     } else if (kFused && warp == kWarpCredit) {
         // (CTA pair: the even CTA returns both m-tiles' credits)
@@ -1486,18 +1488,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_dealloc(tmem, kTmemCols);
         if (lane == 0) TRACE(25, 0, 0);
     }
-    if ((kFused || p.S > 1 || p.sfb_inline || p.direct) && threadIdx.x == 0) {
-        // The last CTA to finish zeroes the staging credits and the scale-pack
-        // count for the next launch, and, if this launch gave up somewhere, the
-        // split-K tile counters.
-        __threadfence();
+    if ((kFused || p.sfb_inline || p.direct || (!kFused && p.rs_rows > 0)) && threadIdx.x == 0) {
+        // The last CTA to finish zeroes the staging credits, the scale-pack
+        // count and the reduce-scatter counts for the next launch.  The count
+        // of finished CTAs releases each CTA's accesses and acquires the others'.
         unsigned long long* done = p.flags + FlagLayout::cta_done(p.bn, p.R);
-        const unsigned long long prev = atomicAdd(done, 1ull);
+        const unsigned long long prev = atom_acq_rel_add_u64(done, 1ull);
         if (prev == (unsigned long long)gridDim.x - 1) {
             // Every other CTA counted itself after its last access to these
             // words, so plain stores do (serialised atomics cost several
-            // microseconds here with many segments).
-            __threadfence();
+            // microseconds here with many segments); the next launch sees them
+            // after this one's end.
             auto zero = [](unsigned long long* w) { *reinterpret_cast<volatile unsigned long long*>(w) = 0ull; };
             if (kFused) {
                 zero(p.flags + FlagLayout::copy_next(p.bn, p.R));
@@ -1515,9 +1516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < p.Mt * p.Nt; ++t) p.rs_cnt[t] = 0ull;
             }
             zero(done);
-            __threadfence();
             TRACE(26, 0, 0);
-            __threadfence();
         }
     }
 }
