@@ -91,6 +91,9 @@ struct FlagLayout {
 struct GemmParams {
     int R, M, N, ka, K, cm, bn, steps;
     int Mt, Nt, S, W;           // m-tiles, n-tiles, K splits, work items
+    // tail split (S == 1, single-CTA kernel): items W_dp .. W-1 are the last
+    // (W - W_dp) / S_tail tiles, each split S_tail ways in K; W_dp = W: none
+    int W_dp, S_tail;
     int pair;                   // 1: CTA-pair kernel, work items are pairs of m-tiles (Mt even)
     int tile_n;                 // BN of this launch: 256 or 128 (Nt = ceil(N / tile_n))
     int fmt_a, fmt_b;           // element formats (MMA type codes): 0 E4M3, 1 E5M2
@@ -114,12 +117,13 @@ struct GemmParams {
     uint16_t* C;                // bf16 [M][N]
     uint16_t* c_host;           // non-null: C goes to this host buffer (its device view) instead, by
                                 // generic stores from the epilogue (no reduce-scatter routing then)
-    // split-K (S > 1): every split writes its fp32 tile to partial[tile][q]
-    // ([BM][BN]) and publishes ready[tile][q] = launch_id; once all S have,
-    // split q sums its share of the tile's units, q = 0..S-1 in order, and
-    // writes C
-    float* partial;             // fp32 [Mt*Nt][S][tile_n/4][BM][4] (4-column chunks, row-contiguous)
-    unsigned long long* ready;  // [Mt*Nt][S]
+    // split-K (S > 1, or a tail item): every split writes its fp32 tile to
+    // partial[slot][q] ([BM][BN]) and publishes ready[slot][q] = launch_id;
+    // once all splits have, split q sums its share of the tile's units, the
+    // splits in order, and writes C.  slot: the tile (mt * Nt + nt) under a
+    // uniform split, its place among the tail's tiles for a tail item.
+    float* partial;             // fp32 [slots][S][tile_n/4][BM][4] (4-column chunks, row-contiguous)
+    unsigned long long* ready;  // [slots][S]
     // fused staging
     int fused, exchange_only;
     int rows_per_chunk, chunks_per_seg, n_copy_tasks;

@@ -115,6 +115,9 @@ struct mxa2a_plan {
     int step_credits = 0;                   // option: whole-step staging credits
     int copy_skew_ns = 0;                   // test knob: delay of every 4th CTA's copies
     int S_fused = 1, S_unfused = 1, W_fused = 0, W_unfused = 0;   // K splits and work items per path
+    int Wdp_fused = 0, Wdp_unfused = 0;     // items before the split tail (= W: no tail split)
+    int St_fused = 1, St_unfused = 1;       // K split of the tail's tiles
+    int tail_split = 1;                     // option: 1 allows the tail split
     int pair_fused = 0, pair_unfused = 0;   // CTA-pair kernel in use, per path
     int group_fused = 1, group_unfused = 1; // raster group, in m rows (tiles or tile pairs)
     int group_cap = 16;                     // option: largest unfused raster group
@@ -198,14 +201,18 @@ void derive(mxa2a_plan* p) {
     // (buffer_num * commMSize rows), the unfused path on all tiles.
     // Split only when the tiles fill at most a quarter of the GPU: the in-kernel
     // reduction of the partials costs more than a partly idle GPU otherwise.
-    auto split_for = [&](int tiles) {
-        if (p->force_split > 0) return std::min(p->force_split, p->R);
+    // No more splits than persistent CTAs (CTA pairs): a tile's splits must
+    // run on different ones (each waits for the others).
+    const int cta_cap = p->grid_cap > 0 ? std::min(p->sm_count, p->grid_cap) : p->sm_count;
+    auto split_for = [&](int tiles, bool pair) {
+        const int lim = std::max(1, pair ? cta_cap / 2 : cta_cap);
+        if (p->force_split > 0) return std::min({p->force_split, p->R, lim});
         int S = 1;
         if (tiles * 4 <= p->sm_count && p->K >= 1024) {
             S = std::min<int>(p->R, p->sm_count / tiles);
             while (S > 1 && p->K / S < 512) --S;
         }
-        return std::max(1, S);
+        return std::max(1, std::min(S, lim));
     };
     const int window_mtiles = (int)std::min<int64_t>(p->Mt, (p->bn * p->cm + BM - 1) / BM);
     // The CTA-pair kernel computes 256-row tiles with one 2-CTA MMA stream; it
@@ -230,8 +237,8 @@ void derive(mxa2a_plan* p) {
     p->tn_unfused = pick(p->pair_unfused);
     p->Nt_fused = (int)((p->N + p->tn_fused - 1) / p->tn_fused);
     p->Nt_unfused = (int)((p->N + p->tn_unfused - 1) / p->tn_unfused);
-    p->S_fused = split_for(window_mtiles * p->Nt_fused);
-    p->S_unfused = split_for(p->Mt * p->Nt_unfused);
+    p->S_fused = split_for(window_mtiles * p->Nt_fused, p->pair_fused);
+    p->S_unfused = split_for(p->Mt * p->Nt_unfused, p->pair_unfused);
     p->W_fused = (p->pair_fused ? p->Mt / 2 : p->Mt) * p->Nt_fused * p->S_fused;
     p->W_unfused = (p->pair_unfused ? p->Mt / 2 : p->Mt) * p->Nt_unfused * p->S_unfused;
     // Raster groups (m rows processed n-tile outer inside a group).  Unfused:
@@ -297,6 +304,28 @@ void derive(mxa2a_plan* p) {
     } else {
         p->grid_unfused = std::max(1, std::min(cap, p->W_unfused));
     }
+    // Tail split (single-CTA kernel, no uniform split): when the tiles fill
+    // the persistent grid more than once, the last round holds rem = W % grid
+    // of them and leaves the other CTAs idle.  If rem is at most half the grid,
+    // those tiles are split in two along K (R even, each half reading R / 2
+    // segments), so that the last round takes half a tile.  A split costs a
+    // fixed epilogue: measured on GB300 (8192^3, traced) about 3.6 us to write
+    // the fp32 partial, 1 us waiting for the other half and 2.5 us for the sum,
+    // against 13.6 us of MMAs saved; so only where a half tile has at least
+    // 32 K blocks (K >= 8192).  Quarter splits of 4096-deep tiles measured
+    // 16-27 us slower than whole tiles.
+    auto tail = [&](int& W, int S, int grid, bool pair, int& Wdp, int& St) {
+        Wdp = W;
+        St = 1;
+        if (!p->tail_split || pair || S != 1 || W <= grid || p->R % 2 != 0 || p->K < 8192) return;
+        const int rem = W % grid;
+        if (rem == 0 || 2 * rem > grid) return;
+        St = 2;
+        Wdp = W - rem;
+        W = Wdp + rem * St;
+    };
+    tail(p->W_fused, p->S_fused, p->grid_fused, p->pair_fused, p->Wdp_fused, p->St_fused);
+    tail(p->W_unfused, p->S_unfused, p->grid_unfused, p->pair_unfused, p->Wdp_unfused, p->St_unfused);
 }
 
 bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
@@ -350,6 +379,8 @@ void fill_params(mxa2a_plan* p, GemmParams& g, const void* const* A_seg, const v
     g.fmt_b = kFmtB[p->elem_types];
     g.S = fused ? p->S_fused : p->S_unfused;
     g.W = fused ? p->W_fused : p->W_unfused;
+    g.W_dp = fused ? p->Wdp_fused : p->Wdp_unfused;
+    g.S_tail = fused ? p->St_fused : p->St_unfused;
     g.pair = fused ? p->pair_fused : p->pair_unfused;
     g.group_m = fused ? p->group_fused : p->group_unfused;
     g.kb_per_seg = (int)(p->ka / BK);
@@ -398,12 +429,14 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MXA2A_OK : MXA2A_ERR_CUDA
 // (Re)allocate the split-K scratch for the plan's current splits (zeroed).
 int ensure_partials(mxa2a_plan* p) {
     const int S = std::max(p->S_fused, p->S_unfused);
-    if (S <= 1) return MXA2A_OK;
+    // partials of the tail split: one per tail item
+    const size_t tail_items = (size_t)std::max(p->W_fused - p->Wdp_fused, p->W_unfused - p->Wdp_unfused);
+    if (S <= 1 && tail_items == 0) return MXA2A_OK;
     // tile t of a path's Mt x Nt tiles holds S partials of BM x tile_n floats;
     // Nt * tile_n <= Ng2 * 128 for both tile widths
     const size_t tiles = (size_t)p->Mt * std::max(p->Nt_fused, p->Nt_unfused);
-    const size_t part = (size_t)p->Mt * S * BM * ((size_t)p->Ng2 * 128) * sizeof(float);
-    const size_t rdy = tiles * S * sizeof(unsigned long long);
+    const size_t part = std::max((size_t)p->Mt * S * BM * ((size_t)p->Ng2 * 128), tail_items * BM * BN) * sizeof(float);
+    const size_t rdy = std::max(tiles * S, tail_items) * sizeof(unsigned long long);
     const size_t need = part + rdy;
     if (need <= p->partial_bytes) return MXA2A_OK;
     if (p->split_ws) cudaFree(p->split_ws);
@@ -521,10 +554,16 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
             g.recv[j] = j == p->rs_rank ? nullptr : static_cast<const uint16_t*>(rs->recv[j]);
     }
     // Split partials are tagged with this run's launch index, which a graph
-    // replays unchanged: a split plan must not be captured.
+    // replays unchanged: a split plan must not be captured, and a captured
+    // run leaves its tail whole.
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return MXA2A_ERR_CUDA;
     if (cap != cudaStreamCaptureStatusNone && g.S > 1) return MXA2A_ERR_CAPTURE_SPLIT;
+    if (cap != cudaStreamCaptureStatusNone && g.S_tail > 1) {
+        g.W = g.W_dp + (g.W - g.W_dp) / g.S_tail;
+        g.W_dp = g.W;
+        g.S_tail = 1;
+    }
     // The B scale pack runs in the GEMM kernel's prologue (a cooperative
     // launch); the CTA-pair kernel (a cluster launch) keeps the separate kernel.
     g.B_scale = static_cast<const uint8_t*>(B_sf);
@@ -1051,6 +1090,10 @@ int mxa2a_set_option(mxa2a_plan* p, int key, int64_t v) {
             if (v < 0 || v > 1024) return MXA2A_ERR_INVALID_OPTION;
             p->group_fused_opt = (int)v;
             break;
+        case MXA2A_OPT_TAIL_SPLIT:
+            if (v != 0 && v != 1) return MXA2A_ERR_INVALID_OPTION;
+            p->tail_split = (int)v;
+            break;
         default:
             return MXA2A_ERR_INVALID_OPTION;
     }
@@ -1077,6 +1120,7 @@ int mxa2a_get_option(mxa2a_plan* p, int key, int64_t* v) {
         case MXA2A_OPT_STEP_CREDITS: *v = p->step_credits; break;
         case MXA2A_OPT_COPY_SKEW_NS: *v = p->copy_skew_ns; break;
         case MXA2A_OPT_GROUP_FUSED: *v = p->group_fused_opt; break;
+        case MXA2A_OPT_TAIL_SPLIT: *v = p->tail_split; break;
         case MXA2A_INFO_GROUP_FUSED: *v = p->group_fused; break;
         case MXA2A_INFO_GROUP_UNFUSED: *v = p->group_unfused; break;
         case MXA2A_INFO_CTA_PAIR: *v = p->pair_fused; break;
@@ -1087,6 +1131,8 @@ int mxa2a_get_option(mxa2a_plan* p, int key, int64_t* v) {
         case MXA2A_INFO_TILE_N_FUSED: *v = p->tn_fused; break;
         case MXA2A_INFO_TILE_N_UNFUSED: *v = p->tn_unfused; break;
         case MXA2A_INFO_KIND: *v = p->kind; break;
+        case MXA2A_INFO_TAIL_SPLIT: *v = p->St_fused; break;
+        case MXA2A_INFO_TAIL_SPLIT_UNFUSED: *v = p->St_unfused; break;
         case MXA2A_INFO_SPLITS: *v = p->S_fused; break;
         case MXA2A_INFO_ITEMS: *v = p->W_fused; break;
         case MXA2A_INFO_SPLITS_UNFUSED: *v = p->S_unfused; break;

@@ -114,8 +114,6 @@ struct __align__(8) SmemCtl {
     volatile uint32_t tx_own[kMaxStages];
     volatile uint32_t tx_odd[kMaxStages];
     volatile int consumed;   // stages whose full barrier the MMA thread has passed
-    volatile int epi_ok;     // epilogue broadcast: the other partials of the tile are ready
-    volatile int epi_warp_ok[kEpiWarps];
 };
 
 // Per kernel variant (CTA pair or not, tile width kBN): pipeline depth, stage
@@ -150,6 +148,8 @@ struct Lay {
 // ------------------------------------------------------------------ work items
 struct Item {
     int mt, nt, q, seg_lo, nseg, rot;
+    int S;      // K splits of this item's tile
+    int tail;   // the tile's place among the split tail's tiles, or -1
 };
 
 // Flattened work id -> (m row, n-tile, K split), where the m row is an m-tile
@@ -159,27 +159,54 @@ struct Item {
 // CTAs running at the same time share a few B tiles and a few A rows in
 // L2), with the n direction reversed on odd groups (zigzag) so a group starts
 // on the B tiles the previous one ended on.  On the fused path a group is
-// whole staging steps that fit in the ring together.  The K split is the
-// innermost index; each item may start its K loop at a rotated segment.
-__device__ __forceinline__ Item decode_item(const GemmParams& p, int w) {
+// whole staging steps that fit in the ring together.  The K split (S ways)
+// is the innermost index; each item may start its K loop at a rotated
+// segment.
+__device__ __forceinline__ Item decode_tile(const GemmParams& p, int w, int S) {
     Item it;
     const int rows = p.pair ? p.Mt / 2 : p.Mt;
-    const int per_group = p.group_m * p.Nt * p.S;
+    const int per_group = p.group_m * p.Nt * S;
     const int g = w / per_group;
     const int gm = min(p.group_m, rows - g * p.group_m);     // m rows in this group
     const int rem = w - g * per_group;
-    const int ntl = rem / (gm * p.S);
-    const int rem2 = rem - ntl * (gm * p.S);
-    it.mt = g * p.group_m + rem2 / p.S;
+    const int ntl = rem / (gm * S);
+    const int rem2 = rem - ntl * (gm * S);
+    it.mt = g * p.group_m + rem2 / S;
     // GEMM + ReduceScatter: start at the m-tile of this rank's first row
     if (p.rs_rows > 0 && !p.pair) it.mt = (it.mt + (p.rs_own * p.rs_rows) / BM) % p.Mt;
-    it.q = rem2 % p.S;
+    it.q = rem2 % S;
     it.nt = (p.zigzag && (g & 1)) ? (p.Nt - 1 - ntl) : ntl;
-    it.seg_lo = it.q * p.R / p.S;
-    const int seg_hi = (it.q + 1) * p.R / p.S;
+    it.seg_lo = it.q * p.R / S;
+    const int seg_hi = (it.q + 1) * p.R / S;
     it.nseg = seg_hi - it.seg_lo;
     it.rot = p.rotate ? (it.mt + it.nt) % it.nseg : 0;
+    it.S = S;
+    it.tail = -1;
     return it;
+}
+
+// Work id -> item.  Items before W_dp are whole tiles (or the uniform split's
+// parts).  With a tail split, the tiles from W_dp on in the same order -- the
+// ones the persistent grid's last, partly filled round would hold -- come as
+// S_tail consecutive items each, split q reading segments q*R/S_tail ..
+// (q+1)*R/S_tail - 1, so that the round's work spreads over more CTAs.
+__device__ __forceinline__ Item decode_item(const GemmParams& p, int w) {
+    if (w < p.W_dp || p.S_tail <= 1) return decode_tile(p, w, p.S);
+    const int t = (w - p.W_dp) / p.S_tail;
+    Item it = decode_tile(p, p.W_dp + t, 1);
+    it.S = p.S_tail;
+    it.tail = t;
+    it.q = (w - p.W_dp) - t * p.S_tail;
+    it.seg_lo = it.q * p.R / it.S;
+    it.nseg = (it.q + 1) * p.R / it.S - it.seg_lo;
+    it.rot = p.rotate ? (it.mt + it.nt) % it.nseg : 0;
+    return it;
+}
+
+// The slot of an item's tile among the split partials: the tile itself under
+// a uniform split, its place in the tail for a tail item.
+__device__ __forceinline__ size_t split_slot(const GemmParams& p, const Item& item, int mt) {
+    return item.tail >= 0 ? (size_t)item.tail : (size_t)mt * p.Nt + item.nt;
 }
 
 // The m-tile a CTA works on for an item.
@@ -322,6 +349,19 @@ __device__ __forceinline__ void named_barrier_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Named barrier that also ANDs a predicate over its threads: true for all of
+// them only if every thread passed true.
+__device__ __forceinline__ bool named_barrier_and(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.and.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // ------------------------------------------------------------------ roles
 template <bool kPair, int kBN>
 __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const CUtensorMap* tmb,
@@ -357,9 +397,9 @@ __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const
         const int b_row = item.nt * kBN + (kPair ? (int)rank * (kBN / 2) : 0);
         // One load per step first: when the copy role is ahead every segment
         // of the item's steps is already staged and the per-segment checks
-        // (a round trip to L2 each) are skipped.  Only without a K split: then
-        // every reader reads every segment, so no segment of the slot's next
-        // step can be published (and counted) before this item has read it.
+        // (a round trip to L2 each) are skipped.  Only for an item without a K
+        // split: it reads every segment, so no segment of the slot's next step
+        // can be published (and counted) before this item has read it.
         if (pid == 0) TRACE(4, w, 0);
         bool all_staged = !fused;
         if (fused && p.step_credits) {
@@ -379,7 +419,7 @@ __device__ void producer_role(const GemmParams& p, const CUtensorMap* tma, const
             }
             fence_proxy_async_global();
             all_staged = true;
-        } else if (fused && p.S == 1) {
+        } else if (fused && item.S == 1) {
             all_staged = true;
             int last_s = -1;
             for (int b = 0; b < nbox && all_staged; ++b) {
@@ -768,6 +808,8 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
     bool sf_ok = true;
     int sf_it = 0;      // next stage whose scales this warp writes
     int item_end = 0;   // stages of the items up to and including the current one
+    const bool together = p.S > 1 || p.S_tail > 1;   // the launch has split items
+    bool dead = false;                                // (then) this warp gave up on a whole-tile item
     int n = 0;   // items done; item n is in accumulator buffer n % kAccBufs
     for (int w = first_item<kPair>(); w < p.W; w += item_stride<kPair>(), ++n) {
         const Item item = decode_item(p, w);
@@ -775,7 +817,7 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
         const int buf = n % L::kAccBufs;
         const uint32_t acc_ph = (uint32_t)(n / L::kAccBufs) & 1u;
         item_end += item.nseg * p.kb_per_seg;
-        if (sf_warp && sf_ok) {
+        if (sf_warp && sf_ok && !dead) {
             int upto = item_end;
             if (w + item_stride<kPair>() < p.W) {
                 const Item nx = decode_item(p, w + item_stride<kPair>());
@@ -785,18 +827,18 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
         }
         // (a warp whose scale stores gave up leaves through the same path as a
         // warp whose wait ran out, so the split path's named barriers see it)
-        const bool got = sf_ok && wait_mbar_warp(p, ctl, &ctl->acc_full[buf], acc_ph, kRoleEpi, kPair);
-        if (p.S > 1) {
-            // the split path synchronises the 8 epilogue warps on a named barrier:
+        const bool got = !dead && sf_ok && wait_mbar_warp(p, ctl, &ctl->acc_full[buf], acc_ph, kRoleEpi, kPair);
+        if (item.S > 1) {
+            // the split path synchronises the 8 epilogue warps on named barriers:
             // leave only all together
-            if (lane == 0) ctl->epi_warp_ok[ep] = got ? 1 : 0;
-            named_barrier_sync(2, kEpiThreads);
-            bool all = true;
-#pragma unroll
-            for (int e = 0; e < kEpiWarps; ++e) all = all && ctl->epi_warp_ok[e] != 0;
-            if (!all) return;
+            if (!named_barrier_and(2, kEpiThreads, got)) return;
         } else if (!got) {
-            return;
+            // A warp gives up alone, except in a launch with split items: there it
+            // stays in the loop doing nothing, so that the next split item's vote
+            // (which it joins) makes all the warps leave together.
+            if (!together) return;
+            dead = true;
+            continue;
         }
         if (leader) TRACE(6, w, 0);
         tc_fence_after();
@@ -810,7 +852,7 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
         uint8_t* cbuf = sEpi + (size_t)ep * kEpiBufBytes;
         const int row_w = mt * BM + quarter * 32;       // first row of this warp's 32 (M % 64 == 0: all
                                                         // 32 rows are inside M or all past it)
-        if (p.S == 1) {
+        if (item.S == 1) {
             uint32_t packed[kBN / 4];
 #pragma unroll
             for (int c = 0; c < kChunks; ++c) {
@@ -888,8 +930,8 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
             // item's MMAs overlap) and publishes ready[tile][q].  Partial tile layout
             // [kBN/4][BM][4]: thread `lrow` of a warp stores the float4 of columns
             // 4g..4g+3 at (g*BM + lrow)*4, so each warp store covers 512 contiguous bytes.
-            const size_t tile = (size_t)mt * p.Nt + item.nt;
-            float* dst = p.partial + (tile * p.S + item.q) * (size_t)(BM * kBN) + ((size_t)(tcol / 4) * BM + lrow) * 4;
+            const size_t slot = split_slot(p, item, mt);
+            float* dst = p.partial + (slot * item.S + item.q) * (size_t)(BM * kBN) + ((size_t)(tcol / 4) * BM + lrow) * 4;
 #pragma unroll 1
             for (int c = 0; c < kChunks; ++c) {
                 uint32_t v[32];
@@ -906,7 +948,7 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
             __threadfence();
             named_barrier_sync(2, kEpiThreads);
             if (leader) {
-                asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p.ready + tile * p.S + item.q),
+                asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p.ready + slot * item.S + item.q),
                              "l"(p.launch_id)
                              : "memory");
                 TRACE(30, w, item.q);
@@ -925,30 +967,28 @@ __device__ void epilogue_role(const GemmParams& p, uint32_t tmem, SmemCtl* ctl, 
 // fixed order q = 0..S-1, the next split's loads in flight while the previous
 // one is added, and stores its BF16 32 x 32 box of C.  Every wait ends: the
 // K split is the innermost item index, so a tile's splits are consecutive
-// items, which the persistent grid runs in one round or two adjacent ones;
-// by induction over the rounds every CTA reaches and publishes each of its
-// items (all CTAs are resident).  False when the wait gave up.
+// items, and with no more splits than CTAs the persistent grid runs them on
+// different CTAs in one round or two adjacent ones; by induction over the
+// rounds every CTA reaches and publishes each of its items (all CTAs are
+// resident).  False when the wait gave up.
 template <int kBN>
 __device__ bool split_reduce(const GemmParams& p, SmemCtl* ctl, const CUtensorMap* tmc, uint8_t* cbuf, int ep,
                              int lane, const Item& item, int mt, int w) {
     const bool leader = (ep == 0 && lane == 0);
-    const size_t tile = (size_t)mt * p.Nt + item.nt;
+    const int S = item.S;
+    const size_t slot = split_slot(p, item, mt);
+    bool ok = true;
     if (leader) {
-        bool ok = true;
-        for (int q = 0; q < p.S && ok; ++q)
-            if (q != item.q) wait_value_u64(p, ctl, p.ready + tile * p.S + q, p.launch_id, &ok);
-        ctl->epi_ok = ok ? 1 : 0;
+        for (int q = 0; q < S && ok; ++q)
+            if (q != item.q) wait_value_u64(p, ctl, p.ready + slot * S + q, p.launch_id, &ok);
         TRACE(31, w, 0);
     }
-    named_barrier_sync(2, kEpiThreads);
-    const bool ok = ctl->epi_ok != 0;   // uniform over the epilogue warps
-    named_barrier_sync(2, kEpiThreads);   // (every warp has read it before the leader writes it again)
-    if (!ok) return false;
-    const float* part_tile = p.partial + tile * (size_t)p.S * (BM * kBN);
+    if (!named_barrier_and(2, kEpiThreads, ok)) return false;   // the leader's outcome, for all
+    const float* part_tile = p.partial + slot * (size_t)S * (BM * kBN);
     const int rows_tile = min(BM, p.M - mt * BM);
     const int units = ((rows_tile + 31) / 32) * (kBN / 32);
 #pragma unroll 1
-    for (int u = item.q + p.S * ep; u < units; u += p.S * kEpiWarps) {
+    for (int u = item.q + S * ep; u < units; u += S * kEpiWarps) {
         const int rg = u / (kBN / 32), cc = u - rg * (kBN / 32);
         const float* base = part_tile + ((size_t)(cc * 8) * BM + (size_t)(rg * 32 + lane)) * 4;
         float acc[32];
@@ -971,11 +1011,11 @@ __device__ bool split_reduce(const GemmParams& p, SmemCtl* ctl, const CUtensorMa
         };
         load(ta, 0);
 #pragma unroll 1
-        for (int q = 0; q < p.S; q += 2) {
-            if (q + 1 < p.S) load(tb, q + 1);
+        for (int q = 0; q < S; q += 2) {
+            if (q + 1 < S) load(tb, q + 1);
             add(ta);
-            if (q + 1 < p.S) {
-                if (q + 2 < p.S) load(ta, q + 2);
+            if (q + 1 < S) {
+                if (q + 2 < S) load(ta, q + 2);
                 add(tb);
             }
         }

@@ -172,6 +172,8 @@ extern "C" int mxa2a_run_noalloc(int R, int64_t M, int64_t kPerRank, int64_t N, 
     g.tile_n = BN;   // the wide tile: one accumulator, 4 pipeline stages
     g.S = 1;
     g.W = g.Mt * g.Nt;
+    g.W_dp = g.W;   // no tail split
+    g.S_tail = 1;
     g.kb_per_seg = (int)(kPerRank / BK);
     g.Mg = g.Mt;
     g.Ng2 = 2 * g.Nt;

@@ -44,6 +44,7 @@ MXA2A_OPT_ELEM_TYPES = 14
 MXA2A_OPT_STEP_CREDITS = 15
 MXA2A_OPT_COPY_SKEW_NS = 16
 MXA2A_OPT_GROUP_FUSED = 17
+MXA2A_OPT_TAIL_SPLIT = 18
 ELEM_TYPES = {("e4m3", "e4m3"): 0, ("e5m2", "e5m2"): 1, ("e4m3", "e5m2"): 2, ("e5m2", "e4m3"): 3}
 MXA2A_INFO_STEPS = 100
 MXA2A_INFO_MTILES = 101
@@ -65,6 +66,8 @@ MXA2A_INFO_GROUP_UNFUSED = 116
 MXA2A_INFO_TILE_N_FUSED = 117
 MXA2A_INFO_TILE_N_UNFUSED = 118
 MXA2A_INFO_KIND = 119
+MXA2A_INFO_TAIL_SPLIT = 120
+MXA2A_INFO_TAIL_SPLIT_UNFUSED = 121
 
 MXA2A_KIND_ALLTOALL = 0
 MXA2A_KIND_ALLGATHER = 1

@@ -441,7 +441,9 @@ def time_config(dev, timed, w, steps, warmup):
             raise RuntimeError(f"device status after timing {w.name}: {st}")
         info = {"splits": plan.get_option(mxa2a.MXA2A_INFO_SPLITS),
                 "cta_pair": plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR),
-                "cta_pair_unfused": plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED)}
+                "cta_pair_unfused": plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED),
+                "tail_split": plan.get_option(mxa2a.MXA2A_INFO_TAIL_SPLIT),
+                "tail_split_unfused": plan.get_option(mxa2a.MXA2A_INFO_TAIL_SPLIT_UNFUSED)}
     return summarize_config(w, fused, kern, unfused, steps, info)
 
 
@@ -622,7 +624,9 @@ def run_ours(args, w):
             if wc.name == w.name:
                 info = {"splits": plan.get_option(mxa2a.MXA2A_INFO_SPLITS),
                         "cta_pair": plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR),
-                        "cta_pair_unfused": plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED)}
+                        "cta_pair_unfused": plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED),
+                        "tail_split": plan.get_option(mxa2a.MXA2A_INFO_TAIL_SPLIT),
+                        "tail_split_unfused": plan.get_option(mxa2a.MXA2A_INFO_TAIL_SPLIT_UNFUSED)}
                 configs[wc.name] = summarize_config(wc, fused_ms, kern_ms if args.path == "fused" else [],
                                                     unfused_ms, args.steps, info)
             else:
@@ -680,6 +684,8 @@ def run_ours(args, w):
                    "commMSize": w.commMSize, "buffer_num": w.buffer_num, "seed": w.seed,
                    "path": args.path, "parallelism": "replicas" if ws > 1 else "single",
                    "splits": plan.get_option(mxa2a.MXA2A_INFO_SPLITS),
+                   "tail_split": plan.get_option(mxa2a.MXA2A_INFO_TAIL_SPLIT if args.path == "fused"
+                                                 else mxa2a.MXA2A_INFO_TAIL_SPLIT_UNFUSED),
                    "cta_pair": plan.get_option(mxa2a.MXA2A_INFO_CTA_PAIR if args.path == "fused"
                                                else mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED),
                    "grid": plan.get_option(mxa2a.MXA2A_INFO_GRID_FUSED if args.path == "fused"

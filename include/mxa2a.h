@@ -371,6 +371,14 @@ enum mxa2a_option {
                                       ring's rows (buffer_num * commMSize); ignored when commMSize is
                                       not a multiple of 128 or with the CTA-pair kernel (the planner's
                                       choice: MXA2A_INFO_GROUP_FUSED) */
+    MXA2A_OPT_TAIL_SPLIT = 18,     /* 1 (default): when a path's tiles fill the persistent grid more
+                                      than once and the last round holds at most half the grid's
+                                      worth, split that round's tiles in two along K (R even, K >=
+                                      8192; each half reads R / 2 segments, the sums done by the kernel
+                                      as with MXA2A_OPT_SPLIT_K) so that twice as many CTAs share it;
+                                      0: whole tiles.  Only the single-CTA kernel without a uniform
+                                      split; a run under CUDA-graph capture leaves its tail whole
+                                      (MXA2A_INFO_TAIL_SPLIT) */
     /* read-only plan facts (mxa2a_get_option only) */
     MXA2A_INFO_STEPS = 100,        /* M / commMSize */
     MXA2A_INFO_MTILES = 101,
@@ -391,7 +399,9 @@ enum mxa2a_option {
     MXA2A_INFO_GROUP_UNFUSED = 116, /* raster group of the unfused path (m rows) */
     MXA2A_INFO_TILE_N_FUSED = 117,  /* tile width of the fused path (128 or 256) */
     MXA2A_INFO_TILE_N_UNFUSED = 118, /* tile width of the unfused path (128 or 256) */
-    MXA2A_INFO_KIND = 119          /* enum mxa2a_kind */
+    MXA2A_INFO_KIND = 119,         /* enum mxa2a_kind */
+    MXA2A_INFO_TAIL_SPLIT = 120,   /* K split of the fused path's last-round tiles (1: none) */
+    MXA2A_INFO_TAIL_SPLIT_UNFUSED = 121 /* the same for the unfused path */
 };
 
 /* Set a tunable (MXA2A_OPT_*) or read it back, or read a plan fact
@@ -452,7 +462,8 @@ int mxa2a_l2_flush(void *device_buf, size_t bytes, void *stream);
  * Same shape rules, data layouts and result as mxa2a_run with E4M3 x E4M3
  * operands (the element-type option of a plan does not exist here), run on
  * the single-CTA kernel with no K split: the result bits equal those of
- * mxa2a_run of a plan with MXA2A_OPT_SPLIT_K = 1 and MXA2A_OPT_CTA_PAIR = 0.
+ * mxa2a_run of a plan with MXA2A_OPT_SPLIT_K = 1, MXA2A_OPT_CTA_PAIR = 0
+ * and MXA2A_OPT_TAIL_SPLIT = 0.
  * It allocates nothing: the staging ring, scale tiles, credit
  * counters and status block live in one static device array of 16 MiB that
  * every GPU which loads this library holds until the process exits.  A shape

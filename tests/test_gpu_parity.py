@@ -247,7 +247,7 @@ def test_narrow_tiles_match_wide(case):
     outs = {}
     for tile in (128, 256):
         # grid 2: each CTA runs several items, so both accumulators are reused
-        with _plan(w, tile_n=tile, split_k=1, grid=2) as p:
+        with _plan(w, tile_n=tile, split_k=1, grid=2, tail_split=0) as p:
             assert p.get_option(mxa2a.MXA2A_INFO_TILE_N_FUSED) == tile
             assert p.get_option(mxa2a.MXA2A_INFO_TILE_N_UNFUSED) == tile
             for fused in (True, False):
@@ -373,6 +373,43 @@ def test_split_k_tiles_straddling_grid_rounds(fused):
     _check_full(w, fused=fused, split_k=3, grid=4)
 
 
+@pytest.mark.parametrize("fused", [True, False])
+def test_tail_split_last_round(fused):
+    """8 tiles (K = 8192) on a grid of 6 CTAs: the second round would hold 2
+    whole tiles, so the planner splits those two along K (each half reading 1
+    of the 2 segments) and 4 CTAs share them.  The tail's tiles are ragged (64
+    of their rows past M, one of them with columns past N), checked against
+    the oracle, against the same plan with whole tiles, and for identical bits
+    over repeated runs; nothing is written past M x N."""
+    w = inputs.Workload("tail", 2, 448, 4096, 400, 64, 4, 67)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    ref = gu.oracle_full(x)
+    info = mxa2a.MXA2A_INFO_TAIL_SPLIT if fused else mxa2a.MXA2A_INFO_TAIL_SPLIT_UNFUSED
+    got = {}
+    for tail in (1, 0):
+        with _plan(w, grid=6, tail_split=tail, split_k=1) as p:
+            assert p.get_option(mxa2a.MXA2A_OPT_TAIL_SPLIT) == tail
+            assert p.get_option(info) == (2 if tail else 1)
+            if fused:
+                assert p.get_option(mxa2a.MXA2A_INFO_ITEMS) == (6 + 2 * 2 if tail else 8)
+            fn = p.run if fused else p.run_unfused
+            bufs = []
+            for _ in range(3):
+                buf = torch.full((w.M * w.N + 4096,), -1, dtype=torch.int16, device="cuda")
+                fn(d["A_seg"], d["A_scale_seg"], d["B"], d["B_scale"], buf[: w.M * w.N].view(w.M, w.N))
+                bufs.append(buf)
+            torch.cuda.synchronize()
+            _status_ok(p)
+        for buf in bufs:
+            assert bool((buf[w.M * w.N:] == -1).all())
+        bits = [gu.host_bits(b[: w.M * w.N].view(w.M, w.N)) for b in bufs]
+        for b in bits[1:]:
+            assert np.array_equal(bits[0], b)
+        got[tail] = bits[0]
+        gu.assert_parity(got[tail], ref, f"tail split {tail} fused={fused}")
+
+
 def test_split_k_deterministic_over_runs():
     """The split partials are summed in a fixed order whichever split finishes
     last, so repeated runs give identical bits."""
@@ -463,6 +500,34 @@ def test_cuda_graph_replay_matches_eager(fused):
             assert np.array_equal(gu.host_bits(C), eager)
         _status_ok(p)
     gu.assert_parity(eager, gu.oracle_full(x), f"graph fused={fused}")
+
+
+def test_cuda_graph_capture_leaves_the_tail_whole():
+    """A plan with a tail split can be captured: the captured run takes its
+    last round's tiles whole (split partials are tagged with the launch index,
+    which a replay repeats), so every replay gives the bits of an eager run
+    without the tail split."""
+    w = inputs.Workload("graphtail", 2, 448, 4096, 400, 64, 4, 71)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w, grid=6, tail_split=0, split_k=1) as p:
+        whole = gu.host_bits(gu.run_gpu(p, d, w.M, w.N))
+        torch.cuda.synchronize()
+    with _plan(w, grid=6, split_k=1) as p:
+        assert p.get_option(mxa2a.MXA2A_INFO_TAIL_SPLIT) == 2
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        C = torch.full((w.M, w.N), -1, dtype=torch.int16, device="cuda")
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            p.run(d["A_seg"], d["A_scale_seg"], d["B"], d["B_scale"], C, side)
+        for _ in range(3):
+            C.fill_(-1)
+            g.replay()
+            torch.cuda.synchronize()
+            assert np.array_equal(gu.host_bits(C), whole)
+        _status_ok(p)
+    gu.assert_parity(whole, gu.oracle_full(x), "graph tail")
 
 
 def test_cuda_graph_capture_refuses_split():
@@ -684,6 +749,9 @@ def test_full_size_workloads_sampled(idx):
     x = inputs.make_inputs(w)
     d = gu.to_device(x)
     rows = gu.sample_rows(w.M, 40 if w.M > 64 else w.M, seed=idx)
+    if w.M >= 1024:
+        # the last m-tiles hold the tiles of the grid's last round (split in K on both paths)
+        rows = np.unique(np.concatenate([rows, [w.M - 700, w.M - 200, w.M - 65, w.M - 1]]))
     with _plan(w, timeout_ns=2_000_000_000) as p:
         Cf = gu.run_gpu(p, d, w.M, w.N, fused=True)
         Cu = gu.run_gpu(p, d, w.M, w.N, fused=False)
@@ -692,11 +760,22 @@ def test_full_size_workloads_sampled(idx):
         got_f = gu.host_bits(Cf)
         got_u = gu.host_bits(Cu)
         same_split = p.get_option(mxa2a.MXA2A_INFO_SPLITS) == p.get_option(mxa2a.MXA2A_INFO_SPLITS_UNFUSED)
+        whole_f, whole_u = got_f, got_u
+        if (p.get_option(mxa2a.MXA2A_INFO_TAIL_SPLIT), p.get_option(mxa2a.MXA2A_INFO_TAIL_SPLIT_UNFUSED)) != (1, 1):
+            # the paths' last rounds hold different tiles (their raster orders differ):
+            # compare the two paths bit for bit with whole tiles
+            p.set_option(mxa2a.MXA2A_OPT_TAIL_SPLIT, 0)
+            whole_f = gu.host_bits(gu.run_gpu(p, d, w.M, w.N, fused=True))
+            whole_u = gu.host_bits(gu.run_gpu(p, d, w.M, w.N, fused=False))
+            torch.cuda.synchronize()
+            _status_ok(p)
     ref = oracle.gemm(x["A_seg"], x["A_scale_seg"], x["B"], x["B_scale"], rows=rows)
     gu.assert_parity(got_f[rows], ref, f"{w.name} fused sampled {len(rows)} rows")
     gu.assert_parity(got_u[rows], ref, f"{w.name} unfused sampled {len(rows)} rows")
+    if whole_f is not got_f:
+        gu.assert_parity(whole_f[rows], ref, f"{w.name} fused, whole tiles, sampled {len(rows)} rows")
     if same_split:
-        assert np.array_equal(got_f, got_u), "fused and unfused differ"
+        assert np.array_equal(whole_f, whole_u), "fused and unfused differ"
     # every output written (no NaN left from the 0xFFFF fill), magnitudes sane
     assert not np.isnan(gu.bits_to_f64(got_f)).any()
 

@@ -101,11 +101,20 @@ def test_allgather_full_size_sampled():
     with _ag_plan(w) as p:
         got_f = _ag_run(p, dev, w.M, w.N, "fused")
         got_u = _ag_run(p, dev, w.M, w.N, "unfused")
+        # 256 tiles on the persistent grid: the last round's tiles are split in K,
+        # and the two paths' raster orders put different tiles there, so the
+        # paths are compared bit for bit with whole tiles
+        tails = (p.get_option(mxa2a.MXA2A_INFO_TAIL_SPLIT), p.get_option(mxa2a.MXA2A_INFO_TAIL_SPLIT_UNFUSED))
+        p.set_option(mxa2a.MXA2A_OPT_TAIL_SPLIT, 0)
+        whole_f = _ag_run(p, dev, w.M, w.N, "fused")
+        whole_u = _ag_run(p, dev, w.M, w.N, "unfused")
     rows = gu.sample_rows(w.M, 24, 3)
-    rows = np.unique(np.concatenate([rows, [w.rowsPerRank - 1, w.rowsPerRank, 3 * w.rowsPerRank]]))
+    rows = np.unique(np.concatenate([rows, [w.rowsPerRank - 1, w.rowsPerRank, 3 * w.rowsPerRank, w.M - 1]]))
     ref = oracle.gemm_allgather(x["A_blk"], x["A_scale_blk"], x["B"], x["B_scale"], rows=rows)
-    gu.assert_parity(got_f[rows], ref, "allgather full size")
-    assert np.array_equal(got_f, got_u)
+    gu.assert_parity(got_f[rows], ref, f"allgather full size, tail split {tails}")
+    gu.assert_parity(got_u[rows], ref, f"allgather full size unfused, tail split {tails}")
+    gu.assert_parity(whole_f[rows], ref, "allgather full size, whole tiles")
+    assert np.array_equal(whole_f, whole_u)
 
 
 def test_allgather_host_entry_and_new_block_pointers():

@@ -39,11 +39,12 @@ def test_noalloc_rejects_problems_larger_than_its_scratch():
 
 def _reference_with_plan(w, d):
     """mxa2a_run of a plan on the entry point's kernel: the single-CTA kernel,
-    K loop not split."""
+    K loop not split (the last round's tiles neither)."""
     C = torch.full((w.M, w.N), -1, dtype=torch.int16, device="cuda")
     with mxa2a.Plan(w.R, w.M, w.kPerRank, w.N, w.commMSize, w.buffer_num) as p:
         p.set_option(mxa2a.MXA2A_OPT_SPLIT_K, 1)
         p.set_option(mxa2a.MXA2A_OPT_CTA_PAIR, 0)
+        p.set_option(mxa2a.MXA2A_OPT_TAIL_SPLIT, 0)
         p.run(d["A_seg"], d["A_scale_seg"], d["B"], d["B_scale"], C)
         torch.cuda.synchronize()
         assert p.status()["code"] == 0
