@@ -21,15 +21,17 @@ def _lib():
     torch.cuda.init()
 
 
-@pytest.mark.parametrize("split", [1, 2])
-def test_lost_staging_signal_times_out_then_recovers(split):
+@pytest.mark.parametrize("split,skip", [(1, 3), (2, 3), (1, 0)])
+def test_lost_staging_signal_times_out_then_recovers(split, skip):
+    """skip 3: a step in the middle never comes; skip 0: the first one, so
+    every producer gives up before its first load."""
     w = inputs.Workload("fault", 2, 512, 256, 512, 64, 2, 53)
     x = inputs.make_inputs(w)
     d = gu.to_device(x)
     with mxa2a.Plan(w.R, w.M, w.kPerRank, w.N, w.commMSize, w.buffer_num) as p:
         p.set_option(mxa2a.MXA2A_OPT_TIMEOUT_NS, 100_000_000)      # 0.1 s per wait
         p.set_option(mxa2a.MXA2A_OPT_SPLIT_K, split)
-        p.set_option(mxa2a.MXA2A_OPT_FAULT_SKIP_STEP, 3)
+        p.set_option(mxa2a.MXA2A_OPT_FAULT_SKIP_STEP, skip)
         gu.run_gpu(p, d, w.M, w.N)
         torch.cuda.synchronize()                                      # returns: every wait is bounded
         st = p.status()
@@ -42,7 +44,7 @@ def test_lost_staging_signal_times_out_then_recovers(split):
         torch.cuda.synchronize()
         assert p.status()["code"] == 0
         got = gu.host_bits(C)
-    gu.assert_parity(got, gu.oracle_full(x), f"after recovery split={split}")
+    gu.assert_parity(got, gu.oracle_full(x), f"after recovery split={split} skip={skip}")
 
 
 def test_status_is_clean_after_normal_runs():
