@@ -628,6 +628,26 @@ def test_host_entry_pinned_output_with_split_k():
     gu.assert_parity(ref, gu.oracle_full(x), "hostsplit")
 
 
+def test_host_entry_pinned_output_with_tail_split():
+    """The tail split's sums write a pinned C through its device view: the
+    same bits as the device run (whose tail is split too), nothing past M x N."""
+    w = inputs.Workload("hosttail", 2, 448, 4096, 400, 64, 4, 107)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w, grid=6, split_k=1) as p:
+        assert p.get_option(mxa2a.MXA2A_INFO_TAIL_SPLIT) == 2
+        ref = gu.host_bits(gu.run_gpu(p, d, w.M, w.N))
+        hA = [a.pin_memory() for a in x["A_seg"]]
+        hS = [a.pin_memory() for a in x["A_scale_seg"]]
+        guard = torch.full((w.M + 1, w.N), -1, dtype=torch.int16).pin_memory()
+        p.run_host(hA, hS, x["B"].pin_memory(), x["B_scale"].pin_memory(), guard[: w.M])
+        torch.cuda.synchronize()
+        _status_ok(p)
+    assert np.array_equal(guard[: w.M].numpy().view(np.uint16), ref)
+    assert bool((guard[w.M] == -1).all())
+    gu.assert_parity(ref, gu.oracle_full(x), "hosttail")
+
+
 @pytest.mark.parametrize("split", [1, 4])
 def test_host_entry_pinned_output_rows_and_columns_past_the_ends(split):
     """M = 64 (half a tile) and N = 400 (a ragged last tile): the epilogue's
