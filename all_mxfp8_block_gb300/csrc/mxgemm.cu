@@ -994,29 +994,18 @@ __device__ bool split_reduce(const GemmParams& p, SmemCtl* ctl, const CUtensorMa
         float acc[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
-        uint4 ta[8], tb[8];
-        auto load = [&](uint4 (&t)[8], int q) {
+#pragma unroll 1
+        for (int q = 0; q < S; ++q) {
             const float* src = base + (size_t)q * (BM * kBN);
+            uint4 t[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) t[j] = ld_cg_v4(src + (size_t)j * BM * 4);
-        };
-        auto add = [&](const uint4 (&t)[8]) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 acc[4 * j] += __uint_as_float(t[j].x);
                 acc[4 * j + 1] += __uint_as_float(t[j].y);
                 acc[4 * j + 2] += __uint_as_float(t[j].z);
                 acc[4 * j + 3] += __uint_as_float(t[j].w);
-            }
-        };
-        load(ta, 0);
-#pragma unroll 1
-        for (int q = 0; q < S; q += 2) {
-            if (q + 1 < S) load(tb, q + 1);
-            add(ta);
-            if (q + 1 < S) {
-                if (q + 2 < S) load(ta, q + 2);
-                add(tb);
             }
         }
         uint32_t wds[16];

@@ -13,6 +13,8 @@ follows a 2048-row one, so the scale tiles of its rows past M are stale in the
 shared array unless the entry point clears them.  It also checks that the
 calls allocate nothing on the device.  This file is collected last on purpose.
 """
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -72,6 +74,8 @@ def test_noalloc_matches_plan_entry_on_calls_in_a_row():
 
     # the first call on the device looks up the scratch array's address (once)
     call(2)
+    torch.cuda.synchronize()
+    gc.collect()   # (earlier tests' tensors are freed now, not during the calls)
     torch.cuda.synchronize()
     free_before, _ = torch.cuda.mem_get_info()
     torch_before = torch.cuda.memory_allocated()
