@@ -304,9 +304,9 @@ void derive(mxa2a_plan* p) {
     } else {
         p->grid_unfused = std::max(1, std::min(cap, p->W_unfused));
     }
-    // Tail split (single-CTA kernel, no uniform split): when the tiles fill
-    // the persistent grid more than once, the last round holds rem = W % grid
-    // of them and leaves the other CTAs idle.  If rem is at most half the grid,
+    // Tail split (no uniform split): when the tiles fill the persistent grid
+    // (its CTAs, or CTA pairs) more than once, the last round holds rem of them
+    // and leaves the others idle.  If rem is at most half the grid,
     // those tiles are split in two along K (R even, each half reading R / 2
     // segments), so that the last round takes half a tile.  A split costs a
     // fixed epilogue: measured on GB300 (8192^3, traced) about 3.6 us to write
@@ -317,9 +317,10 @@ void derive(mxa2a_plan* p) {
     auto tail = [&](int& W, int S, int grid, bool pair, int& Wdp, int& St) {
         Wdp = W;
         St = 1;
-        if (!p->tail_split || pair || S != 1 || W <= grid || p->R % 2 != 0 || p->K < 8192) return;
-        const int rem = W % grid;
-        if (rem == 0 || 2 * rem > grid) return;
+        const int units = pair ? grid / 2 : grid;   // CTAs, or CTA pairs, that take items
+        if (!p->tail_split || S != 1 || W <= units || p->R % 2 != 0 || p->K < 8192) return;
+        const int rem = W % units;
+        if (rem == 0 || 2 * rem > units) return;
         St = 2;
         Wdp = W - rem;
         W = Wdp + rem * St;
@@ -429,8 +430,8 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MXA2A_OK : MXA2A_ERR_CUDA
 // (Re)allocate the split-K scratch for the plan's current splits (zeroed).
 int ensure_partials(mxa2a_plan* p) {
     const int S = std::max(p->S_fused, p->S_unfused);
-    // partials of the tail split: one per tail item
-    const size_t tail_items = (size_t)std::max(p->W_fused - p->Wdp_fused, p->W_unfused - p->Wdp_unfused);
+    // partials of the tail split: one per tail item and CTA (two CTAs per item in a pair)
+    const size_t tail_items = 2 * (size_t)std::max(p->W_fused - p->Wdp_fused, p->W_unfused - p->Wdp_unfused);
     if (S <= 1 && tail_items == 0) return MXA2A_OK;
     // tile t of a path's Mt x Nt tiles holds S partials of BM x tile_n floats;
     // Nt * tile_n <= Ng2 * 128 for both tile widths

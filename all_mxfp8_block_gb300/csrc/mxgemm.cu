@@ -203,10 +203,12 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int w) {
     return it;
 }
 
-// The slot of an item's tile among the split partials: the tile itself under
-// a uniform split, its place in the tail for a tail item.
+// The slot of a CTA's tile among the split partials: the tile itself under a
+// uniform split, its place in the tail for a tail item (in a CTA pair, two
+// slots per tail tile, one per CTA's m-tile).
 __device__ __forceinline__ size_t split_slot(const GemmParams& p, const Item& item, int mt) {
-    return item.tail >= 0 ? (size_t)item.tail : (size_t)mt * p.Nt + item.nt;
+    if (item.tail < 0) return (size_t)mt * p.Nt + item.nt;
+    return p.pair ? 2 * (size_t)item.tail + (size_t)(mt - 2 * item.mt) : (size_t)item.tail;
 }
 
 // The m-tile a CTA works on for an item.

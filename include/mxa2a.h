@@ -371,14 +371,13 @@ enum mxa2a_option {
                                       ring's rows (buffer_num * commMSize); ignored when commMSize is
                                       not a multiple of 128 or with the CTA-pair kernel (the planner's
                                       choice: MXA2A_INFO_GROUP_FUSED) */
-    MXA2A_OPT_TAIL_SPLIT = 18,     /* 1 (default): when a path's tiles fill the persistent grid more
-                                      than once and the last round holds at most half the grid's
-                                      worth, split that round's tiles in two along K (R even, K >=
-                                      8192; each half reads R / 2 segments, the sums done by the kernel
-                                      as with MXA2A_OPT_SPLIT_K) so that twice as many CTAs share it;
-                                      0: whole tiles.  Only the single-CTA kernel without a uniform
-                                      split; a run under CUDA-graph capture leaves its tail whole
-                                      (MXA2A_INFO_TAIL_SPLIT) */
+    MXA2A_OPT_TAIL_SPLIT = 18,     /* 1 (default): when a path's tiles fill the persistent grid (its CTAs,
+                                      or CTA pairs) more than once and the last round holds at most half
+                                      the grid's worth, split that round's tiles in two along K (R even,
+                                      K >= 8192; each half reads R / 2 segments, the sums done by the
+                                      kernel as with MXA2A_OPT_SPLIT_K) so that twice as many CTAs share
+                                      it; 0: whole tiles.  Only without a uniform split; a run under
+                                      CUDA-graph capture leaves its tail whole (MXA2A_INFO_TAIL_SPLIT) */
     /* read-only plan facts (mxa2a_get_option only) */
     MXA2A_INFO_STEPS = 100,        /* M / commMSize */
     MXA2A_INFO_MTILES = 101,

@@ -433,6 +433,28 @@ def test_automatic_split_small_m():
 
 
 @pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("split,tail", [(2, 0), (1, 1)])
+def test_cta_pair_split_items(fused, split, tail):
+    """The CTA-pair kernel's split items, each CTA of a pair writing and
+    summing its own m-tile's partials: a uniform split in two (8 items on 3
+    pairs), and the tail split (4 pair tiles on 3 pairs: the fourth split in
+    two, a slot per CTA); against the oracle, identical bits over runs."""
+    w = inputs.Workload("pairsplit", 2, 512, 4096, 400, 64, 4, 73)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w, cta_pair=1, split_k=split, grid=6, tail_split=tail) as p:
+        assert p.get_option(mxa2a.MXA2A_INFO_CTA_PAIR if fused else mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED) == 1
+        assert p.get_option(mxa2a.MXA2A_INFO_SPLITS if fused else mxa2a.MXA2A_INFO_SPLITS_UNFUSED) == split
+        assert p.get_option(mxa2a.MXA2A_INFO_TAIL_SPLIT if fused else mxa2a.MXA2A_INFO_TAIL_SPLIT_UNFUSED) == \
+            (2 if tail else 1)
+        outs = [gu.host_bits(gu.run_gpu(p, d, w.M, w.N, fused=fused)) for _ in range(2)]
+        torch.cuda.synchronize()
+        _status_ok(p)
+    assert np.array_equal(outs[0], outs[1])
+    gu.assert_parity(outs[0], gu.oracle_full(x), f"pair split={split} tail={tail} fused={fused}")
+
+
+@pytest.mark.parametrize("fused", [True, False])
 def test_cta_pair_kernel_against_single_cta_kernel(fused):
     """The CTA-pair kernel (256-row tiles, .cta_group::2 MMAs issued by the even
     CTA) and the single-CTA kernel agree with the oracle and with each other."""
