@@ -122,7 +122,7 @@ struct mxa2a_plan {
     int group_fused = 1, group_unfused = 1; // raster group, in m rows (tiles or tile pairs)
     int group_cap = 16;                     // option: largest unfused raster group
     int group_fused_opt = 0;                // option: fused raster group in m-tiles (0 = one)
-    int allow_pair = 0;           // option: 1 allows the CTA-pair kernel
+    int allow_pair = 2;           // option: 0 never, 1 both paths, 2 automatic (the CTA-pair kernel)
     int max_pairs_fused = 0, max_pairs_unfused = 0;
     int rows_per_chunk = 1, chunks_per_seg = 1, n_copy_tasks = 0;
     int grid_fused = 0, grid_unfused = 0;
@@ -219,9 +219,23 @@ void derive(mxa2a_plan* p) {
     // needs an even number of 128-row tiles and clusters of two resident CTAs.
     // Both halves of a pair tile are consumed in lock step, so the fused path
     // also needs every staging step of a 256-row tile resident in the ring.
-    const bool pair_ok = p->allow_pair && p->Mt % 2 == 0;
-    p->pair_unfused = (pair_ok && p->max_pairs_unfused > 0) ? 1 : 0;
-    p->pair_fused = (pair_ok && p->max_pairs_fused > 0 && p->bn >= tile_span(p->M, p->cm, 2 * BM)) ? 1 : 0;
+    // Automatic: the fused path on pairs when the staging window holds at least
+    // two pair tiles per pair of SMs, the unfused path on single CTAs.
+    // Measured on GB300 (fused, with the tail split): 8192^3 442 -> 430 us on
+    // pairs (its window holds 256 pair tiles); the 2048 x 4096 x 4096 and
+    // 4096 x 7168 x 2048 problems (32 and 64 pair tiles in the window) 66 -> 75
+    // and 82 -> 92 us; unfused 8192^3 410 -> 424 us.
+    const bool pair_ok = p->allow_pair != 0 && p->Mt % 2 == 0;
+    const int64_t window_pair_tiles = (int64_t)(window_mtiles / 2) * ((p->N + BN - 1) / BN);
+    const bool pair_fused_fits = pair_ok && p->max_pairs_fused > 0 && p->bn >= tile_span(p->M, p->cm, 2 * BM);
+    p->pair_unfused = (pair_ok && p->allow_pair == 1 && p->max_pairs_unfused > 0) ? 1 : 0;
+    // (a requested 128-column tile keeps single CTAs: pair tiles are 256 wide)
+    p->pair_fused = (pair_fused_fits &&
+                     (p->allow_pair == 1 ||
+                      (p->tile_opt != BN_NARROW &&
+                       window_pair_tiles >= 2 * (int64_t)std::min(cta_cap / 2, p->max_pairs_fused))))
+                        ? 1
+                        : 0;
     // Tile width.  The narrow 128-column tile gives twice the work items for
     // the same rows in flight (the fused path can only work on the rows in the
     // staging ring) and double-buffers the TMEM accumulator, at 1.33x the
@@ -565,10 +579,13 @@ int run_impl(mxa2a_plan* p, const void* const* A_seg, const void* const* A_sf, c
         g.W_dp = g.W;
         g.S_tail = 1;
     }
-    // The B scale pack runs in the GEMM kernel's prologue (a cooperative
-    // launch); the CTA-pair kernel (a cluster launch) keeps the separate kernel.
+    // The B scale pack runs in the GEMM kernel's prologue, whose producers then
+    // wait for every CTA's slice: a cooperative launch guarantees that they are
+    // all resident.  The fused CTA-pair kernel (a cluster launch) already relies
+    // on that for its staging credits (its grid never exceeds the pairs that fit
+    // at once) and packs inline too; the unfused one keeps the separate kernel.
     g.B_scale = static_cast<const uint8_t*>(B_sf);
-    g.sfb_inline = g.pair ? 0 : 1;
+    g.sfb_inline = (!g.pair || fused) ? 1 : 0;
     if (!g.sfb_inline) {
         if ((rc = cuda_rc(launch_pack_sfb(static_cast<const uint8_t*>(B_sf), (int)p->N, (int)p->K, p->Ng2, p->sfb,
                                           stream))))
@@ -1064,7 +1081,7 @@ int mxa2a_set_option(mxa2a_plan* p, int key, int64_t v) {
             p->chunk_bytes = v;
             break;
         case MXA2A_OPT_CTA_PAIR:
-            if (v != 0 && v != 1) return MXA2A_ERR_INVALID_OPTION;
+            if (v < 0 || v > 2) return MXA2A_ERR_INVALID_OPTION;
             p->allow_pair = (int)v;
             break;
         case MXA2A_OPT_GROUP_M:

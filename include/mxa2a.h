@@ -344,10 +344,15 @@ enum mxa2a_option {
     MXA2A_OPT_GRID = 8,            /* cap on persistent CTAs (0 = one per SM) */
     MXA2A_OPT_CHUNK_BYTES = 9,     /* target staging copy chunk in bytes; 0 (default): automatic,
                                       about two staging steps' tasks for all copy workers, 4..16 KiB */
-    MXA2A_OPT_CTA_PAIR = 10,       /* 1: use the CTA-pair kernel (256-row tiles, one tcgen05
-                                      cta_group::2 MMA stream per pair) when M/128 is even and, on the
-                                      fused path, buffer_num covers the steps of a 256-row tile;
-                                      0 (default): the single-CTA kernel */
+    MXA2A_OPT_CTA_PAIR = 10,       /* the CTA-pair kernel (256-row tiles, one tcgen05 cta_group::2 MMA
+                                      stream per pair), usable when M/128 is even and, on the fused
+                                      path, buffer_num covers the steps of a 256-row tile.  2 (default):
+                                      the fused path on pairs when its staging window
+                                      (buffer_num * commMSize rows) holds at least two pair tiles per
+                                      resident pair and no 128-column tile is asked for (MXA2A_OPT_TILE_N),
+                                      the unfused path on single CTAs; 1: both paths on
+                                      pairs wherever usable; 0: the single-CTA kernel
+                                      (MXA2A_INFO_CTA_PAIR / _UNFUSED give the choice) */
     MXA2A_OPT_GROUP_M = 11,        /* largest raster group of the unfused path, in m rows
                                       (128-row tiles, or tile pairs), default 16 (the fused path's
                                       group: MXA2A_OPT_GROUP_FUSED) */

@@ -650,6 +650,41 @@ def test_host_entry_pinned_output_with_split_k():
     gu.assert_parity(ref, gu.oracle_full(x), "hostsplit")
 
 
+@pytest.mark.parametrize("tail", [0, 1])
+def test_host_entry_pinned_output_cta_pair(tail):
+    """The CTA-pair kernel's epilogue writes a pinned C through its device view
+    (each CTA of a pair its own rows; with the tail split, the sums too): the
+    device run's bits, nothing past M x N."""
+    w = inputs.Workload("hostpair", 2, 512, 4096, 400, 64, 4, 109)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w, cta_pair=1, grid=6, split_k=1, tail_split=tail) as p:
+        assert p.get_option(mxa2a.MXA2A_INFO_CTA_PAIR) == 1
+        ref = gu.host_bits(gu.run_gpu(p, d, w.M, w.N))
+        hA = [a.pin_memory() for a in x["A_seg"]]
+        hS = [a.pin_memory() for a in x["A_scale_seg"]]
+        guard = torch.full((w.M + 1, w.N), -1, dtype=torch.int16).pin_memory()
+        p.run_host(hA, hS, x["B"].pin_memory(), x["B_scale"].pin_memory(), guard[: w.M])
+        torch.cuda.synchronize()
+        _status_ok(p)
+    assert np.array_equal(guard[: w.M].numpy().view(np.uint16), ref)
+    assert bool((guard[w.M] == -1).all())
+    gu.assert_parity(ref, gu.oracle_full(x), f"hostpair tail={tail}")
+
+
+def test_automatic_cta_pair_choice():
+    """Automatic (default): the fused path on pairs only when the staging window
+    holds at least two pair tiles per resident pair (the 8 x 8192^3 benchmark
+    problem: 256), never the unfused path; the 2048-row problem's window holds
+    32 and stays on single CTAs."""
+    for idx, fused_pair in ((3, 1), (1, 0)):
+        w = inputs.workload(idx)
+        with _plan(w) as p:
+            assert p.get_option(mxa2a.MXA2A_OPT_CTA_PAIR) == 2
+            assert p.get_option(mxa2a.MXA2A_INFO_CTA_PAIR) == fused_pair, w.name
+            assert p.get_option(mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED) == 0, w.name
+
+
 def test_host_entry_pinned_output_with_tail_split():
     """The tail split's sums write a pinned C through its device view: the
     same bits as the device run (whose tail is split too), nothing past M x N."""
