@@ -273,11 +273,15 @@ void derive(mxa2a_plan* p) {
         // Default (option 0): half the ring's steps, so that the other half can be
         // staged while a group is read (measured on the 8192^3 workload on GB300:
         // DRAM reads 1.07 GB -> 0.39 GB per launch, 2-4 % faster).
+        // The CTA-pair kernel's m rows are pairs of m-tiles: the same rule in
+        // units of 256 rows (commMSize a multiple of 256).
+        const int row_f = p->pair_fused ? 2 * BM : BM;
         int g = p->group_fused_opt;
         if (g == 0 && p->cm % BM == 0) g = std::max(1, p->bn / 2) * (int)(p->cm / BM);
-        if (g > 1 && !p->pair_fused && p->cm % BM == 0) {
-            const int tps = (int)(p->cm / BM);                       // m-tiles per step
-            const int ring = (int)((int64_t)p->bn * p->cm / BM);     // m-tiles in the ring
+        if (p->pair_fused) g /= 2;
+        if (g > 1 && p->cm % row_f == 0) {
+            const int tps = (int)(p->cm / row_f);                       // m rows per step
+            const int ring = (int)((int64_t)p->bn * p->cm / row_f);     // m rows in the ring
             int gg = 1;
             if (g <= tps) {
                 for (int d = g; d >= 1; --d)
@@ -285,7 +289,7 @@ void derive(mxa2a_plan* p) {
             } else {
                 gg = std::min(g / tps, ring / tps) * tps;
             }
-            p->group_fused = std::max(1, std::min(gg, p->Mt));
+            p->group_fused = std::max(1, std::min(gg, p->pair_fused ? p->Mt / 2 : p->Mt));
         }
     }
     // Staging copy chunk: the largest divisor of commMSize rows within the

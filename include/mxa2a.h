@@ -374,8 +374,9 @@ enum mxa2a_option {
                                       one step; 1: m-tile by m-tile).  Rounded to a divisor of a
                                       staging step's m-tiles, or to a multiple of them within the
                                       ring's rows (buffer_num * commMSize); ignored when commMSize is
-                                      not a multiple of 128 or with the CTA-pair kernel (the planner's
-                                      choice: MXA2A_INFO_GROUP_FUSED) */
+                                      not a multiple of 128 (with the CTA-pair kernel: 256, the group
+                                      then counted in pairs of m-tiles) (the planner's choice:
+                                      MXA2A_INFO_GROUP_FUSED, in m rows) */
     MXA2A_OPT_TAIL_SPLIT = 18,     /* 1 (default): when a path's tiles fill the persistent grid (its CTAs,
                                       or CTA pairs) more than once and the last round holds at most half
                                       the grid's worth, split that round's tiles in two along K (R even,

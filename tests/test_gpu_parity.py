@@ -335,6 +335,25 @@ def test_fused_raster_groups_same_bits(group):
     assert np.array_equal(got, ref)
 
 
+@pytest.mark.parametrize("group", [0, 1, 2, 4, 8, 16])
+def test_fused_raster_groups_cta_pair(group):
+    """The same with the CTA-pair kernel, whose groups count pairs of m-tiles
+    (one per staging step here, 4 in the ring; the request in m-tiles halved)."""
+    w = inputs.Workload("fgrouppair", 4, 2048, 256, 1040, 256, 4, 93)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w, split_k=1, cta_pair=1) as p:
+        ref = gu.host_bits(gu.run_gpu(p, d, w.M, w.N, fused=False))
+        p.set_option(mxa2a.MXA2A_OPT_GROUP_FUSED, group)
+        assert p.get_option(mxa2a.MXA2A_INFO_CTA_PAIR) == 1
+        want = {0: 2, 1: 1, 2: 1, 4: 2, 8: 4, 16: 4}[group]
+        assert p.get_option(mxa2a.MXA2A_INFO_GROUP_FUSED) == want
+        got = gu.host_bits(gu.run_gpu(p, d, w.M, w.N))
+        torch.cuda.synchronize()
+        _status_ok(p)
+    assert np.array_equal(got, ref)
+
+
 def test_step_credit_options_validated():
     w = inputs.workload(0)
     with _plan(w) as p:
