@@ -691,6 +691,30 @@ def test_host_entry_pinned_output_cta_pair(tail):
     gu.assert_parity(ref, gu.oracle_full(x), f"hostpair tail={tail}")
 
 
+def test_host_entry_automatic_pairs_run_single_cta():
+    """A plan whose fused path is automatically on CTA pairs runs a pinned-C
+    host call on single CTAs (the host link bounds it) and keeps its choice:
+    the device run's bits (no tail split on either kernel here)."""
+    w = inputs.Workload("hostauto", 2, 512, 4096, 400, 128, 4, 111)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with _plan(w, grid=4, split_k=1) as p:
+        assert p.get_option(mxa2a.MXA2A_INFO_CTA_PAIR) == 1
+        ref = gu.host_bits(gu.run_gpu(p, d, w.M, w.N))
+        hA = [a.pin_memory() for a in x["A_seg"]]
+        hS = [a.pin_memory() for a in x["A_scale_seg"]]
+        hC = torch.full((w.M, w.N), -1, dtype=torch.int16).pin_memory()
+        p.run_host(hA, hS, x["B"].pin_memory(), x["B_scale"].pin_memory(), hC)
+        torch.cuda.synchronize()
+        _status_ok(p)
+        assert p.get_option(mxa2a.MXA2A_INFO_CTA_PAIR) == 1
+        again = gu.host_bits(gu.run_gpu(p, d, w.M, w.N))
+        torch.cuda.synchronize()
+    assert np.array_equal(hC.numpy().view(np.uint16), ref)
+    assert np.array_equal(again, ref)
+    gu.assert_parity(ref, gu.oracle_full(x), "hostauto")
+
+
 def test_automatic_cta_pair_choice():
     """Automatic (default): the fused path on pairs only when the staging window
     holds at least two pair tiles per resident pair (the 8 x 8192^3 benchmark
