@@ -307,8 +307,11 @@ int mxa2a_run_unfused(mxa2a_plan *plan, const void *const *A_seg, const void *co
  * the fused kernel's staging copies (the exchange then comes from host
  * memory), pinned B and B_scale are copied by the SMs in one launch, and a
  * pinned C is written by the GEMM's epilogue itself, tile by tile, while the
- * GEMM runs; pageable buffers go through one DMA copy each.  The host buffers must stay unchanged until the stream has
- * passed the run.  Errors as for mxa2a_run.
+ * GEMM runs; pageable buffers go through one DMA copy each.  With a pinned C
+ * a plan whose fused path is on CTA pairs by the automatic choice
+ * (MXA2A_OPT_CTA_PAIR = 2) runs this call on single CTAs, the host link
+ * being the bound; the plan keeps its choice.  The host buffers must stay
+ * unchanged until the stream has passed the run.  Errors as for mxa2a_run.
  * Passage: all_to_all_matmul.cpp (the launcher), InitData and the
  * aclrtMemcpy calls that move the inputs to the device before the launch and
  * the output back after it.
