@@ -1041,54 +1041,15 @@ int mxa2a_get_status(mxa2a_plan* p, mxa2a_status* out) {
     return MXA2A_OK;
 }
 
-int mxa2a_set_option(mxa2a_plan* p, int key, int64_t v) {
-    if (!p) return MXA2A_ERR_NULL_PTR;
+namespace {
+// The options that change the plan's derived choices (validated, stored; the
+// caller derives the plan again).  Not one of them: MXA2A_ERR_INVALID_OPTION.
+int set_planner_option(mxa2a_plan* p, int key, int64_t v) {
     switch (key) {
-        case MXA2A_OPT_TIMEOUT_NS:
-            if (v < 1000) return MXA2A_ERR_INVALID_OPTION;
-            p->timeout_ns = v;
-            return MXA2A_OK;
         case MXA2A_OPT_SPLIT_K:
             if (v < 0 || v > p->R) return MXA2A_ERR_INVALID_OPTION;
             p->force_split = (int)v;
             break;
-        case MXA2A_OPT_ZIGZAG:
-            if (v != 0 && v != 1) return MXA2A_ERR_INVALID_OPTION;
-            p->zigzag = (int)v;
-            return MXA2A_OK;
-        case MXA2A_OPT_ROTATE:
-            if (v != 0 && v != 1) return MXA2A_ERR_INVALID_OPTION;
-            p->rotate = (int)v;
-            return MXA2A_OK;
-        case MXA2A_OPT_RECORD_EVENTS:
-            if (v < 0 || v > mxa2a_plan::kEvRing) return MXA2A_ERR_INVALID_OPTION;
-            if (v > p->ev_count) {
-                if (!p->ev0) {
-                    p->ev0 = new (std::nothrow) cudaEvent_t[mxa2a_plan::kEvRing]();
-                    p->ev1 = new (std::nothrow) cudaEvent_t[mxa2a_plan::kEvRing]();
-                    if (!p->ev0 || !p->ev1) return MXA2A_ERR_CUDA;
-                }
-                for (int i = p->ev_count; i < v; ++i) {
-                    if (cudaEventCreate(&p->ev0[i]) != cudaSuccess) return MXA2A_ERR_CUDA;
-                    if (cudaEventCreate(&p->ev1[i]) != cudaSuccess) {
-                        cudaEventDestroy(p->ev0[i]);
-                        return MXA2A_ERR_CUDA;
-                    }
-                    p->ev_count = i + 1;
-                }
-            }
-            p->record_events = (int)v;
-            p->ev_recorded = 0;
-            return MXA2A_OK;
-        case MXA2A_OPT_EXCHANGE_ONLY:
-            if (v != 0 && v != 1) return MXA2A_ERR_INVALID_OPTION;
-            if (v == 1 && p->bn < p->steps) return MXA2A_ERR_INVALID_OPTION;
-            p->exchange_only = (int)v;
-            return MXA2A_OK;
-        case MXA2A_OPT_FAULT_SKIP_STEP:
-            if (v < -1 || v >= p->steps) return MXA2A_ERR_INVALID_OPTION;
-            p->fault_skip_step = (int)v;
-            return MXA2A_OK;
         case MXA2A_OPT_GRID:
             if (v < 0) return MXA2A_ERR_INVALID_OPTION;
             p->grid_cap = (int)v;
@@ -1132,12 +1093,11 @@ int mxa2a_set_option(mxa2a_plan* p, int key, int64_t v) {
         default:
             return MXA2A_ERR_INVALID_OPTION;
     }
-    derive(p);
-    return ensure_partials(p);
+    return MXA2A_OK;
 }
 
-int mxa2a_get_option(mxa2a_plan* p, int key, int64_t* v) {
-    if (!p || !v) return MXA2A_ERR_NULL_PTR;
+// A plan fact or option value (the body of mxa2a_get_option).
+int plan_get(const mxa2a_plan* p, int key, int64_t* v) {
     switch (key) {
         case MXA2A_OPT_TIMEOUT_NS: *v = p->timeout_ns; break;
         case MXA2A_OPT_SPLIT_K: *v = p->force_split; break;
@@ -1179,6 +1139,103 @@ int mxa2a_get_option(mxa2a_plan* p, int key, int64_t* v) {
         case MXA2A_INFO_SM_COUNT: *v = p->sm_count; break;
         case MXA2A_INFO_LAUNCHES: *v = p->last_launches; break;
         default: return MXA2A_ERR_INVALID_OPTION;
+    }
+    return MXA2A_OK;
+}
+}  // namespace
+
+int mxa2a_set_option(mxa2a_plan* p, int key, int64_t v) {
+    if (!p) return MXA2A_ERR_NULL_PTR;
+    switch (key) {
+        case MXA2A_OPT_TIMEOUT_NS:
+            if (v < 1000) return MXA2A_ERR_INVALID_OPTION;
+            p->timeout_ns = v;
+            return MXA2A_OK;
+        case MXA2A_OPT_ZIGZAG:
+            if (v != 0 && v != 1) return MXA2A_ERR_INVALID_OPTION;
+            p->zigzag = (int)v;
+            return MXA2A_OK;
+        case MXA2A_OPT_ROTATE:
+            if (v != 0 && v != 1) return MXA2A_ERR_INVALID_OPTION;
+            p->rotate = (int)v;
+            return MXA2A_OK;
+        case MXA2A_OPT_RECORD_EVENTS:
+            if (v < 0 || v > mxa2a_plan::kEvRing) return MXA2A_ERR_INVALID_OPTION;
+            if (v > p->ev_count) {
+                if (!p->ev0) {
+                    p->ev0 = new (std::nothrow) cudaEvent_t[mxa2a_plan::kEvRing]();
+                    p->ev1 = new (std::nothrow) cudaEvent_t[mxa2a_plan::kEvRing]();
+                    if (!p->ev0 || !p->ev1) return MXA2A_ERR_CUDA;
+                }
+                for (int i = p->ev_count; i < v; ++i) {
+                    if (cudaEventCreate(&p->ev0[i]) != cudaSuccess) return MXA2A_ERR_CUDA;
+                    if (cudaEventCreate(&p->ev1[i]) != cudaSuccess) {
+                        cudaEventDestroy(p->ev0[i]);
+                        return MXA2A_ERR_CUDA;
+                    }
+                    p->ev_count = i + 1;
+                }
+            }
+            p->record_events = (int)v;
+            p->ev_recorded = 0;
+            return MXA2A_OK;
+        case MXA2A_OPT_EXCHANGE_ONLY:
+            if (v != 0 && v != 1) return MXA2A_ERR_INVALID_OPTION;
+            if (v == 1 && p->bn < p->steps) return MXA2A_ERR_INVALID_OPTION;
+            p->exchange_only = (int)v;
+            return MXA2A_OK;
+        case MXA2A_OPT_FAULT_SKIP_STEP:
+            if (v < -1 || v >= p->steps) return MXA2A_ERR_INVALID_OPTION;
+            p->fault_skip_step = (int)v;
+            return MXA2A_OK;
+        default: {
+            const int rc = set_planner_option(p, key, v);
+            if (rc) return rc;
+        }
+    }
+    derive(p);
+    return ensure_partials(p);
+}
+
+int mxa2a_get_option(mxa2a_plan* p, int key, int64_t* v) {
+    if (!p || !v) return MXA2A_ERR_NULL_PTR;
+    return plan_get(p, key, v);
+}
+
+int mxa2a_plan_preview(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t commMSize, int buffer_num,
+                       int sm_count, int max_pairs_fused, int max_pairs_unfused, const int* opt_keys,
+                       const int64_t* opt_values, int n_opts, const int* info_keys, int64_t* info_values,
+                       int n_info) {
+    const int shape = mxa2a_validate(R, M, kPerRank, N, commMSize, buffer_num);
+    if (shape) return shape;
+    if (sm_count < 1 || max_pairs_fused < 0 || max_pairs_unfused < 0 || n_opts < 0 || n_info < 0)
+        return MXA2A_ERR_INVALID_OPTION;
+    if ((n_opts > 0 && (!opt_keys || !opt_values)) || (n_info > 0 && (!info_keys || !info_values)))
+        return MXA2A_ERR_NULL_PTR;
+    mxa2a_plan p;   // fields only: the same derivation as a created plan's
+    p.R = R;
+    p.kind = MXA2A_KIND_ALLTOALL;
+    p.nseg = R;
+    p.M = M;
+    p.ka = kPerRank;
+    p.N = N;
+    p.cm = commMSize;
+    p.bn = buffer_num;
+    p.device = -1;
+    p.sm_count = sm_count;
+    p.max_pairs_fused = max_pairs_fused;
+    p.max_pairs_unfused = max_pairs_unfused;
+    derive(&p);
+    for (int i = 0; i < n_opts; ++i) {
+        const int rc = set_planner_option(&p, opt_keys[i], opt_values[i]);
+        if (rc) return rc;
+        derive(&p);
+    }
+    for (int i = 0; i < n_info; ++i) {
+        if (info_keys[i] == MXA2A_INFO_WORKSPACE_BYTES || info_keys[i] == MXA2A_INFO_LAUNCHES)
+            return MXA2A_ERR_INVALID_OPTION;
+        const int rc = plan_get(&p, info_keys[i], &info_values[i]);
+        if (rc) return rc;
     }
     return MXA2A_OK;
 }

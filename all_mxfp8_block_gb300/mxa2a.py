@@ -120,6 +120,10 @@ _SIGS = [
     ("mxa2a_get_status", ctypes.c_int, [_VP, ctypes.POINTER(mxa2a_status)]),
     ("mxa2a_set_option", ctypes.c_int, [_VP, ctypes.c_int, _I64]),
     ("mxa2a_get_option", ctypes.c_int, [_VP, ctypes.c_int, ctypes.POINTER(_I64)]),
+    ("mxa2a_plan_preview", ctypes.c_int, [ctypes.c_int, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                          ctypes.POINTER(_I64), ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                          ctypes.POINTER(_I64), ctypes.c_int]),
     ("mxa2a_last_kernel_ms", ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_float)]),
     ("mxa2a_kernel_times", ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_float), ctypes.c_int,
                                           ctypes.POINTER(ctypes.c_int)]),
@@ -189,6 +193,30 @@ def _check(rc: int, what: str):
 # --- the C functions, same names ------------------------------------------------
 def mxa2a_validate(R, M, kPerRank, N, commMSize, buffer_num) -> int:
     return load().mxa2a_validate(R, M, kPerRank, N, commMSize, buffer_num)
+
+
+def mxa2a_plan_preview(R, M, kPerRank, N, commMSize, buffer_num, sm_count, max_pairs_fused, max_pairs_unfused,
+                       options, keys) -> dict:
+    """The planner's choices on the host, no device.  options: (MXA2A_OPT_*
+    key, value) pairs applied in order; keys: the MXA2A_INFO_* / MXA2A_OPT_*
+    keys to read.  Returns {key: value}."""
+    opts = list(options)
+    ok = (ctypes.c_int * max(1, len(opts)))(*[k for k, _ in opts])
+    ov = (_I64 * max(1, len(opts)))(*[v for _, v in opts])
+    keys = list(keys)
+    ik = (ctypes.c_int * max(1, len(keys)))(*keys)
+    iv = (_I64 * max(1, len(keys)))()
+    _check(load().mxa2a_plan_preview(R, M, kPerRank, N, commMSize, buffer_num, sm_count, max_pairs_fused,
+                                     max_pairs_unfused, ok, ov, len(opts), ik, iv, len(keys)),
+           "mxa2a_plan_preview")
+    return {k: int(iv[i]) for i, k in enumerate(keys)}
+
+
+def plan_preview(R, M, kPerRank, N, commMSize, buffer_num, keys, options=(), sm_count=152, max_pairs_fused=76,
+                 max_pairs_unfused=76) -> dict:
+    """mxa2a_plan_preview with a GB300's SM and pair counts by default."""
+    return mxa2a_plan_preview(R, M, kPerRank, N, commMSize, buffer_num, sm_count, max_pairs_fused,
+                              max_pairs_unfused, options, keys)
 
 
 def mxa2a_create(R, M, kPerRank, N, commMSize, buffer_num) -> int:

@@ -425,6 +425,26 @@ enum mxa2a_option {
 int mxa2a_set_option(mxa2a_plan *plan, int key, int64_t value);
 int mxa2a_get_option(mxa2a_plan *plan, int key, int64_t *value);
 
+/* The planner alone, on the host (no device, nothing allocated): the choices
+ * an all-to-all plan of this shape would make on a device with sm_count SMs
+ * on which max_pairs_fused / max_pairs_unfused CTA pairs of the fused /
+ * unfused pair kernel fit at once (a GB300: 152, 76, 76), with the planner
+ * options opt_keys[i] = opt_values[i] (i < n_opts; MXA2A_OPT_SPLIT_K, _GRID,
+ * _CHUNK_BYTES, _CTA_PAIR, _GROUP_M, _TILE_N, _ELEM_TYPES, _STEP_CREDITS,
+ * _COPY_SKEW_NS, _GROUP_FUSED, _TAIL_SPLIT) applied in order.  Writes
+ * info_values[i] = the value mxa2a_get_option would give for info_keys[i]
+ * (i < n_info; any MXA2A_INFO_* or MXA2A_OPT_* key but MXA2A_INFO_WORKSPACE_BYTES
+ * and MXA2A_INFO_LAUNCHES).  Returns the shape's mxa2a_validate code,
+ * MXA2A_ERR_NULL_PTR for a missing array, MXA2A_ERR_INVALID_OPTION for a bad
+ * device description, option or key (the outputs then partly written).
+ * Passage: the performance optimisation guide, section 1.2 (fill all cores:
+ * flattening and splitting the tiles over the cores), whose rules the planner
+ * applies; it is how those rules are checked without a device. */
+int mxa2a_plan_preview(int R, int64_t M, int64_t kPerRank, int64_t N, int64_t commMSize, int buffer_num,
+                       int sm_count, int max_pairs_fused, int max_pairs_unfused, const int *opt_keys,
+                       const int64_t *opt_values, int n_opts, const int *info_keys, int64_t *info_values,
+                       int n_info);
+
 /* Duration of the main GEMM kernel of the last run, in ms (needs
  * MXA2A_OPT_RECORD_EVENTS >= 1; synchronises on that run's end event).
  * Passage: all_to_all_matmul.cpp (the launcher), perf mode: the main kernel
