@@ -739,6 +739,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=str(DEFAULT_WORKLOAD))
+    ap.add_argument("--shape", default="",
+                    help="R,M,kPerRank,N,commMSize,buffer_num[,seed]: a synthetic problem of these sizes instead of "
+                         "--workload (the benchmark problems' input recipe), e.g. a smaller case to profile")
     ap.add_argument("--path", choices=["fused", "unfused"], default="fused")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -763,7 +766,14 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from all_mxfp8_block_gb300 import inputs
-    w = inputs.workload(int(args.workload)) if args.workload.isdigit() else inputs.workload(args.workload)
+    if args.shape:
+        v = [int(s) for s in args.shape.split(",")]
+        if len(v) not in (6, 7):
+            ap.error("--shape wants R,M,kPerRank,N,commMSize,buffer_num[,seed]")
+        R, M, ka, N, cm, bn = v[:6]
+        w = inputs.Workload(f"r{R}_m{M}_k{R * ka}_n{N}", R, M, ka, N, cm, bn, v[6] if len(v) == 7 else 0)
+    else:
+        w = inputs.workload(int(args.workload)) if args.workload.isdigit() else inputs.workload(args.workload)
     if args.impl == "reference":
         return run_reference(args, w)
     if args.only_siblings:
