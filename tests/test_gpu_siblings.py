@@ -117,6 +117,32 @@ def test_allgather_full_size_sampled():
     assert np.array_equal(whole_f, whole_u)
 
 
+@pytest.mark.parametrize("split,grid", [(2, 0), (1, 6)])
+def test_allgather_split_items(split, grid):
+    """The all-gather's split items, whose K ranges are column ranges of every
+    row block: a uniform split in two (all paths the same bits), and the tail
+    split (8 tiles, K = 8192, on 6 CTAs: the last 2 split in two); against the
+    oracle."""
+    w = inputs.AllGatherWorkload("ag_split", 2, 256, 8192, 400, 64, 4, 31)
+    x = inputs.make_allgather_inputs(w)
+    dev = _ag_dev(x)
+    ref = oracle.gemm_allgather(x["A_blk"], x["A_scale_blk"], x["B"], x["B_scale"])
+    opts = dict(split_k=split)
+    if grid:
+        opts["grid"] = grid
+    with _ag_plan(w, **opts) as p:
+        if split == 2:
+            assert p.get_option(mxa2a.MXA2A_INFO_SPLITS) == 2
+        else:
+            assert p.get_option(mxa2a.MXA2A_INFO_TAIL_SPLIT) == 2
+            assert p.get_option(mxa2a.MXA2A_INFO_TAIL_SPLIT_UNFUSED) == 2
+        got = {path: _ag_run(p, dev, w.M, w.N, path) for path in ("fused", "unfused", "direct")}
+    for path, bits in got.items():
+        gu.assert_parity(bits, ref, f"allgather split={split} grid={grid} {path}")
+    if split == 2:
+        assert np.array_equal(got["fused"], got["unfused"]) and np.array_equal(got["fused"], got["direct"])
+
+
 def test_allgather_host_entry_and_new_block_pointers():
     w = inputs.AG_WORKLOADS[0]
     x1 = inputs.make_allgather_inputs(w)
