@@ -133,6 +133,17 @@ def test_other_element_formats_against_oracle(a_fmt, b_fmt, fused):
     _check_full(w, fused=fused, elem_types=mxa2a.ELEM_TYPES[(a_fmt, b_fmt)])
 
 
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("a_fmt,b_fmt", ELEM_PAIRS)
+def test_other_element_formats_cta_pair(a_fmt, b_fmt, fused):
+    """The same on the CTA-pair kernel (its idesc takes the element types too;
+    the fused path's default on large problems), against the oracle."""
+    w = inputs.Workload("fmtpair", 3, 512, 256, 528, 128, 4, 99, a_fmt=a_fmt, b_fmt=b_fmt)
+    with _plan(w, cta_pair=1) as p:
+        assert p.get_option(mxa2a.MXA2A_INFO_CTA_PAIR if fused else mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED) == 1
+    _check_full(w, fused=fused, cta_pair=1, elem_types=mxa2a.ELEM_TYPES[(a_fmt, b_fmt)])
+
+
 @pytest.mark.parametrize("M", [128, 256])
 def test_scale_factors_per_block_and_column(M):
     """One-hot B with varied B scales per 32-block and column: exercises every
