@@ -530,13 +530,16 @@ def test_unfused_raster_groups_same_bits():
 
 
 @pytest.mark.parametrize("fused", [True, False])
-def test_cuda_graph_replay_matches_eager(fused):
+@pytest.mark.parametrize("pair", [0, 1])
+def test_cuda_graph_replay_matches_eager(fused, pair):
     """A run captured into a CUDA graph and replayed gives the eager run's bits
-    (the flags reset themselves at the end of every launch)."""
-    w = inputs.Workload("graph", 2, 256, 256, 512, 64, 2, 83)
+    (the flags, and the CTA-pair kernel's inline B-scale pack count, reset
+    themselves at the end of every launch)."""
+    w = inputs.Workload("graph", 2, 256, 256, 512, 128, 2, 83)
     x = inputs.make_inputs(w)
     d = gu.to_device(x)
-    with _plan(w, split_k=1) as p:
+    with _plan(w, split_k=1, cta_pair=pair) as p:
+        assert p.get_option(mxa2a.MXA2A_INFO_CTA_PAIR if fused else mxa2a.MXA2A_INFO_CTA_PAIR_UNFUSED) == pair
         eager = gu.host_bits(gu.run_gpu(p, d, w.M, w.N, fused=fused))
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
@@ -551,7 +554,7 @@ def test_cuda_graph_replay_matches_eager(fused):
             torch.cuda.synchronize()
             assert np.array_equal(gu.host_bits(C), eager)
         _status_ok(p)
-    gu.assert_parity(eager, gu.oracle_full(x), f"graph fused={fused}")
+    gu.assert_parity(eager, gu.oracle_full(x), f"graph fused={fused} pair={pair}")
 
 
 def test_cuda_graph_capture_leaves_the_tail_whole():
