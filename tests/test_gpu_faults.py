@@ -47,6 +47,33 @@ def test_lost_staging_signal_times_out_then_recovers(split, skip):
     gu.assert_parity(got, gu.oracle_full(x), f"after recovery split={split} skip={skip}")
 
 
+def test_lost_staging_signal_cta_pair():
+    """The same on the fused CTA-pair kernel: both CTAs of every pair give up
+    through their bounded waits, the even CTA completes the stages only one of
+    them armed or loaded, both meet at the cluster barriers, and the next run
+    on the plan is correct."""
+    w = inputs.Workload("faultpair", 2, 512, 256, 512, 128, 2, 57)
+    x = inputs.make_inputs(w)
+    d = gu.to_device(x)
+    with mxa2a.Plan(w.R, w.M, w.kPerRank, w.N, w.commMSize, w.buffer_num) as p:
+        p.set_option(mxa2a.MXA2A_OPT_TIMEOUT_NS, 100_000_000)
+        p.set_option(mxa2a.MXA2A_OPT_CTA_PAIR, 1)
+        p.set_option(mxa2a.MXA2A_OPT_SPLIT_K, 1)
+        assert p.get_option(mxa2a.MXA2A_INFO_CTA_PAIR) == 1
+        p.set_option(mxa2a.MXA2A_OPT_FAULT_SKIP_STEP, 3)
+        gu.run_gpu(p, d, w.M, w.N)
+        torch.cuda.synchronize()
+        st = p.status()
+        assert st["code"] == mxa2a.MXA2A_ERR_TIMEOUT, st
+        assert np.all(p.read_workspace(mxa2a.MXA2A_WS_FLAGS).view(np.uint64) == 0)
+        p.set_option(mxa2a.MXA2A_OPT_FAULT_SKIP_STEP, -1)
+        C = gu.run_gpu(p, d, w.M, w.N)
+        torch.cuda.synchronize()
+        assert p.status()["code"] == 0
+        got = gu.host_bits(C)
+    gu.assert_parity(got, gu.oracle_full(x), "after recovery, CTA pairs")
+
+
 def test_status_is_clean_after_normal_runs():
     w = inputs.workload(0)
     x = inputs.make_inputs(w)
